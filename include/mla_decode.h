@@ -1,0 +1,175 @@
+/*
+ * mla_decode.h -- C ABI of the GB300 (sm_103a) MLA decode library.
+ *
+ * The operation is DeepSeek-R1 forward_absorb Multi-head Latent Attention
+ * decode as stated on kernelbot-amd-mixed-mla-675627 ("MLA decode kernel --
+ * submission template", the module docstring: config block, KV buffer format,
+ * input tuple and output; the naive reference `custom_kernel_bf16` gives the
+ * arithmetic):
+ *
+ *   for each batch entry b, query token t in [qo_indptr[b], qo_indptr[b+1]),
+ *   head h in [0,16):
+ *     s_j      = sm_scale * <q[t,h,0:576], K_j>,   K_j = dequant(kv[j, 0:576])
+ *     out[t,h] = sum_j softmax_j(s) * V_j,          V_j = K_j[0:512]
+ *   for j in [kv_indptr[b], kv_indptr[b+1]).
+ *
+ * All query tokens of a segment attend to all of its KV rows (no causal
+ * mask); a segment with no KV rows yields zeros. The computation is split-K
+ * flash decoding: the KV rows of all segments are partitioned evenly over
+ * `num_splits` CTAs (stage 1: fused QK^T + online softmax + PV with fp8/mxfp4
+ * dequantisation in the operand path), and per-split partial outputs are merged
+ * with LSE weights (stage 2), as in kernelbot-amd-mixed-mla-753817
+ * (module docstring, `mla_flash_decode_stage1`, `mla_flash_decode_stage2`).
+ *
+ * Conventions for every entry point:
+ *   - Pointers named d_* or documented "device" are CUDA device pointers that
+ *     the caller owns; the library never frees or retains them. Host pointers
+ *     are documented as such.
+ *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default stream).
+ *   - Calls that launch work are asynchronous: MLA_OK means "enqueued". A launch
+ *     failure returns MLA_ERR_CUDA. No call synchronises unless documented.
+ *   - The library allocates no device memory per call. It keeps only a cached
+ *     per-device SM count and the kernels' shared-memory attributes.
+ *   - No C++ exception crosses this interface.
+ */
+#ifndef MLA_DECODE_H
+#define MLA_DECODE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define MLA_NUM_HEADS 16   /* query heads (after tensor-parallel split)         */
+#define MLA_D_QK 576       /* kv_lora_rank 512 + qk_rope_head_dim 64            */
+#define MLA_D_V 512        /* v_head_dim = kv_lora_rank                         */
+#define MLA_MX_BLOCK 32    /* elements per e8m0 scale in the mxfp4 KV cache     */
+
+/* Storage formats. kernelbot-amd-mixed-mla-675627, input tuple: kv_data holds
+ * "bf16", "fp8" (per-tensor scale) and "mxfp4" (fp4x2 + fp8_e8m0 scale).      */
+typedef enum {
+  MLA_DTYPE_BF16 = 0,     /* bfloat16                                           */
+  MLA_DTYPE_FP8_E4M3 = 1, /* OCP e4m3fn codes, value = code * per-tensor scale  */
+  MLA_DTYPE_MXFP4 = 2     /* OCP MX: e2m1 nibbles (element 2i low, 2i+1 high),
+                             one e8m0 scale 2^(e-127) per 32 elements           */
+} mla_dtype_t;
+
+typedef enum {
+  MLA_OK = 0,
+  MLA_ERR_INVALID_ARG = 1,  /* null pointer, bad size, misaligned pointer      */
+  MLA_ERR_UNSUPPORTED = 2,  /* a dtype combination the library does not have  */
+  MLA_ERR_WORKSPACE = 3,    /* workspace missing or smaller than required     */
+  MLA_ERR_CUDA = 4,         /* a CUDA runtime call failed                     */
+  MLA_ERR_TIMEOUT = 5,      /* device flag: a bounded wait in a kernel expired */
+  MLA_ERR_DEVICE_CHECK = 6  /* device flag: indptr arrays failed the kernels'
+                               bounds/monotonicity checks; work was skipped   */
+} mla_status_t;
+
+/* Device error flags, as returned by mla_get_device_error().                  */
+#define MLA_DEVFLAG_TIMEOUT 0x1u
+#define MLA_DEVFLAG_BAD_INDPTR 0x2u
+
+typedef struct {
+  int32_t batch;          /* number of segments = len(qo_indptr) - 1, >= 1         */
+  int32_t total_q;        /* rows of q and out (= qo_indptr[batch]), >= 0          */
+  int32_t total_kv;       /* rows of the KV cache (= kv_indptr[batch]), >= 0       */
+  float sm_scale;         /* softmax scale; <= 0 selects 1/sqrt(576)               */
+  mla_dtype_t q_dtype;    /* MLA_DTYPE_BF16, or MLA_DTYPE_FP8_E4M3 (a8w8)          */
+  const float* q_scale;   /* device, one float: q = code * q_scale; NULL unless
+                             q_dtype == MLA_DTYPE_FP8_E4M3                         */
+  int32_t num_splits;     /* KV partitions (stage-1 CTAs); 0 = use mla_plan()      */
+  void* workspace;        /* device scratch of mla_decode_workspace_size() bytes,
+                             256-byte aligned, owned by the caller                 */
+  size_t workspace_bytes;
+} mla_decode_opts;
+
+/* Split planner (the pages choose the split count from batch size and KV
+ * length: kernelbot-amd-mixed-mla-586148 "Adaptive split-K", -753817
+ * `_choose_kv_splits`, -739756 `_get_config`). Here the KV rows of all
+ * segments are divided evenly over the CTAs, so the planner picks only how
+ * many partitions to use: enough to fill the GPU (`sm_count` SMs, one CTA
+ * each), but no partition smaller than a few tiles. Host only; no device
+ * access. sm_count <= 0 queries the current device.
+ * Writes the partition count to *num_splits. Errors: MLA_ERR_INVALID_ARG for
+ * negative sizes or a NULL output.                                           */
+mla_status_t mla_plan(int32_t batch, int32_t total_q, int32_t total_kv, mla_dtype_t kv_dtype,
+                      int32_t sm_count, int32_t* num_splits);
+
+/* Bytes of device workspace that mla_decode() needs for these sizes and this
+ * partition count (0 = what mla_plan() would choose on the current device).
+ * The workspace holds a 256-byte header (the device error flags) and the
+ * per-split partial outputs: (num_splits + total_q) slots of 16x512 fp32 plus
+ * 16 fp32 LSE values. Host only.                                              */
+mla_status_t mla_decode_workspace_size(int32_t batch, int32_t total_q, int32_t total_kv,
+                                       mla_dtype_t kv_dtype, int32_t num_splits, size_t* bytes);
+
+/* The decode.
+ *   q         device, [total_q][16][576] bf16, or e4m3 codes when
+ *             opts->q_dtype == MLA_DTYPE_FP8_E4M3; 16-byte aligned
+ *   kv        device, [total_kv][576] bf16 / e4m3 codes, or [total_kv][288]
+ *             fp4x2 bytes for mxfp4; 16-byte aligned
+ *   kv_scale  device: NULL (bf16), one float (fp8), or [total_kv][18] e8m0
+ *             bytes (mxfp4)
+ *   qo_indptr, kv_indptr  device int32 [batch+1]: monotone, [0] = 0,
+ *             qo_indptr[batch] = total_q, kv_indptr[batch] = total_kv. The
+ *             kernels check this and, on a violation, skip the work and set
+ *             MLA_DEVFLAG_BAD_INDPTR (no out-of-bounds access).
+ *   out       device, [total_q][16][512] bf16 (round to nearest even)
+ * Errors: MLA_ERR_INVALID_ARG (NULL/misaligned pointers, bad sizes),
+ * MLA_ERR_UNSUPPORTED (dtype combination), MLA_ERR_WORKSPACE (too small),
+ * MLA_ERR_CUDA (launch failed). Asynchronous on `stream`.                     */
+mla_status_t mla_decode(const void* q, const void* kv, const void* kv_scale,
+                        const int32_t* qo_indptr, const int32_t* kv_indptr, void* out,
+                        mla_dtype_t kv_dtype, const mla_decode_opts* opts, void* stream);
+
+/* Device buffers (caller-owned) that mla_decode_from_host() stages into.      */
+typedef struct {
+  void* q;             /* bytes of q                                        */
+  void* kv;            /* bytes of the KV cache                             */
+  void* kv_scale;      /* fp8: 4 bytes; mxfp4: total_kv*18 bytes; else NULL  */
+  float* q_scale;      /* 4 bytes when q is fp8, else NULL                  */
+  int32_t* qo_indptr;  /* batch+1 ints                                      */
+  int32_t* kv_indptr;  /* batch+1 ints                                      */
+  void* out;           /* total_q*16*512 bf16                               */
+} mla_device_buffers;
+
+/* The same decode from HOST buffers: enqueues one cudaMemcpyAsync per input
+ * (host -> the caller's device buffers), mla_decode(), and the copy of the
+ * output back to h_out. Host buffers should be pinned for the copies to be
+ * asynchronous. The call returns once everything is enqueued; synchronise
+ * `stream` before reading h_out. h_q_scale is a host float (fp8 q) or NULL;
+ * opts->q_scale is ignored (dev->q_scale is used).                            */
+mla_status_t mla_decode_from_host(const void* h_q, const void* h_kv, const void* h_kv_scale,
+                                  const float* h_q_scale, const int32_t* h_qo_indptr,
+                                  const int32_t* h_kv_indptr, void* h_out, mla_dtype_t kv_dtype,
+                                  const mla_decode_opts* opts, const mla_device_buffers* dev,
+                                  void* stream);
+
+/* Dequantisation through the decode kernels' own operand path: KV rows
+ * [row0, row0+nrows) are loaded and converted exactly as stage 1 does, pushed
+ * through the same tensor-core instruction against an identity operand, and
+ * written as fp32 to d_out [nrows][576]. The result equals the format's
+ * definition (code * scale) bit for bit wherever that value is representable.
+ * Asynchronous. Errors: MLA_ERR_INVALID_ARG.                                  */
+mla_status_t mla_dequant_rows(const void* kv, const void* kv_scale, mla_dtype_t kv_dtype,
+                              int32_t total_kv, int32_t row0, int32_t nrows, float* d_out,
+                              void* stream);
+
+/* Reads the device error flags that kernels set in `workspace` (OR of
+ * MLA_DEVFLAG_*). Synchronises `stream`. Returns MLA_OK, MLA_ERR_TIMEOUT or
+ * MLA_ERR_DEVICE_CHECK (timeout wins); *flags may be NULL.                    */
+mla_status_t mla_get_device_error(const void* workspace, void* stream, uint32_t* flags);
+
+/* Clears the device error flags (flags are sticky until cleared). Async.      */
+mla_status_t mla_reset_device_error(void* workspace, void* stream);
+
+/* Static description of a status code.                                        */
+const char* mla_status_string(mla_status_t status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MLA_DECODE_H */

@@ -1,0 +1,164 @@
+"""GB300 (sm_103a) MLA decode: Python binding of the C-ABI library.
+
+Every function here only marshals arguments to ``libmla_decode.so`` (declared
+in ``include/mla_decode.h``); all computation runs in the library's CUDA
+kernels. PyTorch is used for device memory and streams only. There is no CPU
+fallback: if the library is missing or fails to load, every call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+from .synth import BF16, D_QK, D_V, FP8_E4M3, HEADS, MXFP4  # noqa: F401  (dtype codes / sizes)
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libmla_decode.so")
+
+MLA_OK, MLA_ERR_INVALID_ARG, MLA_ERR_UNSUPPORTED, MLA_ERR_WORKSPACE = 0, 1, 2, 3
+MLA_ERR_CUDA, MLA_ERR_TIMEOUT, MLA_ERR_DEVICE_CHECK = 4, 5, 6
+DEVFLAG_TIMEOUT, DEVFLAG_BAD_INDPTR = 0x1, 0x2
+
+EXPORTED = ("mla_plan", "mla_decode_workspace_size", "mla_decode", "mla_decode_from_host", "mla_dequant_rows",
+            "mla_get_device_error", "mla_reset_device_error", "mla_status_string")
+
+
+class MlaError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: {status_string(status)}")
+
+
+class DecodeOpts(ctypes.Structure):
+    _fields_ = [("batch", ctypes.c_int32), ("total_q", ctypes.c_int32), ("total_kv", ctypes.c_int32),
+                ("sm_scale", ctypes.c_float), ("q_dtype", ctypes.c_int), ("q_scale", ctypes.c_void_p),
+                ("num_splits", ctypes.c_int32), ("workspace", ctypes.c_void_p), ("workspace_bytes", ctypes.c_size_t)]
+
+
+class DeviceBuffers(ctypes.Structure):
+    _fields_ = [("q", ctypes.c_void_p), ("kv", ctypes.c_void_p), ("kv_scale", ctypes.c_void_p),
+                ("q_scale", ctypes.c_void_p), ("qo_indptr", ctypes.c_void_p), ("kv_indptr", ctypes.c_void_p),
+                ("out", ctypes.c_void_p)]
+
+
+_lock = threading.Lock()
+_lib = None
+
+
+def library_path() -> str:
+    return LIB_PATH
+
+
+def lib():
+    """The loaded CUDA library (raises if it was not built)."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(LIB_PATH):
+                raise RuntimeError(f"{LIB_PATH} is missing: build it with "
+                                   "`python -m mla_decode_attention_split_gb300.build` (no CPU fallback exists)")
+            L = ctypes.CDLL(LIB_PATH)
+            P, i32, st = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int
+            L.mla_plan.argtypes = [i32, i32, i32, st, i32, ctypes.POINTER(i32)]
+            L.mla_decode_workspace_size.argtypes = [i32, i32, i32, st, i32, ctypes.POINTER(ctypes.c_size_t)]
+            L.mla_decode.argtypes = [P, P, P, P, P, P, st, ctypes.POINTER(DecodeOpts), P]
+            L.mla_decode_from_host.argtypes = [P, P, P, P, P, P, P, st, ctypes.POINTER(DecodeOpts),
+                                               ctypes.POINTER(DeviceBuffers), P]
+            L.mla_dequant_rows.argtypes = [P, P, st, i32, i32, i32, P, P]
+            L.mla_get_device_error.argtypes = [P, P, ctypes.POINTER(ctypes.c_uint32)]
+            L.mla_reset_device_error.argtypes = [P, P]
+            L.mla_status_string.argtypes = [st]
+            L.mla_status_string.restype = ctypes.c_char_p
+            for name in EXPORTED[:-1]:
+                getattr(L, name).restype = st
+            _lib = L
+    return _lib
+
+
+def status_string(status: int) -> str:
+    return lib().mla_status_string(int(status)).decode()
+
+
+def _check(status: int, where: str) -> None:
+    if status != MLA_OK:
+        raise MlaError(status, where)
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream_handle(stream):
+    if stream is None:
+        import torch
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(getattr(stream, "cuda_stream", stream) or 0)
+
+
+def plan(batch: int, total_q: int, total_kv: int, kv_dtype: int, sm_count: int = 0) -> int:
+    """Number of KV partitions (stage-1 CTAs) the library would use."""
+    out = ctypes.c_int32(0)
+    _check(lib().mla_plan(batch, total_q, total_kv, kv_dtype, sm_count, ctypes.byref(out)), "mla_plan")
+    return out.value
+
+
+def workspace_size(batch: int, total_q: int, total_kv: int, kv_dtype: int, num_splits: int = 0) -> int:
+    out = ctypes.c_size_t(0)
+    _check(lib().mla_decode_workspace_size(batch, total_q, total_kv, kv_dtype, num_splits, ctypes.byref(out)),
+           "mla_decode_workspace_size")
+    return out.value
+
+
+def alloc_workspace(batch: int, total_q: int, total_kv: int, kv_dtype: int, num_splits: int = 0, device="cuda"):
+    """A zeroed device workspace (torch uint8 tensor, 256-byte aligned by the caching allocator)."""
+    import torch
+    n = workspace_size(batch, total_q, total_kv, kv_dtype, num_splits)
+    return torch.zeros(n, dtype=torch.uint8, device=device)
+
+
+def make_opts(batch, total_q, total_kv, *, q_dtype=BF16, q_scale=None, sm_scale=0.0, num_splits=0,
+              workspace=None) -> DecodeOpts:
+    return DecodeOpts(batch=batch, total_q=total_q, total_kv=total_kv, sm_scale=float(sm_scale), q_dtype=q_dtype,
+                      q_scale=None if q_scale is None else q_scale.data_ptr(), num_splits=num_splits,
+                      workspace=None if workspace is None else workspace.data_ptr(),
+                      workspace_bytes=0 if workspace is None else workspace.numel() * workspace.element_size())
+
+
+def decode(q, kv, kv_scale, qo_indptr, kv_indptr, out, kv_dtype: int, *, workspace, q_dtype: int = BF16,
+           q_scale=None, sm_scale: float = 0.0, num_splits: int = 0, stream=None) -> None:
+    """mla_decode() on torch CUDA tensors (layouts as in mla_decode.h). Asynchronous."""
+    opts = make_opts(qo_indptr.numel() - 1, q.shape[0], kv.shape[0], q_dtype=q_dtype, q_scale=q_scale,
+                     sm_scale=sm_scale, num_splits=num_splits, workspace=workspace)
+    _check(lib().mla_decode(_ptr(q), _ptr(kv), _ptr(kv_scale), _ptr(qo_indptr), _ptr(kv_indptr), _ptr(out),
+                            kv_dtype, ctypes.byref(opts), _stream_handle(stream)), "mla_decode")
+
+
+def decode_from_host(h, dev, kv_dtype: int, *, q_dtype: int, workspace, sm_scale: float = 0.0,
+                     num_splits: int = 0, stream=None) -> None:
+    """mla_decode_from_host(): h and dev are dicts of (pinned host / device) torch tensors with keys
+    q, kv, kv_scale, q_scale, qo_indptr, kv_indptr, out. Asynchronous; synchronise before reading h['out']."""
+    opts = make_opts(h["qo_indptr"].numel() - 1, h["q"].shape[0], h["kv"].shape[0], q_dtype=q_dtype,
+                     sm_scale=sm_scale, num_splits=num_splits, workspace=workspace)
+    bufs = DeviceBuffers(**{k: (None if dev.get(k) is None else dev[k].data_ptr()) for k, _ in DeviceBuffers._fields_})
+    _check(lib().mla_decode_from_host(_ptr(h["q"]), _ptr(h["kv"]), _ptr(h.get("kv_scale")), _ptr(h.get("q_scale")),
+                                      _ptr(h["qo_indptr"]), _ptr(h["kv_indptr"]), _ptr(h["out"]), kv_dtype,
+                                      ctypes.byref(opts), ctypes.byref(bufs), _stream_handle(stream)),
+           "mla_decode_from_host")
+
+
+def dequant_rows(kv, kv_scale, kv_dtype: int, row0: int, nrows: int, out, stream=None) -> None:
+    """mla_dequant_rows(): rows [row0, row0+nrows) through the decode kernels' operand path -> out f32."""
+    _check(lib().mla_dequant_rows(_ptr(kv), _ptr(kv_scale), kv_dtype, kv.shape[0], row0, nrows, _ptr(out),
+                                  _stream_handle(stream)), "mla_dequant_rows")
+
+
+def device_error(workspace, stream=None) -> tuple[int, int]:
+    """(status, flags) from the workspace header. Synchronises the stream."""
+    flags = ctypes.c_uint32(0)
+    st = lib().mla_get_device_error(_ptr(workspace), _stream_handle(stream), ctypes.byref(flags))
+    return st, flags.value
+
+
+def reset_device_error(workspace, stream=None) -> None:
+    _check(lib().mla_reset_device_error(_ptr(workspace), _stream_handle(stream)), "mla_reset_device_error")

@@ -1,0 +1,216 @@
+// C-ABI entry points of the MLA decode library (declared in mla_decode.h):
+// argument checks, the split planner, workspace carving and kernel launches.
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+
+#include "mla_decode.h"
+#include "mla_internal.h"
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+int g_sm_count[kMaxDevices] = {0};
+
+int sm_count_of_current_device() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return 0;
+  if (g_sm_count[dev] == 0) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+    g_sm_count[dev] = n;
+  }
+  return g_sm_count[dev];
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Fewest KV rows a partition should get: below this, the per-partition fixed
+// cost (query load, partial write and merge) outweighs the parallelism.
+constexpr int64_t kMinRowsPerSplit = 128;
+constexpr int32_t kMaxSplits = 4096;
+
+int32_t plan_splits(int64_t total_q, int64_t batch, int64_t total_kv, int sm_count) {
+  if (sm_count <= 0) sm_count = 1;
+  // Work estimate: every query token streams its segment's rows; with one
+  // token per segment this is exactly total_kv.
+  int64_t work = total_kv;
+  if (batch > 0 && total_q > batch) work = (total_kv * total_q + batch - 1) / batch;
+  int64_t p = (work + kMinRowsPerSplit - 1) / kMinRowsPerSplit;
+  if (p > sm_count) p = sm_count;
+  if (p < 1) p = 1;
+  return static_cast<int32_t>(p);
+}
+
+size_t kv_bytes(mla_dtype_t dt, int64_t total_kv) {
+  switch (dt) {
+    case MLA_DTYPE_BF16: return static_cast<size_t>(total_kv) * MLA_D_QK * 2;
+    case MLA_DTYPE_FP8_E4M3: return static_cast<size_t>(total_kv) * MLA_D_QK;
+    case MLA_DTYPE_MXFP4: return static_cast<size_t>(total_kv) * (MLA_D_QK / 2);
+  }
+  return 0;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* mla_status_string(mla_status_t s) {
+  switch (s) {
+    case MLA_OK: return "MLA_OK";
+    case MLA_ERR_INVALID_ARG: return "MLA_ERR_INVALID_ARG: invalid argument";
+    case MLA_ERR_UNSUPPORTED: return "MLA_ERR_UNSUPPORTED: unsupported dtype combination";
+    case MLA_ERR_WORKSPACE: return "MLA_ERR_WORKSPACE: workspace missing or too small";
+    case MLA_ERR_CUDA: return "MLA_ERR_CUDA: CUDA runtime error";
+    case MLA_ERR_TIMEOUT: return "MLA_ERR_TIMEOUT: a bounded device wait expired";
+    case MLA_ERR_DEVICE_CHECK: return "MLA_ERR_DEVICE_CHECK: indptr arrays failed the device checks";
+  }
+  return "unknown mla_status_t";
+}
+
+mla_status_t mla_plan(int32_t batch, int32_t total_q, int32_t total_kv, mla_dtype_t kv_dtype, int32_t sm_count,
+                      int32_t* num_splits) {
+  (void)kv_dtype;
+  if (!num_splits || batch < 0 || total_q < 0 || total_kv < 0) return MLA_ERR_INVALID_ARG;
+  if (sm_count <= 0) sm_count = sm_count_of_current_device();
+  *num_splits = plan_splits(total_q, batch, total_kv, sm_count);
+  return MLA_OK;
+}
+
+mla_status_t mla_decode_workspace_size(int32_t batch, int32_t total_q, int32_t total_kv, mla_dtype_t kv_dtype,
+                                       int32_t num_splits, size_t* bytes) {
+  if (!bytes || batch < 0 || total_q < 0 || total_kv < 0 || num_splits < 0 || num_splits > kMaxSplits)
+    return MLA_ERR_INVALID_ARG;
+  if (num_splits == 0) {
+    const mla_status_t st = mla_plan(batch, total_q, total_kv, kv_dtype, 0, &num_splits);
+    if (st != MLA_OK) return st;
+  }
+  *bytes = mla::workspace_bytes_for(num_splits, total_q);
+  return MLA_OK;
+}
+
+mla_status_t mla_decode(const void* q, const void* kv, const void* kv_scale, const int32_t* qo_indptr,
+                        const int32_t* kv_indptr, void* out, mla_dtype_t kv_dtype, const mla_decode_opts* opts,
+                        void* stream) {
+  if (!opts) return MLA_ERR_INVALID_ARG;
+  const int32_t batch = opts->batch, total_q = opts->total_q, total_kv = opts->total_kv;
+  if (batch < 1 || total_q < 0 || total_kv < 0) return MLA_ERR_INVALID_ARG;
+  if (kv_dtype != MLA_DTYPE_BF16 && kv_dtype != MLA_DTYPE_FP8_E4M3 && kv_dtype != MLA_DTYPE_MXFP4)
+    return MLA_ERR_INVALID_ARG;
+  if (opts->q_dtype != MLA_DTYPE_BF16 && opts->q_dtype != MLA_DTYPE_FP8_E4M3) return MLA_ERR_INVALID_ARG;
+  if (!qo_indptr || !kv_indptr) return MLA_ERR_INVALID_ARG;
+  if (total_q > 0 && (!q || !out || !aligned16(q) || !aligned16(out))) return MLA_ERR_INVALID_ARG;
+  if (total_kv > 0 && (!kv || !aligned16(kv))) return MLA_ERR_INVALID_ARG;
+  if (kv_dtype != MLA_DTYPE_BF16 && !kv_scale) return MLA_ERR_INVALID_ARG;
+  if (opts->q_dtype == MLA_DTYPE_FP8_E4M3 && !opts->q_scale) return MLA_ERR_INVALID_ARG;
+  if (!mla::stage1_supported(kv_dtype, opts->q_dtype)) return MLA_ERR_UNSUPPORTED;
+  int32_t splits = opts->num_splits;
+  if (splits < 0 || splits > kMaxSplits) return MLA_ERR_INVALID_ARG;
+  if (splits == 0) splits = plan_splits(total_q, batch, total_kv, sm_count_of_current_device());
+  const size_t need = mla::workspace_bytes_for(splits, total_q);
+  if (!opts->workspace || opts->workspace_bytes < need ||
+      (reinterpret_cast<uintptr_t>(opts->workspace) & 255u) != 0)
+    return MLA_ERR_WORKSPACE;
+  if (total_q == 0) return MLA_OK;
+
+  mla::Stage1Params p;
+  p.q = q;
+  p.kv = kv;
+  p.kv_scale = kv_scale;
+  p.q_scale = opts->q_scale;
+  p.qo_indptr = qo_indptr;
+  p.kv_indptr = kv_indptr;
+  p.batch = batch;
+  p.total_q = total_q;
+  p.total_kv = total_kv;
+  p.num_splits = splits;
+  p.sm_scale = opts->sm_scale > 0.f ? opts->sm_scale : static_cast<float>(1.0 / std::sqrt(576.0));
+  p.out = out;
+  uint8_t* ws = static_cast<uint8_t*>(opts->workspace);
+  p.dev_flags = reinterpret_cast<uint32_t*>(ws);
+  const int64_t slots = static_cast<int64_t>(splits) + total_q;
+  p.part_o = reinterpret_cast<float*>(ws + mla::kHeaderBytes);
+  p.part_lse = p.part_o + slots * mla::kHeads * mla::kDv;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (total_kv > 0) {
+    if (mla::launch_stage1(kv_dtype, opts->q_dtype, p, st) != cudaSuccess) return MLA_ERR_CUDA;
+  }
+  if (mla::launch_stage2(p, st) != cudaSuccess) return MLA_ERR_CUDA;
+  return MLA_OK;
+}
+
+mla_status_t mla_decode_from_host(const void* h_q, const void* h_kv, const void* h_kv_scale, const float* h_q_scale,
+                                  const int32_t* h_qo_indptr, const int32_t* h_kv_indptr, void* h_out,
+                                  mla_dtype_t kv_dtype, const mla_decode_opts* opts, const mla_device_buffers* dev,
+                                  void* stream) {
+  if (!opts || !dev || !h_qo_indptr || !h_kv_indptr) return MLA_ERR_INVALID_ARG;
+  const int64_t batch = opts->batch, total_q = opts->total_q, total_kv = opts->total_kv;
+  if (batch < 1 || total_q < 0 || total_kv < 0) return MLA_ERR_INVALID_ARG;
+  if ((total_q > 0 && (!h_q || !h_out || !dev->q || !dev->out)) || (total_kv > 0 && (!h_kv || !dev->kv)) ||
+      !dev->qo_indptr || !dev->kv_indptr)
+    return MLA_ERR_INVALID_ARG;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const size_t qbytes = static_cast<size_t>(total_q) * MLA_NUM_HEADS * MLA_D_QK *
+                        (opts->q_dtype == MLA_DTYPE_BF16 ? 2 : 1);
+  auto h2d = [&](void* d, const void* h, size_t n) {
+    return n == 0 || cudaMemcpyAsync(d, h, n, cudaMemcpyHostToDevice, st) == cudaSuccess;
+  };
+  bool ok = h2d(dev->q, h_q, qbytes) && h2d(dev->kv, h_kv, kv_bytes(kv_dtype, total_kv)) &&
+            h2d(dev->qo_indptr, h_qo_indptr, sizeof(int32_t) * (batch + 1)) &&
+            h2d(dev->kv_indptr, h_kv_indptr, sizeof(int32_t) * (batch + 1));
+  if (ok && kv_dtype == MLA_DTYPE_FP8_E4M3) {
+    if (!h_kv_scale || !dev->kv_scale) return MLA_ERR_INVALID_ARG;
+    ok = h2d(dev->kv_scale, h_kv_scale, sizeof(float));
+  } else if (ok && kv_dtype == MLA_DTYPE_MXFP4) {
+    if ((!h_kv_scale || !dev->kv_scale) && total_kv > 0) return MLA_ERR_INVALID_ARG;
+    ok = h2d(dev->kv_scale, h_kv_scale, static_cast<size_t>(total_kv) * (MLA_D_QK / MLA_MX_BLOCK));
+  }
+  if (ok && opts->q_dtype == MLA_DTYPE_FP8_E4M3) {
+    if (!h_q_scale || !dev->q_scale) return MLA_ERR_INVALID_ARG;
+    ok = h2d(dev->q_scale, h_q_scale, sizeof(float));
+  }
+  if (!ok) return MLA_ERR_CUDA;
+  mla_decode_opts o = *opts;
+  o.q_scale = dev->q_scale;
+  const mla_status_t s = mla_decode(dev->q, dev->kv, dev->kv_scale, dev->qo_indptr, dev->kv_indptr, dev->out,
+                                    kv_dtype, &o, stream);
+  if (s != MLA_OK) return s;
+  const size_t obytes = static_cast<size_t>(total_q) * MLA_NUM_HEADS * MLA_D_V * 2;
+  if (obytes && cudaMemcpyAsync(h_out, dev->out, obytes, cudaMemcpyDeviceToHost, st) != cudaSuccess)
+    return MLA_ERR_CUDA;
+  return MLA_OK;
+}
+
+mla_status_t mla_dequant_rows(const void* kv, const void* kv_scale, mla_dtype_t kv_dtype, int32_t total_kv,
+                              int32_t row0, int32_t nrows, float* d_out, void* stream) {
+  if (!kv || !d_out || !aligned16(kv) || total_kv < 0 || row0 < 0 || nrows < 0 ||
+      static_cast<int64_t>(row0) + nrows > total_kv)
+    return MLA_ERR_INVALID_ARG;
+  if (kv_dtype == MLA_DTYPE_MXFP4) return MLA_ERR_UNSUPPORTED;
+  if (kv_dtype != MLA_DTYPE_BF16 && kv_dtype != MLA_DTYPE_FP8_E4M3) return MLA_ERR_INVALID_ARG;
+  if (mla::launch_dequant(kv, kv_scale, kv_dtype, total_kv, row0, nrows, d_out, static_cast<cudaStream_t>(stream)) !=
+      cudaSuccess)
+    return MLA_ERR_CUDA;
+  return MLA_OK;
+}
+
+mla_status_t mla_get_device_error(const void* workspace, void* stream, uint32_t* flags) {
+  if (!workspace) return MLA_ERR_INVALID_ARG;
+  uint32_t f = 0;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (cudaMemcpyAsync(&f, workspace, sizeof(f), cudaMemcpyDeviceToHost, st) != cudaSuccess) return MLA_ERR_CUDA;
+  if (cudaStreamSynchronize(st) != cudaSuccess) return MLA_ERR_CUDA;
+  if (flags) *flags = f;
+  if (f & MLA_DEVFLAG_TIMEOUT) return MLA_ERR_TIMEOUT;
+  if (f & MLA_DEVFLAG_BAD_INDPTR) return MLA_ERR_DEVICE_CHECK;
+  return MLA_OK;
+}
+
+mla_status_t mla_reset_device_error(void* workspace, void* stream) {
+  if (!workspace) return MLA_ERR_INVALID_ARG;
+  if (cudaMemsetAsync(workspace, 0, sizeof(uint32_t), static_cast<cudaStream_t>(stream)) != cudaSuccess)
+    return MLA_ERR_CUDA;
+  return MLA_OK;
+}
+
+}  // extern "C"

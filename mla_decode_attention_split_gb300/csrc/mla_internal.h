@@ -1,0 +1,53 @@
+// Internal declarations shared by the library's translation units.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace mla {
+
+constexpr int kHeads = 16;
+constexpr int kDqk = 576;
+constexpr int kDv = 512;
+constexpr int kMxBlock = 32;
+
+// Workspace layout: [header 256 B: error flags][part_o: slots x 16 x 512 f32]
+// [part_lse: slots x 16 f32], slots = num_splits + total_q.
+constexpr size_t kHeaderBytes = 256;
+
+struct Stage1Params {
+  const void* q;
+  const void* kv;
+  const void* kv_scale;
+  const float* q_scale;
+  const int32_t* qo_indptr;
+  const int32_t* kv_indptr;
+  int32_t batch;
+  int32_t total_q;
+  int32_t total_kv;
+  int32_t num_splits;
+  float sm_scale;
+  void* out;          // bf16 [total_q][16][512]
+  float* part_o;      // [slots][16][512]
+  float* part_lse;    // [slots][16] (log2 domain)
+  uint32_t* dev_flags;
+};
+
+// KV formats / query formats as template tags (values match mla_dtype_t).
+enum KvFormat : int { kKvBf16 = 0, kKvFp8 = 1, kKvMxfp4 = 2 };
+enum QFormat : int { kQBf16 = 0, kQFp8 = 1 };
+
+cudaError_t launch_stage1(int kv_fmt, int q_fmt, const Stage1Params& p, cudaStream_t stream);
+cudaError_t launch_stage2(const Stage1Params& p, cudaStream_t stream);
+cudaError_t launch_dequant(const void* kv, const void* kv_scale, int kv_fmt, int32_t total_kv, int32_t row0,
+                           int32_t nrows, float* out, cudaStream_t stream);
+bool stage1_supported(int kv_fmt, int q_fmt);
+
+inline size_t workspace_bytes_for(int64_t num_splits, int64_t total_q) {
+  const int64_t slots = num_splits + total_q;
+  return kHeaderBytes + static_cast<size_t>(slots) * kHeads * kDv * sizeof(float) +
+         static_cast<size_t>(slots) * kHeads * sizeof(float);
+}
+
+}  // namespace mla

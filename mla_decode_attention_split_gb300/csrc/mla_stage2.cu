@@ -1,0 +1,188 @@
+// Stage 2 of split-K MLA decode: merge the per-piece partial outputs of each
+// query token with LSE weights, as in kernelbot-amd-mixed-mla-753817
+// (`mla_flash_decode_stage2`: L = max_s lse_s, w_s = 2^(lse_s - L),
+// out = sum_s w_s O_s / sum_s w_s) with LSEs kept in the log2 domain.
+// Tokens written directly by stage 1 are skipped; tokens of a segment with no
+// KV rows get zeros.
+//
+// Also the dequantisation check kernel, which pushes KV rows through stage 1's
+// operand path (same byte layout, same MMA) against an identity operand.
+#include "mla_device.cuh"
+#include "mla_internal.h"
+#include "mla_partition.cuh"
+
+namespace mla {
+
+constexpr int kThreads2 = 256;
+
+__global__ void __launch_bounds__(kThreads2) mla_stage2_kernel(const Stage1Params p) {
+  __shared__ int64_t sh[16];
+  const int token = blockIdx.x;
+  const SegLocate loc = block_locate<kThreads2, 2>(
+      p.qo_indptr, p.kv_indptr, p.batch, p.total_q, p.total_kv, [](int64_t) { return int64_t(0); }, token, sh);
+  if (!loc.ok) {
+    if (threadIdx.x == 0) atomicOr(p.dev_flags, kFlagBadIndptr);
+    return;
+  }
+  if (loc.seg < 0) return;
+  const int b = loc.seg;
+  const int32_t q0 = __ldg(p.qo_indptr + b);
+  const int64_t kvlen = __ldg(p.kv_indptr + b + 1) - __ldg(p.kv_indptr + b);
+  const int h = threadIdx.x >> 4, d0 = (threadIdx.x & 15) * 32;
+  uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.out) +
+                                        (static_cast<int64_t>(token) * kHeads + h) * kDv + d0);
+  if (kvlen == 0) {
+#pragma unroll
+    for (int k = 0; k < 4; ++k) dst[k] = make_uint4(0u, 0u, 0u, 0u);
+    return;
+  }
+  const int64_t vs = loc.seg_vs + static_cast<int64_t>(token - q0) * kvlen;
+  const int64_t P = p.num_splits;
+  const int64_t c0 = part_of_row(vs, loc.total, P), c1 = part_of_row(vs + kvlen - 1, loc.total, P);
+  if (c0 == c1) return;  // stage 1 wrote this token directly
+  float L = -INFINITY;
+  for (int64_t c = c0; c <= c1; ++c) L = fmaxf(L, __ldg(p.part_lse + (c + token) * kHeads + h));
+  float acc[32];
+#pragma unroll
+  for (int i = 0; i < 32; ++i) acc[i] = 0.f;
+  float wsum = 0.f;
+  for (int64_t c = c0; c <= c1; ++c) {
+    const float wgt = fast_exp2(__ldg(p.part_lse + (c + token) * kHeads + h) - L);
+    wsum += wgt;
+    const float4* src = reinterpret_cast<const float4*>(p.part_o + ((c + token) * kHeads + h) * kDv + d0);
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      const float4 v = __ldg(src + k);
+      acc[4 * k] += wgt * v.x;
+      acc[4 * k + 1] += wgt * v.y;
+      acc[4 * k + 2] += wgt * v.z;
+      acc[4 * k + 3] += wgt * v.w;
+    }
+  }
+  const float inv = 1.0f / wsum;
+  uint32_t w[16];
+#pragma unroll
+  for (int k = 0; k < 16; ++k) w[k] = pack_bf16x2(acc[2 * k] * inv, acc[2 * k + 1] * inv);
+#pragma unroll
+  for (int k = 0; k < 4; ++k) dst[k] = make_uint4(w[4 * k], w[4 * k + 1], w[4 * k + 2], w[4 * k + 3]);
+}
+
+cudaError_t launch_stage2(const Stage1Params& p, cudaStream_t stream) {
+  if (p.total_q == 0) return cudaSuccess;
+  mla_stage2_kernel<<<p.total_q, kThreads2, 0, stream>>>(p);
+  return cudaGetLastError();
+}
+
+// ---------------------------------------------------------------------------
+// Dequantisation check. One warp per 8 KV rows; lane (g, t) takes row g and
+// the same bytes it would take as a score warp (see the stage-1 query
+// fragment layout), then multiplies by an identity operand on the tensor core.
+// C[h][n] = B[kappa][n] where kappa = h (+16 for the second half) selects a
+// contraction index; kappa maps back to the KV dim through the permutation.
+template <int KV>
+__global__ void mla_dequant_kernel(const uint8_t* __restrict__ kv, int32_t total_kv, int32_t row0, int32_t nrows,
+                                   float* __restrict__ out) {
+  const int lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
+  const int base_row = row0 + 8 * blockIdx.x;
+  const int my_row = base_row + g;
+  const bool valid = (my_row < row0 + nrows) && (my_row < total_kv);
+  if (KV == kKvFp8) {
+    // identity halves: A[h][kappa] = 1.0 (e4m3 0x38) iff kappa == h + 16*half
+    uint32_t id[2][4];
+#pragma unroll
+    for (int half = 0; half < 2; ++half)
+#pragma unroll
+      for (int r = 0; r < 4; ++r) {
+        const int arow = g + ((r & 1) ? 8 : 0);
+        const int kbase = 4 * t + ((r & 2) ? 16 : 0);
+        uint32_t wv = 0;
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+          if (kbase + i == arow + 16 * half) wv |= 0x38u << (8 * i);
+        id[half][r] = wv;
+      }
+    const uint8_t* rowp = kv + static_cast<int64_t>(valid ? my_row : 0) * 576;
+#pragma unroll
+    for (int W = 0; W < 5; ++W) {
+      uint4 kb[2];
+      const int off = (W < 4) ? 128 * W + 32 * t : 512 + 16 * t;
+      kb[0] = valid ? __ldg(reinterpret_cast<const uint4*>(rowp + off)) : make_uint4(0, 0, 0, 0);
+      kb[1] = (valid && W < 4) ? __ldg(reinterpret_cast<const uint4*>(rowp + off + 16)) : make_uint4(0, 0, 0, 0);
+#pragma unroll
+      for (int k = 0; k < (W < 4 ? 4 : 2); ++k) {
+        const uint32_t b0 = (k >> 1) ? (((2 * k) & 3) == 0 ? kb[1].x : kb[1].z) : (((2 * k) & 3) == 0 ? kb[0].x : kb[0].z);
+        const uint32_t b1 = (k >> 1) ? (((2 * k) & 3) == 0 ? kb[1].y : kb[1].w) : (((2 * k) & 3) == 0 ? kb[0].y : kb[0].w);
+#pragma unroll
+        for (int half = 0; half < 2; ++half) {
+          float c[4] = {0.f, 0.f, 0.f, 0.f};
+          mma_e4m3(c, id[half], b0, b1);
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const int hrow = g + ((e & 2) ? 8 : 0);  // C row = kappa - 16*half
+            const int n = 2 * t + (e & 1);           // C col = KV row within the group
+            const int kappa = hrow;                  // within the half
+            const int tk = kappa >> 2, i = kappa & 3;
+            const int d = (W < 4 ? 128 * W + 32 * tk + 8 * k : 512 + 16 * tk + 8 * k) + 4 * half + i;
+            const int r = base_row + n;
+            if (r < row0 + nrows && r < total_kv) out[static_cast<int64_t>(r - row0) * 576 + d] = c[e];
+          }
+        }
+      }
+    }
+  } else {
+    // bf16: A = 16x16 identity (bf16 1.0 = 0x3F80); kappa = h.
+    uint32_t id[4];
+#pragma unroll
+    for (int r = 0; r < 4; ++r) {
+      const int arow = g + ((r & 1) ? 8 : 0);
+      const int kbase = 2 * t + ((r & 2) ? 8 : 0);
+      uint32_t wv = 0;
+      if (kbase == arow) wv |= 0x3F80u;
+      if (kbase + 1 == arow) wv |= 0x3F80u << 16;
+      id[r] = wv;
+    }
+    const uint8_t* rowp = kv + static_cast<int64_t>(valid ? my_row : 0) * 1152;
+#pragma unroll
+    for (int W = 0; W < 9; ++W) {
+      uint4 kb[2];
+      const int off = 128 * W + 32 * t;
+      kb[0] = valid ? __ldg(reinterpret_cast<const uint4*>(rowp + off)) : make_uint4(0, 0, 0, 0);
+      kb[1] = valid ? __ldg(reinterpret_cast<const uint4*>(rowp + off + 16)) : make_uint4(0, 0, 0, 0);
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const uint4& src = kb[k >> 1];
+        const uint32_t b0 = ((2 * k) & 3) == 0 ? src.x : src.z;
+        const uint32_t b1 = ((2 * k) & 3) == 0 ? src.y : src.w;
+        float c[4] = {0.f, 0.f, 0.f, 0.f};
+        mma_bf16(c, id, b0, b1);
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const int kappa = g + ((e & 2) ? 8 : 0);
+          const int n = 2 * t + (e & 1);
+          // kappa = 2tk + ee -> d = 64W + 16tk + 4k + ee; kappa = 8 + 2tk + ee -> +2
+          const int hi = kappa >= 8, kk = kappa & 7, tk = kk >> 1, ee = kk & 1;
+          const int d = 64 * W + 16 * tk + 4 * k + 2 * hi + ee;
+          const int r = base_row + n;
+          if (r < row0 + nrows && r < total_kv) out[static_cast<int64_t>(r - row0) * 576 + d] = c[e];
+        }
+      }
+    }
+  }
+}
+
+cudaError_t launch_dequant(const void* kv, const void* kv_scale, int kv_fmt, int32_t total_kv, int32_t row0,
+                           int32_t nrows, float* out, cudaStream_t stream) {
+  (void)kv_scale;
+  if (nrows <= 0) return cudaSuccess;
+  const int blocks = (nrows + 7) / 8;
+  if (kv_fmt == kKvFp8) {
+    mla_dequant_kernel<kKvFp8><<<blocks, 32, 0, stream>>>(static_cast<const uint8_t*>(kv), total_kv, row0, nrows, out);
+  } else if (kv_fmt == kKvBf16) {
+    mla_dequant_kernel<kKvBf16><<<blocks, 32, 0, stream>>>(static_cast<const uint8_t*>(kv), total_kv, row0, nrows, out);
+  } else {
+    return cudaErrorInvalidValue;
+  }
+  return cudaGetLastError();
+}
+
+}  // namespace mla

@@ -1,0 +1,103 @@
+"""The C-ABI library builds (cross-compiled for sm_103a), loads without a GPU,
+and exports every entry point that include/mla_decode.h declares; host-only
+logic (planner, workspace sizing, argument checks) is exercised on CPU."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import mla_decode_attention_split_gb300 as m
+from mla_decode_attention_split_gb300 import build as b
+
+HEADER = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include", "mla_decode.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    b.build()
+    return m.lib()
+
+
+def _declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(mla_[a-z_]+)\s*\(", text)))
+
+
+def test_header_declares_the_boundary():
+    names = _declared_functions()
+    for required in ("mla_decode", "mla_decode_workspace_size", "mla_plan", "mla_status_string"):
+        assert required in names
+    assert set(names) == set(m.EXPORTED)
+
+
+def test_every_declared_symbol_is_exported(lib):
+    for name in _declared_functions():
+        assert hasattr(lib, name), name
+
+
+def test_library_is_built_for_sm103a_only(lib):
+    log = open(os.path.join(b.BUILD_DIR, "ptxas.log")).read()
+    assert "sm_103a" in log and "sm_100" not in log.replace("sm_103a", "")
+
+
+def test_status_strings(lib):
+    for s in range(7):
+        assert m.status_string(s).startswith("MLA_")
+    assert "unknown" in m.status_string(99)
+
+
+def test_planner_host_logic(lib):
+    # one partition per 128 KV rows of work, capped at the SM count
+    assert m.plan(256, 256, 256 * 8192, m.FP8_E4M3, sm_count=152) == 152
+    assert m.plan(4, 4, 4096, m.BF16, sm_count=152) == 32
+    assert m.plan(1, 1, 1, m.FP8_E4M3, sm_count=152) == 1
+    assert m.plan(1, 1, 0, m.FP8_E4M3, sm_count=152) == 1
+    # q_len > 1: work scales with tokens per segment
+    assert m.plan(2, 8, 256, m.BF16, sm_count=152) == 8
+    with pytest.raises(m.MlaError):
+        m.plan(-1, 1, 1, m.BF16, sm_count=152)
+
+
+def test_workspace_size(lib):
+    n = m.workspace_size(4, 4, 4096, m.BF16, num_splits=32)
+    slots = 32 + 4
+    assert n == 256 + slots * 16 * 512 * 4 + slots * 16 * 4
+    with pytest.raises(m.MlaError):
+        m.workspace_size(4, 4, 4096, m.BF16, num_splits=-2)
+
+
+def test_argument_checks_fail_before_any_device_work(lib):
+    L = lib
+    st = L.mla_decode(None, None, None, None, None, None, m.BF16, None, None)
+    assert st == m.MLA_ERR_INVALID_ARG
+    opts = m.DecodeOpts(batch=0, total_q=1, total_kv=1, sm_scale=0.0, q_dtype=m.BF16, q_scale=None, num_splits=1,
+                        workspace=None, workspace_bytes=0)
+    assert L.mla_decode(None, None, None, None, None, None, m.BF16, ctypes.byref(opts), None) == m.MLA_ERR_INVALID_ARG
+    # misaligned q pointer
+    opts.batch = 1
+    buf = (ctypes.c_uint8 * 64)()
+    base = ctypes.addressof(buf)
+    aligned = (base + 15) & ~15
+    st = L.mla_decode(ctypes.c_void_p(aligned + 2), ctypes.c_void_p(aligned), None, ctypes.c_void_p(aligned),
+                      ctypes.c_void_p(aligned), ctypes.c_void_p(aligned), m.BF16, ctypes.byref(opts), None)
+    assert st == m.MLA_ERR_INVALID_ARG
+    # fp8 KV without its scale
+    st = L.mla_decode(ctypes.c_void_p(aligned), ctypes.c_void_p(aligned), None, ctypes.c_void_p(aligned),
+                      ctypes.c_void_p(aligned), ctypes.c_void_p(aligned), m.FP8_E4M3, ctypes.byref(opts), None)
+    assert st == m.MLA_ERR_INVALID_ARG
+    # fp8 q without q_scale
+    opts.q_dtype = m.FP8_E4M3
+    st = L.mla_decode(ctypes.c_void_p(aligned), ctypes.c_void_p(aligned), None, ctypes.c_void_p(aligned),
+                      ctypes.c_void_p(aligned), ctypes.c_void_p(aligned), m.BF16, ctypes.byref(opts), None)
+    assert st == m.MLA_ERR_INVALID_ARG
+    # missing workspace
+    opts.q_dtype = m.BF16
+    st = L.mla_decode(ctypes.c_void_p(aligned), ctypes.c_void_p(aligned), None, ctypes.c_void_p(aligned),
+                      ctypes.c_void_p(aligned), ctypes.c_void_p(aligned), m.BF16, ctypes.byref(opts), None)
+    assert st == m.MLA_ERR_WORKSPACE
+    # dequant entry: row range beyond the cache
+    st = L.mla_dequant_rows(ctypes.c_void_p(aligned), None, m.FP8_E4M3, 10, 5, 6, ctypes.c_void_p(aligned), None)
+    assert st == m.MLA_ERR_INVALID_ARG
+    assert L.mla_get_device_error(None, None, None) == m.MLA_ERR_INVALID_ARG
