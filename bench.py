@@ -1,0 +1,404 @@
+#!/usr/bin/env python
+"""Benchmark: MLA decode µs/call and KV-read GB/s against the GB300 HBM roofline.
+
+One step = one full decode call (stage 1 + stage 2) over the batch of the
+headline workload: fp8 e4m3 KV cache (per-tensor scale), batch 256 x 1 query
+token, kv_len 8192 per sequence, bf16 queries -- 1.21 GB of KV streamed per
+call, larger than the 129 MB L2, so consecutive calls read HBM.
+
+Prints ONE JSON line (rank 0). value = KV-read GB/s over all ranks
+(algorithmic KV bytes / time); us_per_call alongside. Under torchrun each rank
+runs its own copy of the workload (weak scaling, no collective on the data
+path; a barrier and a max over ranks bracket the timing).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+
+--impl reference times the fp64 CPU oracle (the reference semantics) on the
+same workload and metric, one bounded sample per step, on the host cores.
+"""
+from __future__ import annotations
+
+import argparse
+import datetime
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+HEADLINE = "fp8kv_bs256_kv8192"
+METRIC = "MLA decode µs/call and KV-read GB/s vs GB300 HBM peak, per (batch, kv_len, dtype)"
+STAGE1_SOURCES = ["mla_stage1.cu", "mla_device.cuh", "mla_partition.cuh", "mla_internal.h"]
+
+
+def _stage1_source_sha() -> str:
+    h = hashlib.sha256()
+    for f in STAGE1_SOURCES:
+        with open(os.path.join(ROOT, "mla_decode_attention_split_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def _measured_peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return 6800.0, "fallback"
+
+
+def _ncu_traffic(workload: str):
+    """DRAM bytes per stage-1 launch from the committed ncu summary, if it was
+    taken on the current stage-1 source; else None."""
+    path = os.path.join(ROOT, "profiles", "stage1_dram_traffic.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        e = d.get(workload)
+        if e and e.get("source_sha") == _stage1_source_sha():
+            return float(e["dram_bytes_per_launch"])
+    except Exception:
+        pass
+    return None
+
+
+class ClockSampler:
+    """nvidia-smi clocks/throttle reasons sampled every 100 ms in the background."""
+    FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                                          "-lms", "100", "-i", str(self.index)], stdout=subprocess.PIPE,
+                                         stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        self.lines = [ln for ln in out.splitlines() if ln.strip()]
+
+    def summary(self, t0: float, t1: float):
+        rows = []
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 10:
+                continue
+            try:
+                ts = datetime.datetime.strptime(parts[0], "%Y/%m/%d %H:%M:%S.%f").timestamp()
+                rows.append((ts, float(parts[2]), float(parts[3]), parts[6:10]))
+            except ValueError:
+                continue
+        inside = [r for r in rows if t0 - 0.05 <= r[0] <= t1 + 0.05]
+        use = inside or rows
+        if not use:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no nvidia-smi samples"], "samples": 0}
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in use for i, v in enumerate(r[3]) if v.lower() == "active"})
+        return {"sm_mhz": statistics.median(r[1] for r in use), "sm_max_mhz": max(r[2] for r in use),
+                "reasons": reasons, "samples": len(inside)}
+
+
+def _dist():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def _barrier_max(value: float, world: int, device):
+    if world == 1:
+        return value
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def _barrier(world: int):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def kv_bytes(inp) -> int:
+    return inp.kv_bytes()
+
+
+def workload_by_name(synth, name):
+    if name in synth.WORKLOADS:
+        return synth.WORKLOADS[name]
+    # profiling shapes: kvfp8_bs64_kv8192, kvbf16_bs8_kv4096 (bf16 q, one token per segment)
+    fmt, bs, kvl = name.split("_")
+    kv_dtype = {"kvfp8": synth.FP8_E4M3, "kvbf16": synth.BF16}[fmt]
+    return synth.Workload(name, int(bs[2:]), 1, int(kvl[2:]), synth.BF16, kv_dtype)
+
+
+def time_workload(m, synth, torch, name, steps, warmup, flush_l2: bool):
+    """Per-call device time of one workload (stage-1 and total), median over steps."""
+    inp = synth.make_inputs(synth.WORKLOADS[name], "cuda")
+    out = torch.empty((inp.total_q, 16, 512), dtype=torch.bfloat16, device="cuda")
+    ws = m.alloc_workspace(inp.batch, inp.total_q, inp.total_kv, inp.kv_dtype)
+    flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device="cuda") if flush_l2 else None
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
+    tot, st1 = [], []
+    for i in range(warmup + steps):
+        if flush is not None:
+            flush.fill_(i & 0xFF)
+        m.decode(inp.q, inp.kv, inp.kv_scale, inp.qo_indptr, inp.kv_indptr, out, inp.kv_dtype, workspace=ws,
+                 q_dtype=inp.q_dtype, q_scale=inp.q_scale, events=ev)
+        torch.cuda.synchronize()
+        if i >= warmup:
+            tot.append(m.elapsed_ms(ev[0], ev[2]) * 1e3)
+            st1.append(m.elapsed_ms(ev[0], ev[1]) * 1e3)
+    st, flags = m.device_error(ws)
+    assert st == m.MLA_OK, (name, flags)
+    us = statistics.median(tot)
+    return {"us_per_call": round(us, 2), "stage1_us": round(statistics.median(st1), 2),
+            "kv_gbs": round(kv_bytes(inp) / (us * 1e-6) / 1e9, 1), "kv_bytes": kv_bytes(inp),
+            "num_splits": m.plan(inp.batch, inp.total_q, inp.total_kv, inp.kv_dtype),
+            "l2": "flushed (256 MB write) before each call" if flush_l2 else "back-to-back"}
+
+
+def cpu_baseline(inp, synth, oracle, target_s=15.0):
+    """The oracle as it stands, single-threaded, on a bounded sample of segments
+    (all 16 heads each); throughput in KV-read GB/s of the sampled segments."""
+    segs, t_total, nbytes = [], 0.0, 0
+    rowb = inp.kv_bytes() / max(1, inp.total_kv)
+    b = 0
+    while t_total < target_s and b < inp.batch:
+        h = synth.to_host_codes(inp, [b])
+        t0 = time.perf_counter()
+        oracle.mla_decode(h["q"], h["q_dtype"], h["q_scale"], h["kv"], h["kv_dtype"], h["kv_scale"],
+                          h["qo_indptr"], h["kv_indptr"], heads=16, dqk=576, dv=512, sm_scale=synth.sm_scale_default())
+        t_total += time.perf_counter() - t0
+        nbytes += int(h["kv"].shape[0] * rowb)
+        segs.append(b)
+        b += 1
+    gbs = nbytes / t_total / 1e9
+    return {"value": round(gbs, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
+            "sample": f"{len(segs)} of {inp.batch} segments x 16 heads (fp64 C, single thread), {t_total:.1f} s",
+            "us_per_call_equiv": round(inp.kv_bytes() / (gbs * 1e9) * 1e6, 1)}
+
+
+def run_reference(args):
+    world, rank, local = _dist()
+    if rank != 0:
+        return 0
+    import torch
+    import oracle
+    from mla_decode_attention_split_gb300 import synth
+    oracle.build()
+    w = synth.WORKLOADS[HEADLINE]
+    # segments are i.i.d.: a sub-batch of the workload's own shape, cycled
+    sub = min(w.batch, 16)
+    inp = synth.make_inputs(synth.Workload(w.name, sub, w.q_len, w.kv_len, w.q_dtype, w.kv_dtype, seed=w.seed), "cpu")
+    rowb = inp.kv_bytes() / inp.total_kv
+    times, nbytes = [], 0
+    for i in range(args.warmup + args.steps):
+        b = i % inp.batch
+        h = synth.to_host_codes(inp, [b])
+        t0 = time.perf_counter()
+        oracle.mla_decode(h["q"], h["q_dtype"], h["q_scale"], h["kv"], h["kv_dtype"], h["kv_scale"],
+                          h["qo_indptr"], h["kv_indptr"], heads=16, dqk=576, dv=512, sm_scale=synth.sm_scale_default())
+        dt = time.perf_counter() - t0
+        if i >= args.warmup:
+            times.append(dt)
+            nbytes += int(h["kv"].shape[0] * rowb)
+    total = sum(times)
+    gbs = nbytes / total / 1e9
+    line = {"impl": "reference", "metric": METRIC, "value": round(gbs, 4), "unit": "GB/s", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(total / len(times) * 1e3, 3),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": HEADLINE, "batch": w.batch, "q_len": 1, "kv_len": w.kv_len, "q_dtype": "bf16",
+                       "kv_dtype": "fp8_e4m3",
+                       "step": f"one segment (16 heads x 8192 KV rows) per step, cycling over {sub} seeded segments"},
+            "cpu_baseline": {"value": round(gbs, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
+                             "sample": f"{len(times)} steps x 1 segment x 16 heads, fp64 C single thread"},
+            "e2e": {"value": round(gbs, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=4000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-workloads", action="store_true", help="skip the per-workload table")
+    ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end measurement")
+    ap.add_argument("--workload", default=HEADLINE,
+                    help="workload name (the five benchmark workloads, or kv{fp8,bf16}_bs<B>_kv<L> for profiling)")
+    args = ap.parse_args()
+    if args.impl == "reference":
+        return run_reference(args)
+
+    world, rank, local = _dist()
+    import torch
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=device)
+    from mla_decode_attention_split_gb300 import build as _build
+    _build.build()
+    import mla_decode_attention_split_gb300 as m
+    from mla_decode_attention_split_gb300 import synth
+
+    w = workload_by_name(synth, args.workload)
+    inp = synth.make_inputs(w, device)
+    torch.cuda.empty_cache()
+    kvb = kv_bytes(inp)
+    out = torch.empty((inp.total_q, 16, 512), dtype=torch.bfloat16, device=device)
+    splits = m.plan(inp.batch, inp.total_q, inp.total_kv, inp.kv_dtype)
+    ws = m.alloc_workspace(inp.batch, inp.total_q, inp.total_kv, inp.kv_dtype, num_splits=splits)
+    stream = torch.cuda.current_stream()
+    K, W = args.steps, args.warmup
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K)]
+
+    def step(events=None):
+        m.decode(inp.q, inp.kv, inp.kv_scale, inp.qo_indptr, inp.kv_indptr, out, inp.kv_dtype, workspace=ws,
+                 q_dtype=inp.q_dtype, q_scale=inp.q_scale, num_splits=splits, events=events, stream=stream)
+
+    for _ in range(W):
+        step()
+    torch.cuda.synchronize()
+    sampler = ClockSampler(local)
+    sampler.start()
+    time.sleep(0.3)
+    _barrier(world)
+    torch.cuda.synchronize()
+    t_wall0 = time.time()
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    for i in range(K):
+        step(ev[i])
+    t1.record(stream)
+    torch.cuda.synchronize()
+    t_wall1 = time.time()
+    _barrier(world)
+    sampler.stop()
+    st, flags = m.device_error(ws)
+    assert st == m.MLA_OK, (m.status_string(st), flags)
+    ms_total = t0.elapsed_time(t1)
+    ms_total = _barrier_max(ms_total, world, device)
+    stage1_ms = [m.elapsed_ms(e[0], e[1]) for e in ev]
+    stage2_ms = [m.elapsed_ms(e[1], e[2]) for e in ev]
+    s1_avg_s = sum(stage1_ms) / K * 1e-3
+    ms_step = ms_total / K
+    value = kvb * K * world / (ms_total * 1e-3) / 1e9
+    peak, peak_kind = _measured_peaks()
+    achieved = kvb / s1_avg_s / 1e9
+    clocks = sampler.summary(t_wall0, t_wall1)
+
+    # end to end through the host-buffer entry point: every input H2D from
+    # pinned memory and the output D2H inside the timed region, every step
+    e2e = None if args.no_e2e else measure_e2e(m, torch, inp, out, ws, splits, stream, K, world, device, kvb)
+    line = build_line(args, w, inp, kvb, splits, world, K, W, value, ms_step, achieved, peak, peak_kind, s1_avg_s,
+                      stage2_ms, clocks, e2e)
+    finish(args, line, rank, world, w, m, synth, torch, inp)
+    return 0
+
+
+def measure_e2e(m, torch, inp, out, ws, splits, stream, K, world, device, kvb):
+    pin = (lambda t: None if t is None else t.cpu().pin_memory())
+    h = {"q": pin(inp.q), "kv": pin(inp.kv), "kv_scale": pin(inp.kv_scale), "q_scale": pin(inp.q_scale),
+         "qo_indptr": pin(inp.qo_indptr), "kv_indptr": pin(inp.kv_indptr),
+         "out": torch.empty(out.shape, dtype=torch.bfloat16).pin_memory()}
+    dev = {k: (None if v is None else torch.empty_like(v, device=device)) for k, v in h.items()}
+    e2e_steps = max(3, min(K, 50))
+    for _ in range(2):
+        m.decode_from_host(h, dev, inp.kv_dtype, q_dtype=inp.q_dtype, workspace=ws, num_splits=splits, stream=stream)
+    torch.cuda.synchronize()
+    _barrier(world)
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(e2e_steps):
+        m.decode_from_host(h, dev, inp.kv_dtype, q_dtype=inp.q_dtype, workspace=ws, num_splits=splits, stream=stream)
+    b.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = _barrier_max(a.elapsed_time(b), world, device)
+    h2d = sum(v.numel() * v.element_size() for k, v in h.items() if v is not None and k != "out")
+    d2h = h["out"].numel() * 2
+    return {"value": round(kvb * e2e_steps * world / (e2e_ms * 1e-3) / 1e9, 1), "unit": "GB/s",
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": e2e_steps,
+            "us_per_call": round(e2e_ms / e2e_steps * 1e3, 1),
+            "path": "mla_decode_from_host: q, KV cache, scales and indptrs H2D from pinned host memory, out D2H"}
+
+
+def build_line(args, w, inp, kvb, splits, world, K, W, value, ms_step, achieved, peak, peak_kind, s1_avg_s,
+               stage2_ms, clocks, e2e):
+    from mla_decode_attention_split_gb300 import synth
+    line = {"metric": METRIC, "value": round(value, 1), "unit": "GB/s", "n_gpus": world, "steps": K, "warmup": W,
+            "ms_per_step": round(ms_step, 4), "us_per_call": round(ms_step * 1e3, 2), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "e4m3 x e4m3 -> f32 (fp8 KV codes; bf16 q as exact hi+lo e4m3)",
+            "data": "synthetic (seeded N(0,1), quantised as the pages' harness does)",
+            "config": {"workload": w.name, "batch": w.batch, "q_len": w.q_len, "kv_len": w.kv_len,
+                       "q_dtype": synth.DTYPE_NAMES[w.q_dtype], "kv_dtype": synth.DTYPE_NAMES[w.kv_dtype],
+                       "kv_bytes_per_call": kvb, "num_splits": splits,
+                       "l2": (f"inputs larger than L2 ({kvb / 1e9:.2f} GB KV per call, L2 129 MB); no flush"
+                              if kvb > 129e6 else "KV fits in L2: back-to-back calls, warm"),
+                       "parallelism": f"{world} independent replicas (weak scaling)"},
+            "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+                         "frac": round(achieved / peak, 4), "traffic": _ncu_traffic(w.name),
+                         "kernel": f"mla_stage1_kernel<{synth.DTYPE_NAMES[w.kv_dtype]} KV, "
+                                   f"{synth.DTYPE_NAMES[w.q_dtype]} q>",
+                         "algorithmic_bytes": f"{kvb} per launch = {kvb // inp.total_kv} B x {inp.total_kv} KV rows",
+                         "peak_kind": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)",
+                         "stage1_us": round(s1_avg_s * 1e6, 2),
+                         "stage2_us": round(sum(stage2_ms) / K * 1e3, 2)},
+            "clocks": {"sm_mhz": clocks["sm_mhz"], "sm_max_mhz": clocks["sm_max_mhz"], "reasons": clocks["reasons"],
+                       "samples_in_timed_region": clocks["samples"]},
+            "gpu_launches": 2 * K,
+            "e2e": e2e}
+    return line
+
+
+def finish(args, line, rank, world, w, m, synth, torch, inp):
+    if rank == 0 and world == 1:
+        if not args.no_workloads:
+            table = {}
+            for name in synth.WORKLOADS:
+                try:
+                    table[name] = {"cold": time_workload(m, synth, torch, name, 30, 5, True),
+                                   "warm": time_workload(m, synth, torch, name, 30, 5, False)}
+                except m.MlaError as e:
+                    table[name] = {"unsupported": str(e)}
+            line["workloads"] = table
+        if not args.no_cpu_baseline:
+            import oracle
+            oracle.build()
+            line["cpu_baseline"] = cpu_baseline(inp, synth, oracle)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -83,6 +83,9 @@ typedef struct {
   void* workspace;        /* device scratch of mla_decode_workspace_size() bytes,
                              256-byte aligned, owned by the caller                 */
   size_t workspace_bytes;
+  void* profile_events[3]; /* optional cudaEvent_t handles (NULL = none), recorded
+                              on `stream` before stage 1, between stage 1 and
+                              stage 2, and after stage 2 (kernel timing)          */
 } mla_decode_opts;
 
 /* Split planner (the pages choose the split count from batch size and KV
@@ -164,6 +167,11 @@ mla_status_t mla_get_device_error(const void* workspace, void* stream, uint32_t*
 
 /* Clears the device error flags (flags are sticky until cleared). Async.      */
 mla_status_t mla_reset_device_error(void* workspace, void* stream);
+
+/* Milliseconds between two CUDA events (cudaEvent_t passed as void*) that
+ * have completed, e.g. the profile_events of mla_decode_opts. Synchronises
+ * on ev_end. Errors: MLA_ERR_INVALID_ARG (NULL), MLA_ERR_CUDA.                */
+mla_status_t mla_event_elapsed_ms(void* ev_start, void* ev_end, float* ms);
 
 /* Static description of a status code.                                        */
 const char* mla_status_string(mla_status_t status);

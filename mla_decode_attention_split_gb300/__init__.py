@@ -21,7 +21,7 @@ MLA_ERR_CUDA, MLA_ERR_TIMEOUT, MLA_ERR_DEVICE_CHECK = 4, 5, 6
 DEVFLAG_TIMEOUT, DEVFLAG_BAD_INDPTR = 0x1, 0x2
 
 EXPORTED = ("mla_plan", "mla_decode_workspace_size", "mla_decode", "mla_decode_from_host", "mla_dequant_rows",
-            "mla_get_device_error", "mla_reset_device_error", "mla_status_string")
+            "mla_get_device_error", "mla_reset_device_error", "mla_event_elapsed_ms", "mla_status_string")
 
 
 class MlaError(RuntimeError):
@@ -33,7 +33,8 @@ class MlaError(RuntimeError):
 class DecodeOpts(ctypes.Structure):
     _fields_ = [("batch", ctypes.c_int32), ("total_q", ctypes.c_int32), ("total_kv", ctypes.c_int32),
                 ("sm_scale", ctypes.c_float), ("q_dtype", ctypes.c_int), ("q_scale", ctypes.c_void_p),
-                ("num_splits", ctypes.c_int32), ("workspace", ctypes.c_void_p), ("workspace_bytes", ctypes.c_size_t)]
+                ("num_splits", ctypes.c_int32), ("workspace", ctypes.c_void_p), ("workspace_bytes", ctypes.c_size_t),
+                ("profile_events", ctypes.c_void_p * 3)]
 
 
 class DeviceBuffers(ctypes.Structure):
@@ -68,6 +69,7 @@ def lib():
             L.mla_dequant_rows.argtypes = [P, P, st, i32, i32, i32, P, P]
             L.mla_get_device_error.argtypes = [P, P, ctypes.POINTER(ctypes.c_uint32)]
             L.mla_reset_device_error.argtypes = [P, P]
+            L.mla_event_elapsed_ms.argtypes = [P, P, ctypes.POINTER(ctypes.c_float)]
             L.mla_status_string.argtypes = [st]
             L.mla_status_string.restype = ctypes.c_char_p
             for name in EXPORTED[:-1]:
@@ -118,18 +120,25 @@ def alloc_workspace(batch: int, total_q: int, total_kv: int, kv_dtype: int, num_
 
 
 def make_opts(batch, total_q, total_kv, *, q_dtype=BF16, q_scale=None, sm_scale=0.0, num_splits=0,
-              workspace=None) -> DecodeOpts:
-    return DecodeOpts(batch=batch, total_q=total_q, total_kv=total_kv, sm_scale=float(sm_scale), q_dtype=q_dtype,
-                      q_scale=None if q_scale is None else q_scale.data_ptr(), num_splits=num_splits,
-                      workspace=None if workspace is None else workspace.data_ptr(),
-                      workspace_bytes=0 if workspace is None else workspace.numel() * workspace.element_size())
+              workspace=None, events=None) -> DecodeOpts:
+    o = DecodeOpts(batch=batch, total_q=total_q, total_kv=total_kv, sm_scale=float(sm_scale), q_dtype=q_dtype,
+                   q_scale=None if q_scale is None else q_scale.data_ptr(), num_splits=num_splits,
+                   workspace=None if workspace is None else workspace.data_ptr(),
+                   workspace_bytes=0 if workspace is None else workspace.numel() * workspace.element_size())
+    if events is not None:  # three torch.cuda.Event(enable_timing=True)
+        for i, ev in enumerate(events):
+            if ev is not None and not ev.cuda_event:
+                ev.record()  # torch creates the CUDA event on its first record
+            o.profile_events[i] = None if ev is None else ev.cuda_event
+    return o
 
 
 def decode(q, kv, kv_scale, qo_indptr, kv_indptr, out, kv_dtype: int, *, workspace, q_dtype: int = BF16,
-           q_scale=None, sm_scale: float = 0.0, num_splits: int = 0, stream=None) -> None:
-    """mla_decode() on torch CUDA tensors (layouts as in mla_decode.h). Asynchronous."""
+           q_scale=None, sm_scale: float = 0.0, num_splits: int = 0, stream=None, events=None) -> None:
+    """mla_decode() on torch CUDA tensors (layouts as in mla_decode.h). Asynchronous.
+    events: optional three CUDA events recorded around stage 1 and stage 2."""
     opts = make_opts(qo_indptr.numel() - 1, q.shape[0], kv.shape[0], q_dtype=q_dtype, q_scale=q_scale,
-                     sm_scale=sm_scale, num_splits=num_splits, workspace=workspace)
+                     sm_scale=sm_scale, num_splits=num_splits, workspace=workspace, events=events)
     _check(lib().mla_decode(_ptr(q), _ptr(kv), _ptr(kv_scale), _ptr(qo_indptr), _ptr(kv_indptr), _ptr(out),
                             kv_dtype, ctypes.byref(opts), _stream_handle(stream)), "mla_decode")
 
@@ -162,3 +171,13 @@ def device_error(workspace, stream=None) -> tuple[int, int]:
 
 def reset_device_error(workspace, stream=None) -> None:
     _check(lib().mla_reset_device_error(_ptr(workspace), _stream_handle(stream)), "mla_reset_device_error")
+
+
+def elapsed_ms(ev_start, ev_end) -> float:
+    """Milliseconds between two torch CUDA events that the library recorded
+    (profile events); torch's own Event.elapsed_time only accepts events it
+    recorded itself."""
+    ms = ctypes.c_float(0.0)
+    _check(lib().mla_event_elapsed_ms(ctypes.c_void_p(ev_start.cuda_event), ctypes.c_void_p(ev_end.cuda_event),
+                                      ctypes.byref(ms)), "mla_event_elapsed_ms")
+    return ms.value

@@ -132,10 +132,17 @@ mla_status_t mla_decode(const void* q, const void* kv, const void* kv_scale, con
   p.part_o = reinterpret_cast<float*>(ws + mla::kHeaderBytes);
   p.part_lse = p.part_o + slots * mla::kHeads * mla::kDv;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
+  auto mark = [&](int i) {
+    return !opts->profile_events[i] ||
+           cudaEventRecord(static_cast<cudaEvent_t>(opts->profile_events[i]), st) == cudaSuccess;
+  };
+  if (!mark(0)) return MLA_ERR_CUDA;
   if (total_kv > 0) {
     if (mla::launch_stage1(kv_dtype, opts->q_dtype, p, st) != cudaSuccess) return MLA_ERR_CUDA;
   }
+  if (!mark(1)) return MLA_ERR_CUDA;
   if (mla::launch_stage2(p, st) != cudaSuccess) return MLA_ERR_CUDA;
+  if (!mark(2)) return MLA_ERR_CUDA;
   return MLA_OK;
 }
 
@@ -209,6 +216,14 @@ mla_status_t mla_get_device_error(const void* workspace, void* stream, uint32_t*
 mla_status_t mla_reset_device_error(void* workspace, void* stream) {
   if (!workspace) return MLA_ERR_INVALID_ARG;
   if (cudaMemsetAsync(workspace, 0, sizeof(uint32_t), static_cast<cudaStream_t>(stream)) != cudaSuccess)
+    return MLA_ERR_CUDA;
+  return MLA_OK;
+}
+
+mla_status_t mla_event_elapsed_ms(void* ev_start, void* ev_end, float* ms) {
+  if (!ev_start || !ev_end || !ms) return MLA_ERR_INVALID_ARG;
+  if (cudaEventSynchronize(static_cast<cudaEvent_t>(ev_end)) != cudaSuccess) return MLA_ERR_CUDA;
+  if (cudaEventElapsedTime(ms, static_cast<cudaEvent_t>(ev_start), static_cast<cudaEvent_t>(ev_end)) != cudaSuccess)
     return MLA_ERR_CUDA;
   return MLA_OK;
 }
