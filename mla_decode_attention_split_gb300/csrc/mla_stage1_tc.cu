@@ -76,6 +76,27 @@ struct L {
 static_assert(L::kAlloc <= 227 * 1024, "shared memory budget");
 static_assert(L::kOffQ % 1024 == 0 && L::kOffP % 1024 == 0, "swizzled operands need 1024-byte alignment");
 
+// Optional phase timers (build with -DMLA_PHASE_TIMING): cycles per CTA, warp
+// and phase, summed over the launch. Off by default.
+#ifdef MLA_PHASE_TIMING
+constexpr int kPhaseCtas = 1024;
+__device__ unsigned long long g_tc_phase[kPhaseCtas * 8 * 8];
+#define TC_PT_INIT long long tc_pt_ = clock64();
+#define TC_PT(ph)                                                                                          \
+  do {                                                                                                     \
+    const long long now_ = clock64();                                                                      \
+    if ((threadIdx.x & 31) == 0 && blockIdx.x < kPhaseCtas)                                                \
+      atomicAdd(&g_tc_phase[(blockIdx.x * 8 + (threadIdx.x >> 5)) * 8 + (ph)],                             \
+                static_cast<unsigned long long>(now_ - tc_pt_));                                           \
+    tc_pt_ = now_;                                                                                         \
+  } while (0)
+#else
+#define TC_PT_INIT
+#define TC_PT(ph) \
+  do {            \
+  } while (0)
+#endif
+
 struct Ctx {
   uint8_t* g;        // generic pointer to the aligned base
   uint32_t s;        // shared address of the aligned base
@@ -94,20 +115,68 @@ __device__ __forceinline__ void mbar_wait_drain_tc(uint32_t bar, uint32_t parity
 }
 
 // ---------------------------------------------------------------------------
+// Walks the CTA's tiles in order (one 128-row tile at a time) for the L2
+// prefetcher, which runs kPrefetchTiles ahead of the shared-memory loads.
+constexpr int kPrefetchTiles = 4;
+
+struct TileWalker {
+  PieceCursor cur;
+  Piece pc;
+  int r0 = 0;
+  bool have = false;
+  __device__ void init(const PieceCursor& c) {
+    cur = c;
+    have = cur.next(pc);
+    r0 = 0;
+  }
+  // Rows of the next tile: [row, row + nr). Returns false when done.
+  __device__ bool next(int32_t& row, int& nr) {
+    if (!have) return false;
+    row = pc.kv_row + r0;
+    nr = min(kTileRows, pc.nrows - r0);
+    r0 += kTileRows;
+    if (r0 >= pc.nrows) {
+      have = cur.next(pc);
+      r0 = 0;
+    }
+    return true;
+  }
+};
+
 // Warp 0: KV tiles, five 128-row x 128-byte boxes per tile (the last box is
-// half out of the tensor and zero-filled), into stage (tile % 2).
-__device__ void producer(const Ctx& cx, const CUtensorMap* map, PieceCursor cur, int lane) {
+// half out of the tensor and zero-filled), into stage (tile % 2). Each tile is
+// first prefetched into L2 kPrefetchTiles ahead (one line prefetch per lane
+// per 128 bytes), so HBM streams ahead of the two shared-memory stages and the
+// stage loads hit L2.
+__device__ void producer(const Ctx& cx, const CUtensorMap* map, const uint8_t* kv, PieceCursor cur, int lane) {
   const uint64_t pol = policy_evict_first();
+  TileWalker pf;
+  pf.init(cur);
+  auto prefetch_one = [&]() {
+    int32_t row;
+    int nr;
+    if (pf.next(row, nr)) {
+      // the tile's rows are contiguous: nr * 576 bytes, 128-byte lines spread over the lanes
+      const uint8_t* base = kv + static_cast<int64_t>(row) * kDqk;
+      const int lines = (nr * kDqk + 127) >> 7;
+      for (int i = lane; i < lines; i += 32) prefetch_line_l2(base + (i << 7));
+    }
+  };
+  for (int i = 0; i < kPrefetchTiles; ++i) prefetch_one();
   Piece pc;
   uint32_t n = 0;
   bool ok = true;
+  TC_PT_INIT
   while (ok && cur.next(pc)) {
     for (int r0 = 0; r0 < pc.nrows; r0 += kTileRows) {
       const uint32_t s = n & 1u;
+      TC_PT(1);
       if (n >= 2 && !cx.wait(L::kKvEmpty + s, ((n >> 1) - 1) & 1u)) {
         ok = false;
         break;
       }
+      TC_PT(0);
+      prefetch_one();
       if (lane == 0) {
         mbar_arrive_expect_tx(cx.bar(L::kKvFull + s), kStageBytes);
         const uint32_t dst = cx.s + L::kOffKv + s * kStageBytes;
@@ -134,8 +203,10 @@ struct PendingPV {
 
 __device__ bool issue_pv(const Ctx& cx, const PendingPV& t) {
   constexpr uint32_t id_pv = umma_idesc(128, 32, 0, 0, true, true);
+  TC_PT_INIT
   if (!cx.wait(L::kPFull + (t.n & 1u), (t.n >> 1) & 1u)) return false;
   if (t.first && t.k >= 2 && !cx.wait(L::kOEmpty + (t.k & 1u), ((t.k >> 1) - 1) & 1u)) return false;
+  TC_PT(4);
   tc_fence_after();
   const uint32_t stage = cx.s + L::kOffKv + (t.n & 1u) * kStageBytes;
   const uint32_t pbuf = cx.s + L::kOffP + (t.n & 1u) * kPBytes;
@@ -153,6 +224,7 @@ __device__ bool issue_pv(const Ctx& cx, const PendingPV& t) {
   umma_commit(cx.bar(L::kKvEmpty + (t.n & 1u)));
   umma_commit(cx.bar(L::kPEmpty + (t.n & 1u)));
   if (t.last) umma_commit(cx.bar(L::kOFull + (t.k & 1u)));
+  TC_PT(5);
   return true;
 }
 
@@ -162,15 +234,25 @@ __device__ void mma_issuer(const Ctx& cx, PieceCursor cur) {
   uint32_t n = 0, k = 0;
   PendingPV pend{0, 0, false, false, false};
   bool ok = true;
+  TC_PT_INIT
   while (ok && cur.next(pc)) {
+    TC_PT(7);
     if (!cx.wait(L::kQFull + (k & 1u), (k >> 1) & 1u)) break;
+    TC_PT(0);
     const uint32_t qbuf = cx.s + L::kOffQ + (k & 1u) * kQBytes;
     for (int r0 = 0; r0 < pc.nrows; r0 += kTileRows) {
       const uint32_t s = n & 1u;
-      if (!cx.wait(L::kKvFull + s, (n >> 1) & 1u) || (n >= 2 && !cx.wait(L::kSEmpty + s, ((n >> 1) - 1) & 1u))) {
+      TC_PT(7);
+      if (!cx.wait(L::kKvFull + s, (n >> 1) & 1u)) {
         ok = false;
         break;
       }
+      TC_PT(1);
+      if (n >= 2 && !cx.wait(L::kSEmpty + s, ((n >> 1) - 1) & 1u)) {
+        ok = false;
+        break;
+      }
+      TC_PT(2);
       tc_fence_after();
       const uint32_t stage = cx.s + L::kOffKv + s * kStageBytes;
 #pragma unroll
@@ -182,11 +264,15 @@ __device__ void mma_issuer(const Ctx& cx, PieceCursor cur) {
       umma_commit(cx.bar(L::kSFull + s));
       const bool last = r0 + kTileRows >= pc.nrows;
       if (last) umma_commit(cx.bar(L::kQEmpty + (k & 1u)));
+      TC_PT(3);
       if (pend.valid && !issue_pv(cx, pend)) {
         ok = false;
         break;
       }
       pend = PendingPV{n, k, r0 == 0, last, true};
+#ifdef MLA_PHASE_TIMING
+      tc_pt_ = clock64();
+#endif
       ++n;
     }
     ++k;
@@ -338,6 +424,7 @@ __device__ void softmax_role(const Stage1Params& p, const Ctx& cx, PieceCursor c
   float c = setup_q<QF>(p, cx, sx, pc.token, 0, kvsc);
   if (c < 0.f) return;
   uint32_t n = 0, k = 0;
+  TC_PT_INIT
   while (have) {
     const bool have_next = ahead.next(nxt);
     float m[16], l[16];
@@ -349,7 +436,9 @@ __device__ void softmax_role(const Stage1Params& p, const Ctx& cx, PieceCursor c
     for (int r0 = 0; r0 < pc.nrows; r0 += kTileRows) {
       const int nr = min(kTileRows, pc.nrows - r0);
       const uint32_t s = n & 1u;
+      TC_PT(7);
       if (!cx.wait(L::kSFull + s, (n >> 1) & 1u)) return;
+      TC_PT(0);
       tc_fence_after();
       uint32_t sr[32];
       tmem_ld32(cx.tmem + sx.lane_base + kTmemS + 32 * s, sr);
@@ -367,7 +456,9 @@ __device__ void softmax_role(const Stage1Params& p, const Ctx& cx, PieceCursor c
       const float wm = warp_reduce16<true>(x, lane);
       float* rm = red_max + (n & 1u) * 64;
       if ((lane & 1) == 0) rm[sx.wi * 16 + (lane >> 1)] = wm;
+      TC_PT(1);
       if (!group_sync(cx, sx)) return;
+      TC_PT(2);
       bool grew = false;
       float alpha[16];
 #pragma unroll
@@ -396,7 +487,9 @@ __device__ void softmax_role(const Stage1Params& p, const Ctx& cx, PieceCursor c
         lo[q4] = f32x2_to_e4m3x2(kLoScale * (pv[0] - d01.x), kLoScale * (pv[1] - d01.y)) |
                  (f32x2_to_e4m3x2(kLoScale * (pv[2] - d23.x), kLoScale * (pv[3] - d23.y)) << 16);
       }
+      TC_PT(3);
       if (n >= 2 && !cx.wait(L::kPEmpty + s, ((n >> 1) - 1) & 1u)) return;
+      TC_PT(4);
       uint8_t* pb = cx.g + L::kOffP + s * kPBytes + (sx.row >> 3) * 256 + (sx.row & 7) * 16;
       *reinterpret_cast<uint4*>(pb) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
       *reinterpret_cast<uint4*>(pb + 128) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
@@ -428,6 +521,7 @@ __device__ void softmax_role(const Stage1Params& p, const Ctx& cx, PieceCursor c
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(cx.bar(L::kPFull + s));
+      TC_PT(5);
       ++n;
     }
 
@@ -472,6 +566,7 @@ __device__ void softmax_role(const Stage1Params& p, const Ctx& cx, PieceCursor c
     tc_fence_before();
     __syncwarp();
     if (lane == 0) mbar_arrive(cx.bar(L::kOEmpty + (k & 1u)));
+    TC_PT(6);
     pc = nxt;
     have = have_next;
     c = c_next;
@@ -525,7 +620,7 @@ __global__ void __launch_bounds__(kThreads, 1) stage1_tc_kernel(const Stage1Para
   cx.tmem = *reinterpret_cast<volatile uint32_t*>(cx.g + L::kOffSlot);
   PieceCursor cur{p.qo_indptr, p.kv_indptr, p.batch, x0, x1, loc.seg, loc.seg_vs, c};
   if (warp == 0)
-    producer(cx, &kvmap, cur, lane);
+    producer(cx, &kvmap, static_cast<const uint8_t*>(p.kv), cur, lane);
   else if (warp == 1) {
     if (lane == 0) mma_issuer(cx, cur);
     __syncwarp();
@@ -567,6 +662,19 @@ static cudaError_t make_kv_map(CUtensorMap* map, const void* kv, int64_t total_k
                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
+
+#ifdef MLA_PHASE_TIMING
+extern "C" int mla_debug_phase_cycles_tc(unsigned long long* host, int n, int reset) {
+  if (n > kPhaseCtas * 64) n = kPhaseCtas * 64;
+  if (cudaMemcpyFromSymbol(host, g_tc_phase, sizeof(unsigned long long) * n) != cudaSuccess) return -1;
+  if (reset) {
+    void* q = nullptr;
+    if (cudaGetSymbolAddress(&q, g_tc_phase) != cudaSuccess) return -1;
+    if (cudaMemset(q, 0, sizeof(g_tc_phase)) != cudaSuccess) return -1;
+  }
+  return n;
+}
+#endif
 
 template <int QF>
 static cudaError_t launch_q(const Stage1Params& p, cudaStream_t stream) {
