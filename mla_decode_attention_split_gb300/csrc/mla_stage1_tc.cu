@@ -20,11 +20,15 @@
 //    with N = 16, and hi + lo/16 carries x to 8 significant bits wherever hi is
 //    a normal number. The per-tensor kv scale, 2^-shift of q and 1/256 of P are
 //    applied to the fp32 results.
-//  * Warp 0 issues the TMA loads (two 80 KB stages: five 128B-swizzled 128x128
-//    boxes per 128-row tile), warp 1 owns tensor memory and issues QK(n) then
-//    PV(n-1) so the tensor core overlaps the softmax of tile n, warps 2-5 (one
-//    thread per tile row / tensor-memory lane) read S, reduce the per-head max
-//    across the 128 rows, write P into shared memory, rescale O in tensor
+//  * Shared memory holds three 64 KB stages of the 512 V dims of 128-row tiles
+//    (four 128B-swizzled 128x128 TMA boxes each), so two tiles stream in while
+//    one is consumed. The 64 rope dims of each row (used by Q.K^T only) are
+//    loaded by the softmax threads into registers two tiles ahead and written
+//    into a single 8 KB slot as soon as the previous tile's Q.K^T is done.
+//  * Warp 0 issues the TMA loads, warp 1 owns tensor memory and issues QK(n)
+//    then PV(n-1) so the tensor core overlaps the softmax of tile n, warps 2-5
+//    (one thread per tile row / tensor-memory lane) read S, reduce the per-head
+//    max across the 128 rows, write P into shared memory, rescale O in tensor
 //    memory only when some head's running max grew, and run the epilogue.
 //  * Every mbarrier wait is bounded; on a timeout the CTA stops issuing work,
 //    lets in-flight copies and MMAs finish, frees tensor memory and returns.
@@ -39,15 +43,16 @@
 namespace mla {
 namespace tc {
 
-constexpr int kThreads = 192;                       // warp 0 TMA, warp 1 MMA, warps 2-5 softmax
+constexpr int kThreads = 192;                        // warp 0 TMA, warp 1 MMA, warps 2-5 softmax
 constexpr int kTileRows = 128;
-constexpr int kChunks = 5;                          // 128-byte column chunks of a 576-byte row
-constexpr int kChunkBytes = kTileRows * 128;        // 16 KB (one TMA box)
-constexpr int kStageBytes = kChunks * kChunkBytes;  // 80 KB
-constexpr int kStages = 2;
-constexpr int kQChunkBytes = 32 * 128;              // 32 B-operand rows (hi, lo) x 128 B
-constexpr int kQBytes = kChunks * kQChunkBytes;     // 20 KB
-constexpr int kPBytes = kTileRows * 32;             // [row group][hi | lo][8 rows][16 heads]
+constexpr int kVChunks = 4;                          // 128-byte column chunks of the 512 V dims
+constexpr int kChunkBytes = kTileRows * 128;         // 16 KB (one TMA box)
+constexpr int kStageBytes = kVChunks * kChunkBytes;  // 64 KB
+constexpr int kStages = 3;
+constexpr int kQChunkBytes = 32 * 128;               // 32 B-operand rows (hi, lo) x 128 B
+constexpr int kQBytes = 5 * kQChunkBytes;            // 20 KB (chunk 4: rope dims, 64 B used)
+constexpr int kRopeBytes = kTileRows * 64;           // [row group 16][16-B column 4][8 rows][16 B]
+constexpr int kPBytes = kTileRows * 32;              // [row group][hi | lo][8 rows][16 heads]
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kTmemS = 0;                      // 2 buffers x 32 columns
 constexpr uint32_t kTmemO = 64;                     // 2 buffers x (4 blocks x 32 columns)
@@ -58,15 +63,16 @@ constexpr float kLog2e = 1.4426950408889634f;
 struct L {
   static constexpr int kOffKv = 0;
   static constexpr int kOffQ = kOffKv + kStages * kStageBytes;
-  static constexpr int kOffP = kOffQ + 2 * kQBytes;
-  static constexpr int kOffRedMax = kOffP + 2 * kPBytes;          // [2][4][16] f32
+  static constexpr int kOffRope = kOffQ + kQBytes;
+  static constexpr int kOffP = kOffRope + kRopeBytes;
+  static constexpr int kOffRedMax = kOffP + kPBytes;              // [2][4][16] f32
   static constexpr int kOffRedL = kOffRedMax + 2 * 4 * 16 * 4;    // [4][16] f32
   static constexpr int kOffAmax = kOffRedL + 4 * 16 * 4;          // [4] u32
   static constexpr int kOffScan = kOffAmax + 16;                  // 16 x i64
   static constexpr int kOffBars = kOffScan + 16 * 8;
   enum {
-    kKvFull = 0, kKvEmpty = 2, kSFull = 4, kSEmpty = 6, kPFull = 8, kPEmpty = 10, kQFull = 12, kQEmpty = 14,
-    kOFull = 16, kOEmpty = 18, kGrp = 20, kDrain = 22, kNumBars = 23
+    kKvFull = 0, kKvEmpty = 3, kSFull = 6, kSEmpty = 8, kRopeFull = 10, kPFull = 11, kPEmpty = 12, kQFull = 13,
+    kQEmpty = 14, kOFull = 15, kOEmpty = 17, kGrp = 19, kDrain = 21, kNumBars = 22
   };
   static constexpr int kOffSlot = kOffBars + kNumBars * 8;
   static constexpr int kOffAbort = kOffSlot + 8;
@@ -74,7 +80,7 @@ struct L {
   static constexpr int kAlloc = kBytes + 1024;  // slack: the base is aligned up to 1024 B
 };
 static_assert(L::kAlloc <= 227 * 1024, "shared memory budget");
-static_assert(L::kOffQ % 1024 == 0 && L::kOffP % 1024 == 0, "swizzled operands need 1024-byte alignment");
+static_assert(L::kOffQ % 1024 == 0 && L::kOffRope % 1024 == 0, "operands need 1024-byte alignment");
 
 // Optional phase timers (build with -DMLA_PHASE_TIMING): cycles per CTA, warp
 // and phase, summed over the launch. Off by default.
@@ -115,10 +121,7 @@ __device__ __forceinline__ void mbar_wait_drain_tc(uint32_t bar, uint32_t parity
 }
 
 // ---------------------------------------------------------------------------
-// Walks the CTA's tiles in order (one 128-row tile at a time) for the L2
-// prefetcher, which runs kPrefetchTiles ahead of the shared-memory loads.
-constexpr int kPrefetchTiles = 4;
-
+// Walks the CTA's tiles in order (one 128-row tile at a time).
 struct TileWalker {
   PieceCursor cur;
   Piece pc;
@@ -129,11 +132,10 @@ struct TileWalker {
     have = cur.next(pc);
     r0 = 0;
   }
-  // Rows of the next tile: [row, row + nr). Returns false when done.
-  __device__ bool next(int32_t& row, int& nr) {
+  // First KV row of the next tile. Returns false when done.
+  __device__ bool next(int32_t& row) {
     if (!have) return false;
     row = pc.kv_row + r0;
-    nr = min(kTileRows, pc.nrows - r0);
     r0 += kTileRows;
     if (r0 >= pc.nrows) {
       have = cur.next(pc);
@@ -143,44 +145,27 @@ struct TileWalker {
   }
 };
 
-// Warp 0: KV tiles, five 128-row x 128-byte boxes per tile (the last box is
-// half out of the tensor and zero-filled), into stage (tile % 2). Each tile is
-// first prefetched into L2 kPrefetchTiles ahead (one line prefetch per lane
-// per 128 bytes), so HBM streams ahead of the two shared-memory stages and the
-// stage loads hit L2.
-__device__ void producer(const Ctx& cx, const CUtensorMap* map, const uint8_t* kv, PieceCursor cur, int lane) {
+// Warp 0: the V dims of each tile, four 128-row x 128-byte boxes, into stage
+// (tile % 3) once the tile three back has been released by its P.V.
+__device__ void producer(const Ctx& cx, const CUtensorMap* map, PieceCursor cur, int lane) {
   const uint64_t pol = policy_evict_first();
-  TileWalker pf;
-  pf.init(cur);
-  auto prefetch_one = [&]() {
-    int32_t row;
-    int nr;
-    if (pf.next(row, nr)) {
-      // the tile's rows are contiguous: nr * 576 bytes, 128-byte lines spread over the lanes
-      const uint8_t* base = kv + static_cast<int64_t>(row) * kDqk;
-      const int lines = (nr * kDqk + 127) >> 7;
-      for (int i = lane; i < lines; i += 32) prefetch_line_l2(base + (i << 7));
-    }
-  };
-  for (int i = 0; i < kPrefetchTiles; ++i) prefetch_one();
   Piece pc;
   uint32_t n = 0;
   bool ok = true;
   TC_PT_INIT
   while (ok && cur.next(pc)) {
     for (int r0 = 0; r0 < pc.nrows; r0 += kTileRows) {
-      const uint32_t s = n & 1u;
+      const uint32_t s = n % kStages, rnd = n / kStages;
       TC_PT(1);
-      if (n >= 2 && !cx.wait(L::kKvEmpty + s, ((n >> 1) - 1) & 1u)) {
+      if (rnd >= 1 && !cx.wait(L::kKvEmpty + s, (rnd - 1) & 1u)) {
         ok = false;
         break;
       }
       TC_PT(0);
-      prefetch_one();
       if (lane == 0) {
         mbar_arrive_expect_tx(cx.bar(L::kKvFull + s), kStageBytes);
         const uint32_t dst = cx.s + L::kOffKv + s * kStageBytes;
-        for (int c = 0; c < kChunks; ++c)
+        for (int c = 0; c < kVChunks; ++c)
           tma_load_2d(dst + c * kChunkBytes, map, c * 128, pc.kv_row + r0, cx.bar(L::kKvFull + s), pol);
       }
       __syncwarp();
@@ -188,9 +173,9 @@ __device__ void producer(const Ctx& cx, const CUtensorMap* map, const uint8_t* k
     }
   }
   // the last tile issued on each stage must have landed before the CTA exits
-  for (uint32_t s = 0; s < 2 && s < n; ++s) {
-    const uint32_t last = ((n - 1 - s) >> 1) * 2 + s;
-    mbar_wait_drain_tc(cx.bar(L::kKvFull + s), (last >> 1) & 1u);
+  for (uint32_t s = 0; s < kStages && s < n; ++s) {
+    const uint32_t last = ((n - 1 - s) / kStages) * kStages + s;
+    mbar_wait_drain_tc(cx.bar(L::kKvFull + s), (last / kStages) & 1u);
   }
 }
 
@@ -204,12 +189,12 @@ struct PendingPV {
 __device__ bool issue_pv(const Ctx& cx, const PendingPV& t) {
   constexpr uint32_t id_pv = umma_idesc(128, 32, 0, 0, true, true);
   TC_PT_INIT
-  if (!cx.wait(L::kPFull + (t.n & 1u), (t.n >> 1) & 1u)) return false;
+  if (!cx.wait(L::kPFull, t.n & 1u)) return false;
   if (t.first && t.k >= 2 && !cx.wait(L::kOEmpty + (t.k & 1u), ((t.k >> 1) - 1) & 1u)) return false;
   TC_PT(4);
   tc_fence_after();
-  const uint32_t stage = cx.s + L::kOffKv + (t.n & 1u) * kStageBytes;
-  const uint32_t pbuf = cx.s + L::kOffP + (t.n & 1u) * kPBytes;
+  const uint32_t stage = cx.s + L::kOffKv + (t.n % kStages) * kStageBytes;
+  const uint32_t pbuf = cx.s + L::kOffP;
   const uint32_t obuf = cx.tmem + kTmemO + (t.k & 1u) * 128;
 #pragma unroll
   for (int mb = 0; mb < 4; ++mb)
@@ -221,8 +206,8 @@ __device__ bool issue_pv(const Ctx& cx, const PendingPV& t) {
       const uint64_t b = smem_desc(pbuf + ks * 1024, 256, 128, kLayoutNone);
       umma_e4m3(obuf + 32 * mb, a, b, id_pv, (ks > 0 || !t.first) ? 1u : 0u);
     }
-  umma_commit(cx.bar(L::kKvEmpty + (t.n & 1u)));
-  umma_commit(cx.bar(L::kPEmpty + (t.n & 1u)));
+  umma_commit(cx.bar(L::kKvEmpty + (t.n % kStages)));
+  umma_commit(cx.bar(L::kPEmpty));
   if (t.last) umma_commit(cx.bar(L::kOFull + (t.k & 1u)));
   TC_PT(5);
   return true;
@@ -237,13 +222,13 @@ __device__ void mma_issuer(const Ctx& cx, PieceCursor cur) {
   TC_PT_INIT
   while (ok && cur.next(pc)) {
     TC_PT(7);
-    if (!cx.wait(L::kQFull + (k & 1u), (k >> 1) & 1u)) break;
+    if (!cx.wait(L::kQFull, k & 1u)) break;
     TC_PT(0);
-    const uint32_t qbuf = cx.s + L::kOffQ + (k & 1u) * kQBytes;
+    const uint32_t qbuf = cx.s + L::kOffQ;
     for (int r0 = 0; r0 < pc.nrows; r0 += kTileRows) {
-      const uint32_t s = n & 1u;
+      const uint32_t s = n & 1u, st = n % kStages;
       TC_PT(7);
-      if (!cx.wait(L::kKvFull + s, (n >> 1) & 1u)) {
+      if (!cx.wait(L::kKvFull + st, (n / kStages) & 1u) || !cx.wait(L::kRopeFull, n & 1u)) {
         ok = false;
         break;
       }
@@ -254,16 +239,22 @@ __device__ void mma_issuer(const Ctx& cx, PieceCursor cur) {
       }
       TC_PT(2);
       tc_fence_after();
-      const uint32_t stage = cx.s + L::kOffKv + s * kStageBytes;
+      const uint32_t stage = cx.s + L::kOffKv + st * kStageBytes;
 #pragma unroll
-      for (int ks = 0; ks < 18; ++ks) {
+      for (int ks = 0; ks < 16; ++ks) {  // the 512 V dims, from the stage
         const uint64_t a = smem_desc(stage + (ks >> 2) * kChunkBytes + (ks & 3) * 32, 16, 1024, kLayoutSw128);
         const uint64_t b = smem_desc(qbuf + (ks >> 2) * kQChunkBytes + (ks & 3) * 32, 16, 1024, kLayoutSw128);
         umma_e4m3(cx.tmem + kTmemS + 32 * s, a, b, id_qk, ks > 0 ? 1u : 0u);
       }
+#pragma unroll
+      for (int ks = 0; ks < 2; ++ks) {  // the 64 rope dims, from the rope slot (no swizzle)
+        const uint64_t a = smem_desc(cx.s + L::kOffRope + ks * 256, 128, 512, kLayoutNone);
+        const uint64_t b = smem_desc(qbuf + 4 * kQChunkBytes + ks * 32, 16, 1024, kLayoutSw128);
+        umma_e4m3(cx.tmem + kTmemS + 32 * s, a, b, id_qk, 1u);
+      }
       umma_commit(cx.bar(L::kSFull + s));
       const bool last = r0 + kTileRows >= pc.nrows;
-      if (last) umma_commit(cx.bar(L::kQEmpty + (k & 1u)));
+      if (last) umma_commit(cx.bar(L::kQEmpty));
       TC_PT(3);
       if (pend.valid && !issue_pv(cx, pend)) {
         ok = false;
@@ -342,10 +333,11 @@ __device__ __forceinline__ bool group_sync(const Ctx& cx, SoftmaxCtx& sx) {
 // Returns the score scale (exp2 domain) or a negative value on abort.
 template <int QF>
 __device__ float setup_q(const Stage1Params& p, const Ctx& cx, SoftmaxCtx& sx, int token, uint32_t kk, float kvsc) {
-  if (kk >= 2 && !cx.wait(L::kQEmpty + (kk & 1u), ((kk >> 1) - 1) & 1u)) return -1.f;
+  // the single Q buffer is free once the previous piece's last Q.K^T is done
+  if (kk >= 1 && !cx.wait(L::kQEmpty, (kk - 1) & 1u)) return -1.f;
   const int t = 32 * sx.wi + sx.lane;  // 0..127
   const int h = t >> 3, d0 = 72 * (t & 7);
-  uint8_t* qb = cx.g + L::kOffQ + (kk & 1u) * kQBytes;
+  uint8_t* qb = cx.g + L::kOffQ;
   auto qaddr = [&](int row, int d) -> uint32_t* {
     const int unit = (d & 127) >> 4;
     return reinterpret_cast<uint32_t*>(qb + (d >> 7) * kQChunkBytes + (row >> 3) * 1024 + (row & 7) * 128 +
@@ -401,8 +393,36 @@ __device__ float setup_q(const Stage1Params& p, const Ctx& cx, SoftmaxCtx& sx, i
   }
   fence_async_smem();
   __syncwarp();
-  if (sx.lane == 0) mbar_arrive(cx.bar(L::kQFull + (kk & 1u)));
+  if (sx.lane == 0) mbar_arrive(cx.bar(L::kQFull));
   return c;
+}
+
+// Rope dims (bytes 512..575) of one tile row, from global memory into registers;
+// rows past the end of the cache read as zero.
+__device__ __forceinline__ void load_rope(const Stage1Params& p, TileWalker& rw, int row, uint4 (&r)[4]) {
+  int32_t row0;
+  const bool have = rw.next(row0);
+  const int64_t g = static_cast<int64_t>(row0) + row;
+  if (have && g < p.total_kv) {
+    const uint4* src = reinterpret_cast<const uint4*>(static_cast<const uint8_t*>(p.kv) + g * kDqk + 512);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) r[i] = __ldg(src + i);
+  } else {
+#pragma unroll
+    for (int i = 0; i < 4; ++i) r[i] = make_uint4(0u, 0u, 0u, 0u);
+  }
+}
+
+// Writes one row's rope bytes into the slot (no-swizzle K-major A operand:
+// 8-row x 16-byte core matrices, 128 B apart along K, 512 B apart along rows)
+// and hands the slot to the MMA warp.
+__device__ __forceinline__ void store_rope(const Ctx& cx, const SoftmaxCtx& sx, const uint4 (&r)[4]) {
+  uint8_t* base = cx.g + L::kOffRope + (sx.row >> 3) * 512 + (sx.row & 7) * 16;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) *reinterpret_cast<uint4*>(base + i * 128) = r[i];
+  fence_async_smem();
+  __syncwarp();
+  if (sx.lane == 0) mbar_arrive(cx.bar(L::kRopeFull));
 }
 
 template <int QF>
@@ -421,9 +441,24 @@ __device__ void softmax_role(const Stage1Params& p, const Ctx& cx, PieceCursor c
   Piece pc, nxt;
   bool have = ahead.next(pc);
   if (!have) return;
+  // rope of tiles 0 and 1 into registers; tile 0 into the slot; tile 2 loads
+  TileWalker rw;
+  rw.init(cur);
+  uint4 rb0[4], rb1[4];  // rope of the even / odd tile in flight
+  load_rope(p, rw, sx.row, rb0);
+  load_rope(p, rw, sx.row, rb1);
+  store_rope(cx, sx, rb0);
+  load_rope(p, rw, sx.row, rb0);
   float c = setup_q<QF>(p, cx, sx, pc.token, 0, kvsc);
   if (c < 0.f) return;
   uint32_t n = 0, k = 0;
+  int tiles_left = 0;  // tiles of the CTA after the current one (for the rope slot)
+  {
+    PieceCursor cnt = cur;
+    Piece t;
+    while (cnt.next(t)) tiles_left += (t.nrows + kTileRows - 1) / kTileRows;
+    tiles_left -= 1;
+  }
   TC_PT_INIT
   while (have) {
     const bool have_next = ahead.next(nxt);
@@ -439,6 +474,17 @@ __device__ void softmax_role(const Stage1Params& p, const Ctx& cx, PieceCursor c
       TC_PT(7);
       if (!cx.wait(L::kSFull + s, (n >> 1) & 1u)) return;
       TC_PT(0);
+      // Q.K^T(n) is done: the rope slot takes tile n+1, its registers tile n+3
+      if (tiles_left > 0) {
+        if (n & 1u) {
+          store_rope(cx, sx, rb0);
+          load_rope(p, rw, sx.row, rb0);
+        } else {
+          store_rope(cx, sx, rb1);
+          load_rope(p, rw, sx.row, rb1);
+        }
+      }
+      --tiles_left;
       tc_fence_after();
       uint32_t sr[32];
       tmem_ld32(cx.tmem + sx.lane_base + kTmemS + 32 * s, sr);
@@ -488,22 +534,22 @@ __device__ void softmax_role(const Stage1Params& p, const Ctx& cx, PieceCursor c
                  (f32x2_to_e4m3x2(kLoScale * (pv[2] - d23.x), kLoScale * (pv[3] - d23.y)) << 16);
       }
       TC_PT(3);
-      if (n >= 2 && !cx.wait(L::kPEmpty + s, ((n >> 1) - 1) & 1u)) return;
+      // single P buffer: P.V(n-1) must be done
+      if (n >= 1 && !cx.wait(L::kPEmpty, (n - 1) & 1u)) return;
       TC_PT(4);
-      uint8_t* pb = cx.g + L::kOffP + s * kPBytes + (sx.row >> 3) * 256 + (sx.row & 7) * 16;
+      uint8_t* pb = cx.g + L::kOffP + (sx.row >> 3) * 256 + (sx.row & 7) * 16;
       *reinterpret_cast<uint4*>(pb) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
       *reinterpret_cast<uint4*>(pb + 128) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
       if (!valid) {
         // rows past the piece: zero their V bytes so P = 0 meets finite values
-        uint8_t* vrow = cx.g + L::kOffKv + s * kStageBytes + sx.row * 128;
+        uint8_t* vrow = cx.g + L::kOffKv + (n % kStages) * kStageBytes + sx.row * 128;
 #pragma unroll
         for (int ch = 0; ch < 4; ++ch)
 #pragma unroll
           for (int u = 0; u < 8; ++u) *reinterpret_cast<uint4*>(vrow + ch * kChunkBytes + u * 16) = make_uint4(0, 0, 0, 0);
       }
       if (rescale) {
-        // O of this piece is final for tile n-1 once PV(n-1) has completed
-        if (!cx.wait(L::kPEmpty + ((n - 1) & 1u), ((n - 1) >> 1) & 1u)) return;
+        // O of this piece is final for tile n-1: P.V(n-1) completed (waited above)
         tc_fence_after();
         const uint32_t ob = cx.tmem + sx.lane_base + kTmemO + (k & 1u) * 128;
 #pragma unroll
@@ -520,7 +566,7 @@ __device__ void softmax_role(const Stage1Params& p, const Ctx& cx, PieceCursor c
       fence_async_smem();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(cx.bar(L::kPFull + s));
+      if (lane == 0) mbar_arrive(cx.bar(L::kPFull));
       TC_PT(5);
       ++n;
     }
@@ -585,19 +631,22 @@ __global__ void __launch_bounds__(kThreads, 1) stage1_tc_kernel(const Stage1Para
   cx.flags = p.dev_flags;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
-    for (int i = 0; i < 2; ++i) {
+    for (int i = 0; i < kStages; ++i) {
       mbar_init(cx.bar(L::kKvFull + i), 1);
       mbar_init(cx.bar(L::kKvEmpty + i), 1);
+    }
+    for (int i = 0; i < 2; ++i) {
       mbar_init(cx.bar(L::kSFull + i), 1);
       mbar_init(cx.bar(L::kSEmpty + i), 4);
-      mbar_init(cx.bar(L::kPFull + i), 4);
-      mbar_init(cx.bar(L::kPEmpty + i), 1);
-      mbar_init(cx.bar(L::kQFull + i), 4);
-      mbar_init(cx.bar(L::kQEmpty + i), 1);
       mbar_init(cx.bar(L::kOFull + i), 1);
       mbar_init(cx.bar(L::kOEmpty + i), 4);
       mbar_init(cx.bar(L::kGrp + i), 4);
     }
+    mbar_init(cx.bar(L::kRopeFull), 4);
+    mbar_init(cx.bar(L::kPFull), 4);
+    mbar_init(cx.bar(L::kPEmpty), 1);
+    mbar_init(cx.bar(L::kQFull), 4);
+    mbar_init(cx.bar(L::kQEmpty), 1);
     mbar_init(cx.bar(L::kDrain), 1);
     *cx.abort_word = 0u;
     fence_mbar_init();
@@ -620,7 +669,7 @@ __global__ void __launch_bounds__(kThreads, 1) stage1_tc_kernel(const Stage1Para
   cx.tmem = *reinterpret_cast<volatile uint32_t*>(cx.g + L::kOffSlot);
   PieceCursor cur{p.qo_indptr, p.kv_indptr, p.batch, x0, x1, loc.seg, loc.seg_vs, c};
   if (warp == 0)
-    producer(cx, &kvmap, static_cast<const uint8_t*>(p.kv), cur, lane);
+    producer(cx, &kvmap, cur, lane);
   else if (warp == 1) {
     if (lane == 0) mma_issuer(cx, cur);
     __syncwarp();

@@ -100,10 +100,4 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst_smem, const CUtensorMap
       : "memory");
 }
 
-// Prefetch the cache line holding `p` into L2 through the load/store path
-// (keeps the TMA engine free for the shared-memory loads).
-__device__ __forceinline__ void prefetch_line_l2(const void* p) {
-  asm volatile("prefetch.global.L2::evict_last [%0];" ::"l"(p));
-}
-
 }  // namespace mla
