@@ -63,8 +63,11 @@ typedef enum {
   MLA_ERR_WORKSPACE = 3,    /* workspace missing or smaller than required     */
   MLA_ERR_CUDA = 4,         /* a CUDA runtime call failed                     */
   MLA_ERR_TIMEOUT = 5,      /* device flag: a bounded wait in a kernel expired */
-  MLA_ERR_DEVICE_CHECK = 6  /* device flag: indptr arrays failed the kernels'
+  MLA_ERR_DEVICE_CHECK = 6, /* device flag: indptr arrays failed the kernels'
                                bounds/monotonicity checks; work was skipped   */
+  MLA_ERR_TOO_LARGE = 7     /* the call needs more scratch than the library's
+                               fixed device array holds (see
+                               mla_decode_static_workspace)                   */
 } mla_status_t;
 
 /* Device error flags, as returned by mla_get_device_error().                  */
@@ -172,6 +175,35 @@ mla_status_t mla_reset_device_error(void* workspace, void* stream);
  * have completed, e.g. the profile_events of mla_decode_opts. Synchronises
  * on ev_end. Errors: MLA_ERR_INVALID_ARG (NULL), MLA_ERR_CUDA.                */
 mla_status_t mla_event_elapsed_ms(void* ev_start, void* ev_end, float* ms);
+
+/* The decode for callers that cannot allocate device memory. Not part of the
+ * method on the pages (they have no counterpart): it exists for callers that
+ * must not call cudaMalloc at decode time -- code that runs while a CUDA
+ * stream is being captured into a graph, or engines that reserve all device
+ * memory up front and forbid allocations afterwards -- and so cannot provide
+ * the workspace that mla_decode() needs.
+ *
+ * Same arguments and results as mla_decode(); opts->workspace and
+ * opts->workspace_bytes are ignored. The scratch (device error flags and
+ * per-split partials) is a fixed MLA_STATIC_WORKSPACE_BYTES array inside the
+ * library, reserved on every GPU that loads the library until the process
+ * exits. This call allocates nothing: no cudaMalloc/cudaFree and no
+ * allocating library routine.
+ *   - The first call on a device looks up the array's device address
+ *     (cudaGetSymbolAddress) and caches it; make that first call before any
+ *     stream capture.
+ *   - Calls whose scratch need (mla_decode_workspace_size()) exceeds
+ *     MLA_STATIC_WORKSPACE_BYTES return MLA_ERR_TOO_LARGE and launch nothing.
+ *   - Every call shares the one array and clears its error flags at the start;
+ *     two calls that overlap on the GPU (different streams, no ordering) race
+ *     on it and produce undefined results. Calls on one stream are ordered.
+ *   - The device error flags of this entry point are not readable by the
+ *     caller; argument errors are returned as for mla_decode().              */
+#define MLA_STATIC_WORKSPACE_BYTES (16u * 1024u * 1024u)
+mla_status_t mla_decode_static_workspace(const void* q, const void* kv, const void* kv_scale,
+                                         const int32_t* qo_indptr, const int32_t* kv_indptr,
+                                         void* out, mla_dtype_t kv_dtype,
+                                         const mla_decode_opts* opts, void* stream);
 
 /* Static description of a status code.                                        */
 const char* mla_status_string(mla_status_t status);

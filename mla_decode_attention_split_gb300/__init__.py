@@ -21,7 +21,10 @@ MLA_ERR_CUDA, MLA_ERR_TIMEOUT, MLA_ERR_DEVICE_CHECK = 4, 5, 6
 DEVFLAG_TIMEOUT, DEVFLAG_BAD_INDPTR = 0x1, 0x2
 
 EXPORTED = ("mla_plan", "mla_decode_workspace_size", "mla_decode", "mla_decode_from_host", "mla_dequant_rows",
-            "mla_get_device_error", "mla_reset_device_error", "mla_event_elapsed_ms", "mla_status_string")
+            "mla_get_device_error", "mla_reset_device_error", "mla_event_elapsed_ms", "mla_decode_static_workspace",
+            "mla_status_string")
+MLA_ERR_TOO_LARGE = 7
+STATIC_WORKSPACE_BYTES = 16 * 1024 * 1024
 
 
 class MlaError(RuntimeError):
@@ -70,6 +73,7 @@ def lib():
             L.mla_get_device_error.argtypes = [P, P, ctypes.POINTER(ctypes.c_uint32)]
             L.mla_reset_device_error.argtypes = [P, P]
             L.mla_event_elapsed_ms.argtypes = [P, P, ctypes.POINTER(ctypes.c_float)]
+            L.mla_decode_static_workspace.argtypes = [P, P, P, P, P, P, st, ctypes.POINTER(DecodeOpts), P]
             L.mla_status_string.argtypes = [st]
             L.mla_status_string.restype = ctypes.c_char_p
             for name in EXPORTED[:-1]:

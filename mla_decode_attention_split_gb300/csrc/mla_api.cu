@@ -64,6 +64,8 @@ const char* mla_status_string(mla_status_t s) {
     case MLA_ERR_CUDA: return "MLA_ERR_CUDA: CUDA runtime error";
     case MLA_ERR_TIMEOUT: return "MLA_ERR_TIMEOUT: a bounded device wait expired";
     case MLA_ERR_DEVICE_CHECK: return "MLA_ERR_DEVICE_CHECK: indptr arrays failed the device checks";
+    case MLA_ERR_TOO_LARGE:
+      return "MLA_ERR_TOO_LARGE: the call needs more scratch than the library's fixed device array holds";
   }
   return "unknown mla_status_t";
 }
@@ -229,3 +231,40 @@ mla_status_t mla_event_elapsed_ms(void* ev_start, void* ev_end, float* ms) {
 }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------------------
+// The allocation-free variant: the workspace is this fixed device array.
+namespace {
+
+static __device__ __align__(256) unsigned char g_static_workspace[MLA_STATIC_WORKSPACE_BYTES];
+
+// Device address of g_static_workspace on each device, looked up on the first
+// call made with that device current (the host-side symbol is not an address).
+void* g_static_ws_ptr[kMaxDevices] = {nullptr};
+
+}  // namespace
+
+extern "C" mla_status_t mla_decode_static_workspace(const void* q, const void* kv, const void* kv_scale,
+                                                    const int32_t* qo_indptr, const int32_t* kv_indptr, void* out,
+                                                    mla_dtype_t kv_dtype, const mla_decode_opts* opts, void* stream) {
+  if (!opts) return MLA_ERR_INVALID_ARG;
+  if (opts->batch < 1 || opts->total_q < 0 || opts->total_kv < 0 || opts->num_splits < 0 ||
+      opts->num_splits > kMaxSplits)
+    return MLA_ERR_INVALID_ARG;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return MLA_ERR_CUDA;
+  if (!g_static_ws_ptr[dev]) {
+    void* ptr = nullptr;
+    if (cudaGetSymbolAddress(&ptr, g_static_workspace) != cudaSuccess || !ptr) return MLA_ERR_CUDA;
+    g_static_ws_ptr[dev] = ptr;
+  }
+  mla_decode_opts o = *opts;
+  if (o.num_splits == 0) o.num_splits = plan_splits(o.total_q, o.batch, o.total_kv, sm_count_of_current_device());
+  if (mla::workspace_bytes_for(o.num_splits, o.total_q) > MLA_STATIC_WORKSPACE_BYTES) return MLA_ERR_TOO_LARGE;
+  // the error flags are the only scratch that must start at zero
+  if (cudaMemsetAsync(g_static_ws_ptr[dev], 0, sizeof(uint32_t), static_cast<cudaStream_t>(stream)) != cudaSuccess)
+    return MLA_ERR_CUDA;
+  o.workspace = g_static_ws_ptr[dev];
+  o.workspace_bytes = MLA_STATIC_WORKSPACE_BYTES;
+  return mla_decode(q, kv, kv_scale, qo_indptr, kv_indptr, out, kv_dtype, &o, stream);
+}

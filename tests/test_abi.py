@@ -43,7 +43,7 @@ def test_library_is_built_for_sm103a_only(lib):
 
 
 def test_status_strings(lib):
-    for s in range(7):
+    for s in range(8):
         assert m.status_string(s).startswith("MLA_")
     assert "unknown" in m.status_string(99)
 
