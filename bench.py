@@ -33,7 +33,7 @@ sys.path.insert(0, ROOT)
 
 HEADLINE = "fp8kv_bs256_kv8192"
 METRIC = "MLA decode µs/call and KV-read GB/s vs GB300 HBM peak, per (batch, kv_len, dtype)"
-STAGE1_SOURCES = ["mla_stage1.cu", "mla_device.cuh", "mla_partition.cuh", "mla_internal.h"]
+STAGE1_SOURCES = ["mla_stage1_tc.cu", "mla_tcgen05.cuh", "mla_device.cuh", "mla_partition.cuh", "mla_internal.h"]
 
 
 def _stage1_source_sha() -> str:
@@ -55,7 +55,8 @@ def _measured_peaks():
 
 def _ncu_traffic(workload: str):
     """DRAM bytes per stage-1 launch from the committed ncu summary, if it was
-    taken on the current stage-1 source; else None."""
+    taken on the current stage-1 source; else None. A capture of a smaller case
+    is scaled to the workload by KV rows (traffic grows with the rows)."""
     path = os.path.join(ROOT, "profiles", "stage1_dram_traffic.json")
     try:
         with open(path) as f:
@@ -365,7 +366,8 @@ def build_line(args, w, inp, kvb, splits, world, K, W, value, ms_step, achieved,
                        "parallelism": f"{world} independent replicas (weak scaling)"},
             "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                          "frac": round(achieved / peak, 4), "traffic": _ncu_traffic(w.name),
-                         "kernel": f"mla_stage1_kernel<{synth.DTYPE_NAMES[w.kv_dtype]} KV, "
+                         "kernel": ("stage1_tc_kernel (tcgen05)" if w.kv_dtype == synth.FP8_E4M3 else
+                                    "mla_stage1_kernel (warp MMA)") + f" <{synth.DTYPE_NAMES[w.kv_dtype]} KV, "
                                    f"{synth.DTYPE_NAMES[w.q_dtype]} q>",
                          "algorithmic_bytes": f"{kvb} per launch = {kvb // inp.total_kv} B x {inp.total_kv} KV rows",
                          "peak_kind": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)",
