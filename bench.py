@@ -150,9 +150,9 @@ def kv_bytes(inp) -> int:
 def workload_by_name(synth, name):
     if name in synth.WORKLOADS:
         return synth.WORKLOADS[name]
-    # profiling shapes: kvfp8_bs64_kv8192, kvbf16_bs8_kv4096 (bf16 q, one token per segment)
+    # profiling shapes: kvfp8_bs64_kv8192, kvbf16_bs8_kv4096, kvmx_bs64_kv8192 (bf16 q, one token per segment)
     fmt, bs, kvl = name.split("_")
-    kv_dtype = {"kvfp8": synth.FP8_E4M3, "kvbf16": synth.BF16}[fmt]
+    kv_dtype = {"kvfp8": synth.FP8_E4M3, "kvbf16": synth.BF16, "kvmx": synth.MXFP4}[fmt]
     return synth.Workload(name, int(bs[2:]), 1, int(kvl[2:]), synth.BF16, kv_dtype)
 
 

@@ -117,7 +117,11 @@ mla_status_t mla_decode_workspace_size(int32_t batch, int32_t total_q, int32_t t
  *   kv        device, [total_kv][576] bf16 / e4m3 codes, or [total_kv][288]
  *             fp4x2 bytes for mxfp4; 16-byte aligned
  *   kv_scale  device: NULL (bf16), one float (fp8), or [total_kv][18] e8m0
- *             bytes (mxfp4)
+ *             bytes (mxfp4; 2-byte aligned). mxfp4 rows are used as e2m1
+ *             values rebased to the row's largest block scale R: blocks whose
+ *             scale is more than 15 below R count as zero (their elements are
+ *             at most 6 * 2^(R - 143)); a NaN scale code (0xFF) gives
+ *             unspecified output values.
  *   qo_indptr, kv_indptr  device int32 [batch+1]: monotone, [0] = 0,
  *             qo_indptr[batch] = total_q, kv_indptr[batch] = total_kv. The
  *             kernels check this and, on a violation, skip the work and set

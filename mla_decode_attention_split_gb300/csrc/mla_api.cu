@@ -104,6 +104,7 @@ mla_status_t mla_decode(const void* q, const void* kv, const void* kv_scale, con
   if (total_q > 0 && (!q || !out || !aligned16(q) || !aligned16(out))) return MLA_ERR_INVALID_ARG;
   if (total_kv > 0 && (!kv || !aligned16(kv))) return MLA_ERR_INVALID_ARG;
   if (kv_dtype != MLA_DTYPE_BF16 && !kv_scale) return MLA_ERR_INVALID_ARG;
+  if (kv_dtype == MLA_DTYPE_MXFP4 && (reinterpret_cast<uintptr_t>(kv_scale) & 1u) != 0) return MLA_ERR_INVALID_ARG;
   if (opts->q_dtype == MLA_DTYPE_FP8_E4M3 && !opts->q_scale) return MLA_ERR_INVALID_ARG;
   if (!mla::stage1_supported(kv_dtype, opts->q_dtype)) return MLA_ERR_UNSUPPORTED;
   int32_t splits = opts->num_splits;

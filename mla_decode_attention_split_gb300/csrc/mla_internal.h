@@ -41,6 +41,8 @@ enum QFormat : int { kQBf16 = 0, kQFp8 = 1 };
 cudaError_t launch_stage1(int kv_fmt, int q_fmt, const Stage1Params& p, cudaStream_t stream);
 // fp8 KV on the tcgen05 tensor cores (mla_stage1_tc.cu)
 cudaError_t launch_stage1_tc_fp8(int q_fmt, const Stage1Params& p, cudaStream_t stream);
+// mxfp4 KV on the tcgen05 tensor cores (mla_stage1_mx.cu)
+cudaError_t launch_stage1_tc_mxfp4(int q_fmt, const Stage1Params& p, cudaStream_t stream);
 cudaError_t launch_stage2(const Stage1Params& p, cudaStream_t stream);
 cudaError_t launch_dequant(const void* kv, const void* kv_scale, int kv_fmt, int32_t total_kv, int32_t row0,
                            int32_t nrows, float* out, cudaStream_t stream);

@@ -788,11 +788,12 @@ extern "C" int mla_debug_phase_cycles(unsigned long long* host, int n, int reset
 #endif
 
 bool stage1_supported(int kv_fmt, int q_fmt) {
-  return (kv_fmt == kKvFp8 || kv_fmt == kKvBf16) && (q_fmt == kQBf16 || q_fmt == kQFp8);
+  return (kv_fmt == kKvFp8 || kv_fmt == kKvBf16 || kv_fmt == kKvMxfp4) && (q_fmt == kQBf16 || q_fmt == kQFp8);
 }
 
 cudaError_t launch_stage1(int kv_fmt, int q_fmt, const Stage1Params& p, cudaStream_t stream) {
   if (kv_fmt == kKvFp8) return launch_stage1_tc_fp8(q_fmt, p, stream);
+  if (kv_fmt == kKvMxfp4) return launch_stage1_tc_mxfp4(q_fmt, p, stream);
   if (kv_fmt == kKvBf16) {
     return q_fmt == kQBf16 ? launch_t<kKvBf16, kQBf16>(p, stream) : launch_t<kKvBf16, kQFp8>(p, stream);
   }

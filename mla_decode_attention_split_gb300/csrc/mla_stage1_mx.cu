@@ -1,0 +1,595 @@
+// Stage 1 of split-K MLA decode for an mxfp4 KV cache (OCP MX: e2m1 elements,
+// one e8m0 scale per 32 along the head dimension) on the tcgen05 tensor cores.
+//
+// Method: the same split-K flash decoding partials as the fp8 kernel
+// (kernelbot-amd-mixed-mla-753817, `mla_flash_decode_stage1`); the KV row is
+// K[d] = e2m1[d] * 2^(scale[d / 32] - 127).
+//
+// GB300 design:
+//  * The MX block scales run along the head dimension. For Q.K^T that is the
+//    contraction, but for P.V it is the output (M) dimension, which no
+//    block-scaled MMA form can take, so each row is converted once into an
+//    8-bit operand that serves both products: every e2m1 element becomes an
+//    e5m2 value rebased to the row's largest block exponent R,
+//    e5m2 = e2m1 * 2^(scale - R). That is exact while scale >= R - 15 (e5m2
+//    reaches down to 2^-16 with subnormals); blocks more than 15 binades below
+//    the row's largest are flushed to zero: their elements are at most
+//    6 * 2^(R - 143), under 2^-15 of the largest block's range.
+//  * The row factor 2^r, r = R - 127, multiplies that row's scores, and enters
+//    P.V through the weights: per head, the softmax keeps m = max x (for the
+//    denominator l) and mu = max (x + r) (the reference of O), writes
+//    P = 2^(x + r - mu) (<= 1, the largest term of O exactly 1), and the
+//    epilogue multiplies O by 2^(mu - m) / l.
+//  * Conversion is per tile row (one thread per row) from registers loaded
+//    two tiles ahead into one of two 72 KB stages (V dims in the 128B-swizzled
+//    K-major layout of a TMA box, rope dims in the no-swizzle rope layout).
+//    With two stages, a stage is rewritten only once the P.V of the tile two
+//    back is done, so tiles move in pairs: the converters fill both stages,
+//    the tensor pipe runs Q.K^T of both tiles, then P.V of both, while the
+//    softmax of the first tile overlaps the second Q.K^T and the next pair's
+//    conversion overlaps the P.V.
+//  * Warps 0-3 convert (warp 0, lane 0 also issues the UMMAs and owns tensor
+//    memory), warps 4-7 run the online softmax (thread = row = TMEM lane).
+//    Every mbarrier wait is bounded.
+#include "mla_tc_common.cuh"
+
+namespace mla {
+namespace tc {
+namespace mx {
+
+constexpr int kThreads = 256;
+constexpr int kStages = 2;
+constexpr int kStageBytes = kVBytes + kRopeBytes;  // 72 KB: V dims + rope dims (e5m2)
+constexpr int kMaxRebase = 15;  // e5m2 holds e2m1 * 2^-down exactly for down <= 15
+
+struct L {
+  static constexpr int kThreads = mx::kThreads;
+  static constexpr int kOffKv = 0;
+  static constexpr int kOffQ = kOffKv + kStages * kStageBytes;
+  static constexpr int kOffP = kOffQ + kQBytes;                      // 2 x 4 KB
+  static constexpr int kOffRexp = kOffP + 2 * kPBytes;               // [2][128] u8: R of each row
+  static constexpr int kOffRedMax = kOffRexp + 2 * kTileRows;        // [2][4][16] f32
+  static constexpr int kOffRedMu = kOffRedMax + 2 * 4 * 16 * 4;      // [2][4][16] f32
+  static constexpr int kOffRedL = kOffRedMu + 2 * 4 * 16 * 4;        // [4][16] f32
+  static constexpr int kOffAmax = kOffRedL + 4 * 16 * 4;             // [4] u32
+  static constexpr int kOffScan = kOffAmax + 16;                     // 16 x i64
+  static constexpr int kOffRaw = kOffScan + 16 * 8;                  // [4 warps][32 rows][288 B] fp4x2
+  static constexpr int kOffRawSc = kOffRaw + 4 * 32 * (kDqk / 2);    // [4 warps][32 rows][18 B] e8m0
+  static constexpr int kOffBars = kOffRawSc + 4 * 32 * (kDqk / kMxBlock);
+  enum {
+    kKvFull = 0, kSFull = 2, kSEmpty = 4, kPFull = 6, kPvDone = 8, kQFull = 10, kQEmpty = 11, kOFull = 12,
+    kOEmpty = 14, kGrp = 16, kDrain = 18, kNumBars = 19
+  };
+  static constexpr int kOffSlot = kOffBars + kNumBars * 8;
+  static constexpr int kOffAbort = kOffSlot + 8;
+  static constexpr int kBytes = kOffAbort + 8;
+  static constexpr int kAlloc = kBytes + 1024;
+  template <class C>
+  __device__ static void init_barriers(const C& cx) {
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(cx.bar(kKvFull + i), 4);  // the 4 converter warps
+      mbar_init(cx.bar(kSFull + i), 1);
+      mbar_init(cx.bar(kSEmpty + i), 4);
+      mbar_init(cx.bar(kPFull + i), 4);
+      mbar_init(cx.bar(kPvDone + i), 1);
+      mbar_init(cx.bar(kOFull + i), 1);
+      mbar_init(cx.bar(kOEmpty + i), 4);
+      mbar_init(cx.bar(kGrp + i), 4);
+    }
+    mbar_init(cx.bar(kQFull), 4);
+    mbar_init(cx.bar(kQEmpty), 1);
+    mbar_init(cx.bar(kDrain), 1);
+  }
+};
+static_assert(L::kAlloc <= 227 * 1024, "shared memory budget");
+static_assert(kStageBytes % 1024 == 0 && L::kOffQ % 1024 == 0 && L::kOffP % 1024 == 0, "operand alignment");
+static_assert(L::kOffRaw % 16 == 0 && L::kOffBars % 8 == 0, "staging alignment");
+using Cx = Ctx<L>;
+
+// Optional phase timers (build with -DMLA_PHASE_TIMING): cycles per CTA, warp
+// and phase, summed over the launch. Off by default.
+#ifdef MLA_PHASE_TIMING
+constexpr int kPhaseCtas = 1024;
+__device__ unsigned long long g_mx_phase[kPhaseCtas * 8 * 8];
+#define MX_PT_INIT long long mx_pt_ = clock64();
+#define MX_PT(ph)                                                                                          \
+  do {                                                                                                     \
+    const long long now_ = clock64();                                                                      \
+    if ((threadIdx.x & 31) == 0 && blockIdx.x < kPhaseCtas)                                                \
+      atomicAdd(&g_mx_phase[(blockIdx.x * 8 + (threadIdx.x >> 5)) * 8 + (ph)],                             \
+                static_cast<unsigned long long>(now_ - mx_pt_));                                           \
+    mx_pt_ = now_;                                                                                         \
+  } while (0)
+#else
+#define MX_PT_INIT
+#define MX_PT(ph) \
+  do {            \
+  } while (0)
+#endif
+
+// ---------------------------------------------------------------------------
+// Converters (warps 0-3; thread = tile row).
+
+// The raw rows of one warp's 32 tile rows, loaded coalesced: lane l holds
+// 16-byte unit 32 j + l of the warp's 32 x 288 contiguous fp4x2 bytes and
+// 2-byte word 32 k + l of its 32 x 18 scale bytes.
+struct MxRaw {
+  uint4 nib[18];
+  uint32_t sc[9];
+};
+
+// Global loads that stay where they are written (issued two tiles ahead of
+// their use; the compiler may not sink them next to the use).
+__device__ __forceinline__ uint4 ld_pinned_v4(const void* p) {
+  uint4 v;
+  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(p));
+  return v;
+}
+__device__ __forceinline__ uint32_t ld_pinned_u16(const void* p) {
+  uint16_t v;
+  asm volatile("ld.global.nc.L1::no_allocate.u16 %0, [%1];" : "=h"(v) : "l"(p));
+  return v;
+}
+
+// Loads the warp's rows of the next tile (rows past the end of the cache or of
+// the CTA's tiles read as zero).
+__device__ __forceinline__ void load_mx_raw(const Stage1Params& p, TileWalker& rw, int warp, int lane, MxRaw& r) {
+  int32_t row0;
+  const bool have = rw.next(row0);
+  const int64_t gb = static_cast<int64_t>(row0) + 32 * warp;
+  const uint8_t* kvb = static_cast<const uint8_t*>(p.kv) + gb * (kDqk / 2) + 16 * lane;
+  const uint8_t* scb = static_cast<const uint8_t*>(p.kv_scale) + gb * (kDqk / kMxBlock) + 2 * lane;
+  if (have && gb + 32 <= p.total_kv) {
+#pragma unroll
+    for (int j = 0; j < 18; ++j) r.nib[j] = ld_pinned_v4(kvb + 512 * j);
+#pragma unroll
+    for (int k = 0; k < 9; ++k) r.sc[k] = ld_pinned_u16(scb + 64 * k);
+  } else if (have && gb < p.total_kv) {
+    // the warp's rows straddle the end of the cache: unit u belongs to row u / 18
+    const int nvalid = static_cast<int>(p.total_kv - gb);
+#pragma unroll
+    for (int j = 0; j < 18; ++j)
+      r.nib[j] = (32 * j + lane) / 18 < nvalid ? ld_pinned_v4(kvb + 512 * j) : make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+    for (int k = 0; k < 9; ++k) r.sc[k] = (64 * k + 2 * lane) / 18 < nvalid ? ld_pinned_u16(scb + 64 * k) : 0u;
+  } else {
+#pragma unroll
+    for (int j = 0; j < 18; ++j) r.nib[j] = make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+    for (int k = 0; k < 9; ++k) r.sc[k] = 0u;
+  }
+}
+
+// Registers -> the warp's staging area, in memory order (conflict-free).
+__device__ __forceinline__ void dump_raw(uint8_t* raw_w, uint8_t* sc_w, int lane, const MxRaw& r) {
+#pragma unroll
+  for (int j = 0; j < 18; ++j) *reinterpret_cast<uint4*>(raw_w + 16 * (32 * j + lane)) = r.nib[j];
+#pragma unroll
+  for (int k = 0; k < 9; ++k) *reinterpret_cast<uint16_t*>(sc_w + 2 * (32 * k + lane)) = static_cast<uint16_t>(r.sc[k]);
+}
+
+// e2m1 -> rebased e5m2, through f16: the hardware conversion turns each byte
+// (two e2m1 codes) into two exact f16 values, an f16 multiply by 2^-down
+// rebases them (exact: every e2m1 value times 2^-down, down <= 15, is an f16
+// number with at most 2 significant bits below the leading one), and e5m2 is
+// the high byte of f16 (same exponent bias, 2 mantissa bits), so the bytes are
+// exact. A block more than 15 binades below the row's largest is multiplied by
+// zero (flushed).
+__device__ __forceinline__ uint32_t rebase_scale2(uint32_t down) {
+  const uint32_t s = down <= static_cast<uint32_t>(kMaxRebase) ? ((15u - down) << 10) : 0u;  // f16 2^-down
+  return s | (s << 16);
+}
+
+// Eight e2m1 codes (one 32-bit word, element 0 in the lowest nibble) -> eight
+// e5m2 bytes: byte i of out_lo is element i, of out_hi element 4 + i.
+__device__ __forceinline__ void e2m1x8_to_e5m2x8(uint32_t w, uint32_t s2, uint32_t& out_lo, uint32_t& out_hi) {
+  uint32_t h0, h1, h2, h3;
+  asm("{\n .reg .b8 b0, b1, b2, b3;\n mov.b32 {b0, b1, b2, b3}, %4;\n"
+      " cvt.rn.f16x2.e2m1x2 %0, b0;\n cvt.rn.f16x2.e2m1x2 %1, b1;\n"
+      " cvt.rn.f16x2.e2m1x2 %2, b2;\n cvt.rn.f16x2.e2m1x2 %3, b3;\n"
+      " mul.rn.f16x2 %0, %0, %5;\n mul.rn.f16x2 %1, %1, %5;\n"
+      " mul.rn.f16x2 %2, %2, %5;\n mul.rn.f16x2 %3, %3, %5;\n}"
+      : "=r"(h0), "=r"(h1), "=r"(h2), "=r"(h3)
+      : "r"(w), "r"(s2));
+  out_lo = prmt(h0, h1, 0x7531u);  // high bytes of the four f16 values
+  out_hi = prmt(h2, h3, 0x7531u);
+}
+
+// 32 e2m1 codes (16 bytes) -> 32 e5m2 bytes as two 16-byte units.
+__device__ __forceinline__ void convert_block(const uint4& v, uint32_t s2, uint4& lo, uint4& hi) {
+  e2m1x8_to_e5m2x8(v.x, s2, lo.x, lo.y);
+  e2m1x8_to_e5m2x8(v.y, s2, lo.z, lo.w);
+  e2m1x8_to_e5m2x8(v.z, s2, hi.x, hi.y);
+  e2m1x8_to_e5m2x8(v.w, s2, hi.z, hi.w);
+}
+
+// Converts this thread's row (tile row tr, staged at srow / ssc) into the
+// stage: V dims into the 128B-swizzled chunks, rope dims into the no-swizzle
+// rope part; records R.
+__device__ __forceinline__ void convert_row(uint8_t* stage, uint8_t* rexp, int tr, const uint8_t* srow,
+                                            const uint8_t* ssc) {
+  uint32_t R = 0;
+#pragma unroll
+  for (int k = 0; k < 9; ++k) {
+    const uint32_t h = *reinterpret_cast<const uint16_t*>(ssc + 2 * k);
+    R = max(R, max(h & 0xFFu, h >> 8));
+  }
+  const int sw = tr & 7;
+  uint8_t* vrow = stage + tr * 128;
+#pragma unroll 1
+  for (int b = 0; b < 16; b += 2) {  // blocks b, b + 1 of V chunk b / 4
+    const uint32_t sc = *reinterpret_cast<const uint16_t*>(ssc + b);
+    const uint4 v0 = *reinterpret_cast<const uint4*>(srow + 16 * b);
+    const uint4 v1 = *reinterpret_cast<const uint4*>(srow + 16 * (b + 1));
+    uint8_t* rb = vrow + (b >> 2) * kChunkBytes;
+    const int u0 = 2 * (b & 3);  // elements 32(b%4).. of the chunk: 16-byte units u0 .. u0+3, swizzled by row
+    uint4 lo, hi;
+    convert_block(v0, rebase_scale2(R - (sc & 0xFFu)), lo, hi);
+    *reinterpret_cast<uint4*>(rb + ((u0 ^ sw) << 4)) = lo;
+    *reinterpret_cast<uint4*>(rb + (((u0 + 1) ^ sw) << 4)) = hi;
+    convert_block(v1, rebase_scale2(R - (sc >> 8)), lo, hi);
+    *reinterpret_cast<uint4*>(rb + (((u0 + 2) ^ sw) << 4)) = lo;
+    *reinterpret_cast<uint4*>(rb + (((u0 + 3) ^ sw) << 4)) = hi;
+  }
+  // rope dims: blocks 16, 17 -> 16-byte columns 0..3 of the no-swizzle operand
+  uint8_t* rrow = stage + kVBytes + (tr >> 3) * 512 + (tr & 7) * 16;
+  const uint32_t sc2 = *reinterpret_cast<const uint16_t*>(ssc + 16);
+#pragma unroll
+  for (int q = 0; q < 2; ++q) {
+    const uint4 v = *reinterpret_cast<const uint4*>(srow + 16 * (16 + q));
+    uint4 lo, hi;
+    convert_block(v, rebase_scale2(R - ((sc2 >> (8 * q)) & 0xFFu)), lo, hi);
+    *reinterpret_cast<uint4*>(rrow + (2 * q) * 128) = lo;
+    *reinterpret_cast<uint4*>(rrow + (2 * q + 1) * 128) = hi;
+  }
+  rexp[tr] = static_cast<uint8_t>(R);
+}
+
+// Stage i % 2 is free for tile i once the P.V of tile i - 2 is done.
+__device__ __forceinline__ bool wait_stage(const Cx& cx, uint32_t i) {
+  return i < 2 || cx.wait(L::kPvDone + (i & 1u), ((i - 2) >> 1) & 1u);
+}
+
+// Tile i (this warp's rows staged in raw_w / sc_w) into stage i % 2.
+__device__ __forceinline__ void convert_tile(const Cx& cx, uint32_t i, int warp, int lane, const uint8_t* raw_w,
+                                             const uint8_t* sc_w) {
+  const uint32_t st = i & 1u;
+  convert_row(cx.g + L::kOffKv + st * kStageBytes, cx.g + L::kOffRexp + st * kTileRows, 32 * warp + lane,
+              raw_w + lane * (kDqk / 2), sc_w + lane * (kDqk / kMxBlock));
+}
+
+// Hands stage i % 2 to the UMMA issuer (generic-proxy writes made visible to
+// the tensor core first).
+__device__ __forceinline__ void publish_tile(const Cx& cx, uint32_t i, int lane) {
+  fence_async_smem();
+  __syncwarp();
+  if (lane == 0) mbar_arrive(cx.bar(L::kKvFull + (i & 1u)));
+}
+
+// Per-tile bookkeeping of the UMMA issuer.
+struct TileMeta {
+  uint32_t k;  // piece index within the CTA
+  bool first, last;
+};
+struct MetaWalker {
+  PieceCursor cur;
+  Piece pc;
+  int r0;
+  uint32_t k;
+  __device__ void init(const PieceCursor& c) {
+    cur = c;
+    cur.next(pc);
+    r0 = 0;
+    k = 0;
+  }
+  __device__ TileMeta next() {
+    const TileMeta m{k, r0 == 0, r0 + kTileRows >= pc.nrows};
+    r0 += kTileRows;
+    if (r0 >= pc.nrows) {
+      cur.next(pc);
+      r0 = 0;
+      ++k;
+    }
+    return m;
+  }
+};
+
+constexpr uint32_t kIdQK = umma_idesc(128, 32, 1, 0, false, false);  // A e5m2 K-major, B e4m3
+constexpr uint32_t kIdPV = umma_idesc(128, 32, 1, 0, true, true);    // A = V^T MN-major, B = P^T MN-major
+
+__device__ __forceinline__ bool issue_qk(const Cx& cx, uint32_t i, const TileMeta& t) {
+  const uint32_t b = i & 1u;
+  if (t.first && !cx.wait(L::kQFull, t.k & 1u)) return false;
+  if (!cx.wait(L::kKvFull + b, (i >> 1) & 1u)) return false;
+  if (i >= 2 && !cx.wait(L::kSEmpty + b, ((i - 2) >> 1) & 1u)) return false;
+  tc_fence_after();
+  const uint32_t stage = cx.s + L::kOffKv + b * kStageBytes, qbuf = cx.s + L::kOffQ;
+  const uint32_t d = cx.tmem + kTmemS + 32 * b;
+#pragma unroll
+  for (int ks = 0; ks < 16; ++ks) umma_e4m3(d, qk_desc_a(stage, ks), qk_desc_b(qbuf, ks), kIdQK, ks > 0 ? 1u : 0u);
+#pragma unroll
+  for (int ks = 0; ks < 2; ++ks) umma_e4m3(d, rope_desc_a(stage + kVBytes, ks), qk_desc_b(qbuf, 16 + ks), kIdQK, 1u);
+  umma_commit(cx.bar(L::kSFull + b));
+  if (t.last) umma_commit(cx.bar(L::kQEmpty));
+  return true;
+}
+
+__device__ __forceinline__ bool issue_pv(const Cx& cx, uint32_t i, const TileMeta& t) {
+  const uint32_t b = i & 1u;
+  if (!cx.wait(L::kPFull + b, (i >> 1) & 1u)) return false;
+  if (t.first && t.k >= 2 && !cx.wait(L::kOEmpty + (t.k & 1u), ((t.k >> 1) - 1) & 1u)) return false;
+  tc_fence_after();
+  const uint32_t stage = cx.s + L::kOffKv + b * kStageBytes, pbuf = cx.s + L::kOffP + b * kPBytes;
+  const uint32_t obuf = cx.tmem + kTmemO + (t.k & 1u) * 128;
+#pragma unroll
+  for (int mb = 0; mb < 4; ++mb)
+#pragma unroll
+    for (int ks = 0; ks < 4; ++ks)
+      umma_e4m3(obuf + 32 * mb, pv_desc_a(stage, mb, ks), pv_desc_b(pbuf, ks), kIdPV, (ks > 0 || !t.first) ? 1u : 0u);
+  umma_commit(cx.bar(L::kPvDone + b));
+  if (t.last) umma_commit(cx.bar(L::kOFull + (t.k & 1u)));
+  return true;
+}
+
+__device__ void converter_role(const Stage1Params& p, const Cx& cx, PieceCursor cur, int warp, int lane) {
+  const bool issuer = (warp == 0 && lane == 0);
+  const uint32_t ntiles = static_cast<uint32_t>(count_tiles(cur));
+  uint8_t* raw_w = cx.g + L::kOffRaw + warp * 32 * (kDqk / 2);
+  uint8_t* sc_w = cx.g + L::kOffRawSc + warp * 32 * (kDqk / kMxBlock);
+  TileWalker rw;
+  rw.init(cur);
+  MetaWalker mq, mp;
+  mq.init(cur);
+  mp.init(cur);
+  MxRaw ra, rb;  // the even / odd tile in flight
+  load_mx_raw(p, rw, warp, lane, ra);
+  load_mx_raw(p, rw, warp, lane, rb);
+  bool ok = true;
+  MX_PT_INIT
+  for (uint32_t i = 0; ok && i < ntiles; i += 2) {
+    const bool two = i + 1 < ntiles;
+    MX_PT(7);
+    if (!wait_stage(cx, i)) break;
+    MX_PT(3);
+    dump_raw(raw_w, sc_w, lane, ra);
+    __syncwarp();
+    MX_PT(4);
+    load_mx_raw(p, rw, warp, lane, ra);  // tile i + 2
+    MX_PT(5);
+    convert_tile(cx, i, warp, lane, raw_w, sc_w);
+    MX_PT(0);
+    publish_tile(cx, i, lane);
+    MX_PT(6);
+    if (warp == 0) {
+      if (issuer) ok = issue_qk(cx, i, mq.next());
+      ok = __shfl_sync(0xffffffffu, ok, 0);
+      if (!ok) break;
+    }
+    MX_PT(1);
+    if (two) {
+      if (!wait_stage(cx, i + 1)) break;
+      MX_PT(3);
+      dump_raw(raw_w, sc_w, lane, rb);
+      __syncwarp();
+      MX_PT(4);
+      load_mx_raw(p, rw, warp, lane, rb);  // tile i + 3
+      MX_PT(5);
+      convert_tile(cx, i + 1, warp, lane, raw_w, sc_w);
+      MX_PT(0);
+      publish_tile(cx, i + 1, lane);
+      MX_PT(6);
+      if (warp == 0) {
+        if (issuer) ok = issue_qk(cx, i + 1, mq.next());
+        ok = __shfl_sync(0xffffffffu, ok, 0);
+        if (!ok) break;
+      }
+      MX_PT(1);
+    }
+    if (warp == 0) {
+      if (issuer) {
+        ok = issue_pv(cx, i, mp.next());
+        if (ok && two) ok = issue_pv(cx, i + 1, mp.next());
+      }
+      ok = __shfl_sync(0xffffffffu, ok, 0);
+      MX_PT(2);
+    }
+  }
+  if (warp == 0) {
+    // every issued tcgen05 operation completes before tensor memory is freed
+    if (issuer) {
+      umma_commit(cx.bar(L::kDrain));
+      mbar_wait_drain_tc(cx.bar(L::kDrain), 0);
+    }
+    __syncwarp();
+  }
+}
+
+// 2^e for an integer e in [-127, 127] (exact).
+__device__ __forceinline__ float exp2i(int e) {
+  return e >= -126 ? __uint_as_float(static_cast<uint32_t>(e + 127) << 23) : __uint_as_float(0x00400000u);
+}
+
+// ---------------------------------------------------------------------------
+// Softmax (warps 4-7).
+template <int QF>
+__device__ void softmax_role(const Stage1Params& p, const Cx& cx, PieceCursor cur, int warp, int lane) {
+  SoftmaxCtx sx;
+  sx.lane = lane;
+  sx.wi = warp - 4;
+  sx.row = 32 * (warp & 3) + lane;
+  sx.lane_base = static_cast<uint32_t>(32 * (warp & 3)) << 16;
+  sx.gcount = 0;
+  float* red_max = reinterpret_cast<float*>(cx.g + L::kOffRedMax);
+  float* red_mu = reinterpret_cast<float*>(cx.g + L::kOffRedMu);
+  float* red_l = reinterpret_cast<float*>(cx.g + L::kOffRedL);
+  PieceCursor ahead = cur;
+  Piece pc, nxt;
+  bool have = ahead.next(pc);
+  if (!have) return;
+  float c = setup_q<L, QF>(p, cx, sx, pc.token, 0, 1.0f);
+  if (c < 0.f) return;
+  uint32_t i = 0, k = 0;
+  MX_PT_INIT
+  while (have) {
+    const bool have_next = ahead.next(nxt);
+    float m[16], mu[16], l[16];
+#pragma unroll
+    for (int h = 0; h < 16; ++h) {
+      m[h] = -INFINITY;
+      mu[h] = -INFINITY;
+      l[h] = 0.f;
+    }
+    for (int r0 = 0; r0 < pc.nrows; r0 += kTileRows) {
+      const int nr = min(kTileRows, pc.nrows - r0);
+      const uint32_t b = i & 1u;
+      const bool valid = sx.row < nr;
+      MX_PT(7);
+      if (!cx.wait(L::kSFull + b, (i >> 1) & 1u)) return;
+      // the converters' row exponents of this stage (already complete: Q.K^T read the stage)
+      if (!cx.wait(L::kKvFull + b, (i >> 1) & 1u)) return;
+      MX_PT(0);
+      const int r = static_cast<int>(cx.g[L::kOffRexp + b * kTileRows + sx.row]) - 127;
+      tc_fence_after();
+      uint32_t sr[32];
+      tmem_ld32(cx.tmem + sx.lane_base + kTmemS + 32 * b, sr);
+      tmem_wait_ld();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(cx.bar(L::kSEmpty + b));
+      const float cr = c * exp2i(r), rf = static_cast<float>(r);
+      float x[16], z[16];
+#pragma unroll
+      for (int h = 0; h < 16; ++h) {
+        const float v = (__uint_as_float(sr[h]) + __uint_as_float(sr[16 + h]) * (1.0f / kLoScale)) * cr;
+        x[h] = valid ? v : -INFINITY;
+        z[h] = x[h] + rf;
+      }
+      float* rm = red_max + b * 64;
+      float* rz = red_mu + b * 64;
+      const float wm = warp_reduce16<true>(x, lane);
+      const float wz = warp_reduce16<true>(z, lane);
+      if ((lane & 1) == 0) {
+        rm[sx.wi * 16 + (lane >> 1)] = wm;
+        rz[sx.wi * 16 + (lane >> 1)] = wz;
+      }
+      MX_PT(1);
+      if (!group_sync(cx, sx)) return;
+      MX_PT(2);
+      bool grew = false;
+      float alpha[16], alpha_o[16];
+#pragma unroll
+      for (int h = 0; h < 16; ++h) {
+        const float mn = fmaxf(m[h], fmaxf(fmaxf(rm[h], rm[16 + h]), fmaxf(rm[32 + h], rm[48 + h])));
+        const float un = fmaxf(mu[h], fmaxf(fmaxf(rz[h], rz[16 + h]), fmaxf(rz[32 + h], rz[48 + h])));
+        alpha[h] = fast_exp2(m[h] - mn);
+        alpha_o[h] = fast_exp2(mu[h] - un);
+        grew |= un > mu[h];
+        m[h] = mn;
+        mu[h] = un;
+      }
+      float pv[16];
+#pragma unroll
+      for (int h = 0; h < 16; ++h) {
+        l[h] = l[h] * alpha[h] + fast_exp2(x[h] - m[h]);
+        pv[h] = fast_exp2(z[h] - mu[h]) * kPScale;
+      }
+      MX_PT(3);
+      // P buffer b is free once the P.V of tile i - 2 is done
+      if (i >= 2 && !cx.wait(L::kPvDone + b, ((i - 2) >> 1) & 1u)) return;
+      put_p_row(cx.g + L::kOffP + b * kPBytes, sx.row, pv);
+      if (grew && r0 > 0) {
+        // O holds this piece up to tile i - 1: wait for that P.V, then rescale
+        if (!cx.wait(L::kPvDone + (b ^ 1u), ((i - 1) >> 1) & 1u)) return;
+        tc_fence_after();
+        rescale_o(cx.tmem + sx.lane_base + kTmemO + (k & 1u) * 128, alpha_o);
+      }
+      MX_PT(4);
+      fence_async_smem();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(cx.bar(L::kPFull + b));
+      MX_PT(5);
+      ++i;
+    }
+    // the next piece's q goes in while this piece's last P.V runs
+    float c_next = c;
+    if (have_next) {
+      c_next = setup_q<L, QF>(p, cx, sx, nxt.token, k + 1, 1.0f);
+      if (c_next < 0.f) return;
+    }
+    const float wl = warp_reduce16<false>(l, lane);
+    if ((lane & 1) == 0) red_l[sx.wi * 16 + (lane >> 1)] = wl;
+    if (!group_sync(cx, sx)) return;
+    float f[16];
+#pragma unroll
+    for (int h = 0; h < 16; ++h) {
+      const float L = red_l[h] + red_l[16 + h] + red_l[32 + h] + red_l[48 + h];
+      f[h] = fast_exp2(mu[h] - m[h]) / (kPScale * L);
+      if (!pc.direct && sx.row == h) p.part_lse[pc.slot * kHeads + h] = m[h] + fast_log2(L);
+    }
+    if (!cx.wait(L::kOFull + (k & 1u), (k >> 1) & 1u)) return;
+    tc_fence_after();
+    store_o(p, pc, cx.tmem + sx.lane_base + kTmemO + (k & 1u) * 128, sx.row, f);
+    tc_fence_before();
+    __syncwarp();
+    if (lane == 0) mbar_arrive(cx.bar(L::kOEmpty + (k & 1u)));
+    MX_PT(6);
+    pc = nxt;
+    have = have_next;
+    c = c_next;
+    ++k;
+  }
+}
+
+template <int QF>
+__global__ void __launch_bounds__(kThreads, 1) stage1_mx_kernel(const Stage1Params p) {
+  extern __shared__ uint8_t smem_raw[];
+  Cx cx;
+  PieceCursor cur;
+  if (!cta_begin(p, cx, smem_raw, 0, cur)) return;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (warp < 4)
+    converter_role(p, cx, cur, warp, lane);
+  else
+    softmax_role<QF>(p, cx, cur, warp, lane);
+  cta_end(cx, 0);
+}
+
+#ifdef MLA_PHASE_TIMING
+extern "C" int mla_debug_phase_cycles_mx(unsigned long long* host, int n, int reset) {
+  if (n > kPhaseCtas * 64) n = kPhaseCtas * 64;
+  if (cudaMemcpyFromSymbol(host, g_mx_phase, sizeof(unsigned long long) * n) != cudaSuccess) return -1;
+  if (reset) {
+    void* q = nullptr;
+    if (cudaGetSymbolAddress(&q, g_mx_phase) != cudaSuccess) return -1;
+    if (cudaMemset(q, 0, sizeof(g_mx_phase)) != cudaSuccess) return -1;
+  }
+  return n;
+}
+#endif
+
+template <int QF>
+static cudaError_t launch_q(const Stage1Params& p, cudaStream_t stream) {
+  static int configured_device = -1;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (configured_device != dev) {
+    e = cudaFuncSetAttribute(stage1_mx_kernel<QF>, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kAlloc);
+    if (e != cudaSuccess) return e;
+    configured_device = dev;
+  }
+  stage1_mx_kernel<QF><<<p.num_splits, kThreads, L::kAlloc, stream>>>(p);
+  return cudaGetLastError();
+}
+
+}  // namespace mx
+}  // namespace tc
+
+cudaError_t launch_stage1_tc_mxfp4(int q_fmt, const Stage1Params& p, cudaStream_t stream) {
+  return q_fmt == kQBf16 ? tc::mx::launch_q<kQBf16>(p, stream) : tc::mx::launch_q<kQFp8>(p, stream);
+}
+
+}  // namespace mla

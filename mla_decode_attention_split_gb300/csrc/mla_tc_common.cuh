@@ -1,0 +1,341 @@
+// Pieces shared by the tcgen05 stage-1 kernels (fp8 KV in mla_stage1_tc.cu,
+// mxfp4 KV in mla_stage1_mx.cu): tile geometry, the shared-memory context,
+// the tile walker, the per-head warp reductions and the q operand setup.
+//
+// Both kernels compute, per query token and split, the online-softmax partial
+// of split-K flash decoding (kernelbot-amd-mixed-mla-753817,
+// `mla_flash_decode_stage1`) with 128 KV rows as the MMA M dimension and the
+// 16 heads (hi and lo halves of the bf16 operand, N = 32) as N.
+#pragma once
+
+#include <cuda.h>
+
+#include "mla_device.cuh"
+#include "mla_internal.h"
+#include "mla_partition.cuh"
+#include "mla_tcgen05.cuh"
+
+namespace mla {
+namespace tc {
+
+constexpr int kTileRows = 128;
+constexpr int kVChunks = 4;                   // 128-byte column chunks of the 512 V dims
+constexpr int kChunkBytes = kTileRows * 128;  // 16 KB (one 128 x 128 B swizzled box)
+constexpr int kVBytes = kVChunks * kChunkBytes;  // 64 KB
+constexpr int kQChunkBytes = 32 * 128;        // 32 B-operand rows (hi, lo) x 128 B
+constexpr int kQBytes = 5 * kQChunkBytes;     // 20 KB (chunk 4: rope dims, 64 B used)
+constexpr int kRopeBytes = kTileRows * 64;    // [row group 16][16-B column 4][8 rows][16 B]
+constexpr int kPBytes = kTileRows * 32;       // [row group][hi | lo][8 rows][16 heads]
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kTmemS = 0;                // 2 buffers x 32 columns
+constexpr uint32_t kTmemO = 64;               // 2 buffers x (4 blocks x 32 columns)
+constexpr float kLoScale = 16.0f;
+constexpr float kPScale = 256.0f;
+constexpr float kLog2e = 1.4426950408889634f;
+
+// Shared-memory context of one CTA; LL is the kernel's layout (offsets and
+// barrier indices).
+template <class LL>
+struct Ctx {
+  uint8_t* g;  // generic pointer to the 1024-aligned base
+  uint32_t s;  // shared address of the aligned base
+  volatile uint32_t* abort_word;
+  uint32_t* flags;
+  uint32_t tmem;
+  __device__ __forceinline__ uint32_t bar(int i) const { return s + LL::kOffBars + 8u * i; }
+  __device__ __forceinline__ bool wait(int i, uint32_t parity) const { return mbar_wait(bar(i), parity, abort_word, flags); }
+};
+
+// Bounded wait used while draining on exit (no abort check: the CTA leaves
+// either way).
+__device__ __forceinline__ void mbar_wait_drain_tc(uint32_t bar, uint32_t parity) {
+  const long long t0 = clock64();
+  while (!mbar_try_wait(bar, parity)) {
+    if (clock64() - t0 > kWaitLimitCycles) return;
+  }
+}
+
+// Walks the CTA's tiles in order (one 128-row tile at a time).
+struct TileWalker {
+  PieceCursor cur;
+  Piece pc;
+  int r0 = 0;
+  bool have = false;
+  __device__ void init(const PieceCursor& c) {
+    cur = c;
+    have = cur.next(pc);
+    r0 = 0;
+  }
+  // First KV row of the next tile. Returns false when done.
+  __device__ bool next(int32_t& row) {
+    if (!have) return false;
+    row = pc.kv_row + r0;
+    r0 += kTileRows;
+    if (r0 >= pc.nrows) {
+      have = cur.next(pc);
+      r0 = 0;
+    }
+    return true;
+  }
+};
+
+__device__ __forceinline__ int count_tiles(PieceCursor cur) {
+  Piece t;
+  int n = 0;
+  while (cur.next(t)) n += (t.nrows + kTileRows - 1) / kTileRows;
+  return n;
+}
+
+// Max (or sum) of 16 per-head values over the 32 lanes of a warp: each halving
+// step trades half of the heads with the partner lane, so after four steps
+// lane l holds head l >> 1 over 16 lanes and a last step completes the warp.
+template <bool kMax>
+__device__ __forceinline__ float warp_reduce16(const float (&v)[16], int lane) {
+  float a[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const bool up = lane & 16;
+    const float keep = up ? v[i + 8] : v[i], send = up ? v[i] : v[i + 8];
+    const float r = __shfl_xor_sync(0xffffffffu, send, 16);
+    a[i] = kMax ? fmaxf(keep, r) : keep + r;
+  }
+  float b[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const bool up = lane & 8;
+    const float keep = up ? a[i + 4] : a[i], send = up ? a[i] : a[i + 4];
+    const float r = __shfl_xor_sync(0xffffffffu, send, 8);
+    b[i] = kMax ? fmaxf(keep, r) : keep + r;
+  }
+  float c[2];
+#pragma unroll
+  for (int i = 0; i < 2; ++i) {
+    const bool up = lane & 4;
+    const float keep = up ? b[i + 2] : b[i], send = up ? b[i] : b[i + 2];
+    const float r = __shfl_xor_sync(0xffffffffu, send, 4);
+    c[i] = kMax ? fmaxf(keep, r) : keep + r;
+  }
+  const bool up = lane & 2;
+  const float keep = up ? c[1] : c[0], send = up ? c[0] : c[1];
+  const float r = __shfl_xor_sync(0xffffffffu, send, 2);
+  float d = kMax ? fmaxf(keep, r) : keep + r;
+  const float r1 = __shfl_xor_sync(0xffffffffu, d, 1);
+  return kMax ? fmaxf(d, r1) : d + r1;
+}
+
+// The 4 softmax warps: thread = tile row = tensor-memory lane.
+struct SoftmaxCtx {
+  int row, wi, lane;
+  uint32_t lane_base;
+  uint32_t gcount;
+};
+
+// Barrier among the 4 softmax warps (two alternating mbarriers of count 4).
+template <class LL>
+__device__ __forceinline__ bool group_sync(const Ctx<LL>& cx, SoftmaxCtx& sx) {
+  const uint32_t k = sx.gcount & 1u, par = (sx.gcount >> 1) & 1u;
+  ++sx.gcount;
+  __syncwarp();
+  if (sx.lane == 0) mbar_arrive(cx.bar(LL::kGrp + k));
+  return cx.wait(LL::kGrp + k, par);
+}
+
+// q of one token -> the Q buffer as the B operand (K-major, 128B swizzle,
+// rows 0-15 = e4m3(q 2^shift), rows 16-31 = e4m3(16 (q 2^shift - hi))).
+// Returns the score scale (exp2 domain, times `kvsc`) or a negative value on
+// abort. Piece kk >= 1 waits until the previous piece's last Q.K^T is done.
+template <class LL, int QF>
+__device__ float setup_q(const Stage1Params& p, const Ctx<LL>& cx, SoftmaxCtx& sx, int token, uint32_t kk, float kvsc) {
+  if (kk >= 1 && !cx.wait(LL::kQEmpty, (kk - 1) & 1u)) return -1.f;
+  const int t = 32 * sx.wi + sx.lane;  // 0..127
+  const int h = t >> 3, d0 = 72 * (t & 7);
+  uint8_t* qb = cx.g + LL::kOffQ;
+  auto qaddr = [&](int row, int d) -> uint32_t* {
+    const int unit = (d & 127) >> 4;
+    return reinterpret_cast<uint32_t*>(qb + (d >> 7) * kQChunkBytes + (row >> 3) * 1024 + (row & 7) * 128 +
+                                       ((unit ^ (row & 7)) << 4) + (d & 15));
+  };
+  float c;
+  if (QF == kQBf16) {
+    const uint16_t* src = static_cast<const uint16_t*>(p.q) + (static_cast<int64_t>(token) * kHeads + h) * kDqk + d0;
+    uint32_t w[36];
+#pragma unroll
+    for (int i = 0; i < 9; ++i) {
+      const uint4 v = __ldg(reinterpret_cast<const uint4*>(src) + i);
+      w[4 * i] = v.x; w[4 * i + 1] = v.y; w[4 * i + 2] = v.z; w[4 * i + 3] = v.w;
+    }
+    uint32_t mx = 0;
+#pragma unroll
+    for (int i = 0; i < 36; ++i) mx = __vmaxu2(mx, w[i] & 0x7FFF7FFFu);
+    mx = max(mx & 0xFFFFu, mx >> 16);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+    uint32_t* am = reinterpret_cast<uint32_t*>(cx.g + LL::kOffAmax);
+    if (sx.lane == 0) am[sx.wi] = mx;
+    if (!group_sync(cx, sx)) return -1.f;
+    mx = max(max(am[0], am[1]), max(am[2], am[3]));
+    const int e = static_cast<int>((mx >> 7) & 0xFF);  // biased exponent of max |q|
+    int shift = (mx == 0) ? 0 : 134 - e;               // max |q| 2^shift in [128, 256)
+    shift = max(-126, min(126, shift));
+    const float up = __uint_as_float(static_cast<uint32_t>(shift + 127) << 23);
+    const float down = __uint_as_float(static_cast<uint32_t>(127 - shift) << 23);
+#pragma unroll
+    for (int g = 0; g < 18; ++g) {  // groups of 4 dims: d0 + 4g
+      const float x0 = bf16_bits_to_f32(w[2 * g] & 0xFFFFu) * up, x1 = bf16_bits_to_f32(w[2 * g] >> 16) * up;
+      const float x2 = bf16_bits_to_f32(w[2 * g + 1] & 0xFFFFu) * up, x3 = bf16_bits_to_f32(w[2 * g + 1] >> 16) * up;
+      const uint32_t h01 = f32x2_to_e4m3x2(x0, x1), h23 = f32x2_to_e4m3x2(x2, x3);
+      const float2 d01 = e4m3x2_to_f32x2(h01), d23 = e4m3x2_to_f32x2(h23);
+      const uint32_t l01 = f32x2_to_e4m3x2(kLoScale * (x0 - d01.x), kLoScale * (x1 - d01.y));
+      const uint32_t l23 = f32x2_to_e4m3x2(kLoScale * (x2 - d23.x), kLoScale * (x3 - d23.y));
+      *qaddr(h, d0 + 4 * g) = h01 | (h23 << 16);
+      *qaddr(16 + h, d0 + 4 * g) = l01 | (l23 << 16);
+    }
+    c = p.sm_scale * kLog2e * kvsc * down;
+  } else {
+    const uint8_t* src = static_cast<const uint8_t*>(p.q) + (static_cast<int64_t>(token) * kHeads + h) * kDqk + d0;
+#pragma unroll
+    for (int i = 0; i < 9; ++i) {
+      const uint2 v = __ldg(reinterpret_cast<const uint2*>(src) + i);
+      *qaddr(h, d0 + 8 * i) = v.x;
+      *qaddr(h, d0 + 8 * i + 4) = v.y;
+      *qaddr(16 + h, d0 + 8 * i) = 0u;
+      *qaddr(16 + h, d0 + 8 * i + 4) = 0u;
+    }
+    c = p.sm_scale * kLog2e * kvsc * __ldg(p.q_scale);
+  }
+  fence_async_smem();
+  __syncwarp();
+  if (sx.lane == 0) mbar_arrive(cx.bar(LL::kQFull));
+  return c;
+}
+
+// One row's 64 rope bytes into a no-swizzle K-major A operand: 8-row x 16-byte
+// core matrices, 128 B apart along K, 512 B apart along rows.
+__device__ __forceinline__ void put_rope_row(uint8_t* rope_base, int row, const uint4 (&r)[4]) {
+  uint8_t* base = rope_base + (row >> 3) * 512 + (row & 7) * 16;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) *reinterpret_cast<uint4*>(base + i * 128) = r[i];
+}
+
+// UMMA descriptors for the two products of a tile, shared by both kernels.
+//   Q.K^T k-step ks (32 dims): A = KV rows (K-major, 128B swizzle), B = Q.
+__device__ __forceinline__ uint64_t qk_desc_a(uint32_t vbase, int ks) {
+  return smem_desc(vbase + (ks >> 2) * kChunkBytes + (ks & 3) * 32, 16, 1024, kLayoutSw128);
+}
+__device__ __forceinline__ uint64_t qk_desc_b(uint32_t qbuf, int ks) {
+  return smem_desc(qbuf + (ks >> 2) * kQChunkBytes + (ks & 3) * 32, 16, 1024, kLayoutSw128);
+}
+//   rope k-step ks (32 dims): A = the no-swizzle rope operand, B = Q chunk 4.
+__device__ __forceinline__ uint64_t rope_desc_a(uint32_t rope, int ks) {
+  return smem_desc(rope + ks * 256, 128, 512, kLayoutNone);
+}
+//   P.V: A = V^T dims 128 mb.. of rows 32 ks.. (MN-major, 8-row atoms 1024 B
+//   apart); B = P^T with N = 32 (hi heads, lo heads: core matrices 128 B
+//   apart), K = rows (8-row groups 256 B apart).
+__device__ __forceinline__ uint64_t pv_desc_a(uint32_t vbase, int mb, int ks) {
+  return smem_desc(vbase + mb * kChunkBytes + ks * 4096, kChunkBytes, 1024, kLayoutSw128);
+}
+__device__ __forceinline__ uint64_t pv_desc_b(uint32_t pbuf, int ks) { return smem_desc(pbuf + ks * 1024, 256, 128, kLayoutNone); }
+
+// One row of softmax weights (16 heads, already times kPScale) as hi/lo e4m3
+// into the P operand.
+__device__ __forceinline__ void put_p_row(uint8_t* pbuf, int row, const float (&pv)[16]) {
+  uint32_t hi[4], lo[4];
+#pragma unroll
+  for (int q4 = 0; q4 < 4; ++q4) {
+    const uint32_t h01 = f32x2_to_e4m3x2(pv[4 * q4], pv[4 * q4 + 1]), h23 = f32x2_to_e4m3x2(pv[4 * q4 + 2], pv[4 * q4 + 3]);
+    const float2 d01 = e4m3x2_to_f32x2(h01), d23 = e4m3x2_to_f32x2(h23);
+    hi[q4] = h01 | (h23 << 16);
+    lo[q4] = f32x2_to_e4m3x2(kLoScale * (pv[4 * q4] - d01.x), kLoScale * (pv[4 * q4 + 1] - d01.y)) |
+             (f32x2_to_e4m3x2(kLoScale * (pv[4 * q4 + 2] - d23.x), kLoScale * (pv[4 * q4 + 3] - d23.y)) << 16);
+  }
+  uint8_t* pb = pbuf + (row >> 3) * 256 + (row & 7) * 16;
+  *reinterpret_cast<uint4*>(pb) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+  *reinterpret_cast<uint4*>(pb + 128) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+}
+
+// Multiplies the 4 x 32 O columns of this thread's lane by alpha[head].
+__device__ __forceinline__ void rescale_o(uint32_t ob, const float (&alpha)[16]) {
+#pragma unroll
+  for (int mb = 0; mb < 4; ++mb) {
+    uint32_t o[32];
+    tmem_ld32(ob + 32 * mb, o);
+    tmem_wait_ld();
+#pragma unroll
+    for (int j = 0; j < 32; ++j) o[j] = __float_as_uint(__uint_as_float(o[j]) * alpha[j & 15]);
+    tmem_st32(ob + 32 * mb, o);
+  }
+  tmem_wait_st();
+}
+
+// Epilogue for one piece: O (hi + lo/16 columns) times f[head] to the bf16
+// output (a whole-run piece) or the fp32 partial slot.
+__device__ __forceinline__ void store_o(const Stage1Params& p, const Piece& pc, uint32_t ob, int row, const float (&f)[16]) {
+#pragma unroll
+  for (int mb = 0; mb < 4; ++mb) {
+    uint32_t o[32];
+    tmem_ld32(ob + 32 * mb, o);
+    tmem_wait_ld();
+    const int dim = 128 * mb + row;
+    if (pc.direct) {
+      __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(p.out) + static_cast<int64_t>(pc.token) * kHeads * kDv + dim;
+#pragma unroll
+      for (int h = 0; h < 16; ++h)
+        dst[h * kDv] = __float2bfloat16_rn((__uint_as_float(o[h]) + __uint_as_float(o[16 + h]) * (1.0f / kLoScale)) * f[h]);
+    } else {
+      float* dst = p.part_o + pc.slot * kHeads * kDv + dim;
+#pragma unroll
+      for (int h = 0; h < 16; ++h)
+        dst[h * kDv] = (__uint_as_float(o[h]) + __uint_as_float(o[16 + h]) * (1.0f / kLoScale)) * f[h];
+    }
+  }
+}
+
+// Barrier setup, the block's partition and tensor-memory allocation, common to
+// both kernels. Returns false (before any allocation) when the CTA has no work
+// or the indptrs are invalid.
+template <class LL>
+__device__ __forceinline__ bool cta_begin(const Stage1Params& p, Ctx<LL>& cx, uint8_t* smem_raw, int alloc_warp,
+                                          PieceCursor& cur) {
+  const uint32_t raw = smem_addr(smem_raw);
+  cx.s = (raw + 1023u) & ~1023u;
+  cx.g = smem_raw + (cx.s - raw);
+  cx.abort_word = reinterpret_cast<volatile uint32_t*>(cx.g + LL::kOffAbort);
+  cx.flags = p.dev_flags;
+  if (threadIdx.x == 0) {
+    LL::init_barriers(cx);
+    *cx.abort_word = 0u;
+    fence_mbar_init();
+  }
+  const int64_t parts = p.num_splits, c = blockIdx.x;
+  int64_t* sh = reinterpret_cast<int64_t*>(cx.g + LL::kOffScan);
+  const SegLocate loc = block_locate<LL::kThreads, 1>(
+      p.qo_indptr, p.kv_indptr, p.batch, p.total_q, p.total_kv,
+      [=](int64_t total) { return part_start(c, total, parts); }, 0, sh);
+  if (!loc.ok) {
+    if (threadIdx.x == 0) atomicOr(p.dev_flags, kFlagBadIndptr);
+    return false;
+  }
+  const int64_t x0 = part_start(c, loc.total, parts), x1 = part_start(c + 1, loc.total, parts);
+  if (x0 >= x1 || loc.seg < 0) return false;  // uniform across the block
+  if ((threadIdx.x >> 5) == alloc_warp) tmem_alloc(cx.s + LL::kOffSlot, kTmemCols);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  cx.tmem = *reinterpret_cast<volatile uint32_t*>(cx.g + LL::kOffSlot);
+  cur = PieceCursor{p.qo_indptr, p.kv_indptr, p.batch, x0, x1, loc.seg, loc.seg_vs, c};
+  return true;
+}
+
+template <class LL>
+__device__ __forceinline__ void cta_end(const Ctx<LL>& cx, int alloc_warp) {
+  tc_fence_before();
+  __syncthreads();
+  if ((threadIdx.x >> 5) == alloc_warp) {
+    tc_fence_after();
+    tmem_dealloc(cx.tmem, kTmemCols);
+  }
+}
+
+}  // namespace tc
+}  // namespace mla

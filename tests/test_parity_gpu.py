@@ -6,6 +6,8 @@ error of the design is far below that (bf16 output rounding ~1e-3 relative
 plus bf16-precision softmax weights), so a tighter regression bound of 5e-3
 rel-L2 is also asserted. Dequantisation is compared bit for bit.
 """
+import dataclasses
+
 import numpy as np
 import pytest
 import torch
@@ -54,7 +56,7 @@ def check(got, ref, tight=True):
     err = np.abs(got - ref).max() if got.size else 0.0
     nrm = np.linalg.norm(ref)
     rel = np.linalg.norm(got - ref) / nrm if nrm > 0 else np.linalg.norm(got)
-    assert err <= MAX_ABS, f"max abs {err:.3e}"
+    assert err <= MAX_ABS, f"max abs {err:.3e} (rel-L2 {rel:.3e})"
     assert rel <= REL_L2, f"rel-L2 {rel:.3e}"
     if tight:
         assert rel <= REL_L2_TIGHT, f"rel-L2 {rel:.3e} above the regression bound"
@@ -62,7 +64,7 @@ def check(got, ref, tight=True):
 
 
 COMBOS = [(synth.BF16, synth.BF16), (synth.BF16, synth.FP8_E4M3), (synth.FP8_E4M3, synth.FP8_E4M3),
-          (synth.FP8_E4M3, synth.BF16)]
+          (synth.FP8_E4M3, synth.BF16), (synth.BF16, synth.MXFP4), (synth.FP8_E4M3, synth.MXFP4)]
 RAGGED = [1, 63, 64, 65, 700, 1301, 129, 2]
 
 
@@ -75,7 +77,8 @@ def test_ragged_segments_all_split_counts(q_dtype, kv_dtype, num_splits):
     check(got.float().cpu().numpy(), oracle_ref(inp))
 
 
-@pytest.mark.parametrize("q_dtype,kv_dtype", [(synth.BF16, synth.FP8_E4M3), (synth.BF16, synth.BF16)])
+@pytest.mark.parametrize("q_dtype,kv_dtype", [(synth.BF16, synth.FP8_E4M3), (synth.BF16, synth.BF16),
+                                              (synth.BF16, synth.MXFP4)])
 def test_multi_token_and_empty_segments(q_dtype, kv_dtype):
     # q_len > 1 (non-causal: every token sees the whole segment), kv_len 0 -> zeros, q_len 0 segments
     w = synth.Workload("edge", 5, 1, 0, q_dtype, kv_dtype, seed=5)
@@ -85,6 +88,47 @@ def test_multi_token_and_empty_segments(q_dtype, kv_dtype):
         ref = oracle_ref(inp)
         assert np.array_equal(got[2], np.zeros_like(got[2]))
         check(got, ref)
+
+
+def _with_mxfp4_rows(inp, kvf):
+    """The same inputs with the KV cache replaced by the mxfp4 quantisation of kvf."""
+    kv, sc = synth.quantize_mxfp4(kvf)
+    return dataclasses.replace(inp, kv=kv.contiguous(), kv_scale=sc.contiguous(), kv_dtype=synth.MXFP4)
+
+
+def test_mxfp4_rows_of_very_different_magnitude():
+    # per-row magnitudes 2^-6 .. 2^6 plus all-zero rows: the row exponents differ
+    # across the tile, so the softmax weights carry 2^(x + r - mu) over a wide range
+    lens = [700, 129, 1301, 64]
+    w = synth.Workload("mxrows", len(lens), 1, 0, synth.BF16, synth.MXFP4, seed=31)
+    inp = synth.make_inputs(w, "cuda", kv_lens=lens)
+    g = torch.Generator(device="cuda").manual_seed(77)
+    kvf = torch.randn((inp.total_kv, synth.D_QK), generator=g, device="cuda")
+    e = torch.randint(-6, 7, (inp.total_kv, 1), generator=g, device="cuda").float()
+    kvf = kvf * torch.pow(2.0, e)
+    kvf[::37] = 0.0
+    inp = _with_mxfp4_rows(inp, kvf)
+    ref = oracle_ref(inp)
+    # outputs reach |V| ~ 2^8 here: the absolute bound applies to out / max|out|
+    s = np.abs(ref).max()
+    for ns in (1, 9):
+        check(run_decode(inp, num_splits=ns).float().cpu().numpy() / s, ref / s)
+
+
+def test_mxfp4_blocks_far_below_the_row_maximum():
+    # block magnitudes 2^0 .. 2^-20 inside each row: blocks more than 15 binades
+    # below the row's largest scale are flushed by the kernel (elements under
+    # 2^-15 of the row's largest block range), which the oracle keeps exactly
+    lens = [513, 77, 1000]
+    w = synth.Workload("mxblocks", len(lens), 1, 0, synth.BF16, synth.MXFP4, seed=32)
+    inp = synth.make_inputs(w, "cuda", kv_lens=lens)
+    g = torch.Generator(device="cuda").manual_seed(78)
+    kvf = torch.randn((inp.total_kv, synth.D_QK), generator=g, device="cuda")
+    e = torch.randint(-20, 1, (inp.total_kv, synth.D_QK // 32, 1), generator=g, device="cuda").float()
+    kvf = (kvf.view(inp.total_kv, -1, 32) * torch.pow(2.0, e)).view(inp.total_kv, synth.D_QK)
+    inp = _with_mxfp4_rows(inp, kvf)
+    assert int((inp.kv_scale.max(dim=1).values.int()[:, None] - inp.kv_scale.int() > 15).sum()) > 0
+    check(run_decode(inp, num_splits=5).float().cpu().numpy(), oracle_ref(inp))
 
 
 def test_single_row_segments_return_v_rows():
@@ -104,8 +148,9 @@ def test_sm_scale_override():
     check(got.float().cpu().numpy(), oracle_ref(inp, sm_scale=0.1))
 
 
-def test_deterministic_bitwise():
-    w = synth.Workload("det", 4, 1, 0, synth.BF16, synth.FP8_E4M3, seed=4)
+@pytest.mark.parametrize("kv_dtype", [synth.FP8_E4M3, synth.MXFP4])
+def test_deterministic_bitwise(kv_dtype):
+    w = synth.Workload("det", 4, 1, 0, synth.BF16, kv_dtype, seed=4)
     inp = synth.make_inputs(w, "cuda", kv_lens=[3000, 17, 900, 2048])
     a = run_decode(inp, num_splits=11)
     b = run_decode(inp, num_splits=11)
@@ -199,7 +244,7 @@ def test_workload_a8w8_bs64_kv1024_full():
     check(got.float().cpu().numpy(), oracle_ref(inp))
 
 
-@pytest.mark.parametrize("name", ["fp8kv_bs32_kv8192", "fp8kv_bs256_kv8192"])
+@pytest.mark.parametrize("name", ["fp8kv_bs32_kv8192", "fp8kv_bs256_kv8192", "mxfp4_bs128_ragged16384"])
 def test_workload_large_sampled(name):
     """Full size, the benchmark's launch configuration (planner default); the
     oracle computes a sample of (token, head) rows spread over the batch."""
