@@ -37,7 +37,12 @@ namespace mla {
 namespace tc {
 namespace mx {
 
-constexpr int kThreads = 256;
+constexpr int kThreads = 384;  // warpgroup 0 converts, 1 runs the softmax, 2 issues the UMMAs (warp 8)
+// Registers per thread: launched at 168 (384 threads), then the issuing
+// warpgroup gives up 112 so the converting and softmax warpgroups get 224
+// (128 x (224 + 224 + 56) = 384 x 168: the split uses exactly the launch budget).
+constexpr uint32_t kLaunchRegs = 168, kWorkRegs = 224, kIssueRegs = 56;
+static_assert(kWorkRegs * 2 + kIssueRegs == 3 * kLaunchRegs, "register split must equal the launch budget");
 constexpr int kStages = 2;
 constexpr int kStageBytes = kVBytes + kRopeBytes;  // 72 KB: V dims + rope dims (e5m2)
 constexpr int kMaxRebase = 15;  // e5m2 holds e2m1 * 2^-down exactly for down <= 15
@@ -53,7 +58,8 @@ struct L {
   static constexpr int kOffRedL = kOffRedMu + 2 * 4 * 16 * 4;        // [4][16] f32
   static constexpr int kOffAmax = kOffRedL + 4 * 16 * 4;             // [4] u32
   static constexpr int kOffScan = kOffAmax + 16;                     // 16 x i64
-  static constexpr int kOffRaw = kOffScan + 16 * 8;                  // [4 warps][32 rows][288 B] fp4x2
+  static constexpr int kOffMeta = kOffScan + 16 * 8;                 // [4] u32: bookkeeping of tile i in slot i % 4
+  static constexpr int kOffRaw = kOffMeta + 16;                  // [4 warps][32 rows][288 B] fp4x2
   static constexpr int kOffRawSc = kOffRaw + 4 * 32 * (kDqk / 2);    // [4 warps][32 rows][18 B] e8m0
   static constexpr int kOffBars = kOffRawSc + 4 * 32 * (kDqk / kMxBlock);
   enum {
@@ -90,13 +96,14 @@ using Cx = Ctx<L>;
 // and phase, summed over the launch. Off by default.
 #ifdef MLA_PHASE_TIMING
 constexpr int kPhaseCtas = 1024;
-__device__ unsigned long long g_mx_phase[kPhaseCtas * 8 * 8];
+constexpr int kPhaseWarps = kThreads / 32;
+__device__ unsigned long long g_mx_phase[kPhaseCtas * kPhaseWarps * 8];
 #define MX_PT_INIT long long mx_pt_ = clock64();
 #define MX_PT(ph)                                                                                          \
   do {                                                                                                     \
     const long long now_ = clock64();                                                                      \
     if ((threadIdx.x & 31) == 0 && blockIdx.x < kPhaseCtas)                                                \
-      atomicAdd(&g_mx_phase[(blockIdx.x * 8 + (threadIdx.x >> 5)) * 8 + (ph)],                             \
+      atomicAdd(&g_mx_phase[(blockIdx.x * kPhaseWarps + (threadIdx.x >> 5)) * 8 + (ph)],                   \
                 static_cast<unsigned long long>(now_ - mx_pt_));                                           \
     mx_pt_ = now_;                                                                                         \
   } while (0)
@@ -118,6 +125,43 @@ struct MxRaw {
   uint32_t sc[9];
 };
 
+// Per-tile bookkeeping of the UMMA issuer, packed in one word: bit 0 = first
+// tile of its piece, bit 1 = last tile of its piece, bits 2.. = piece index
+// within the CTA.
+struct TileMeta {
+  uint32_t k;
+  bool first, last;
+  __device__ static TileMeta unpack(uint32_t w) { return TileMeta{w >> 2, (w & 1u) != 0, (w & 2u) != 0}; }
+};
+
+// The CTA's tiles in order, with their bookkeeping words.
+struct MetaTileWalker {
+  PieceCursor cur;
+  Piece pc;
+  int r0 = 0;
+  uint32_t k = 0;
+  bool have = false;
+  __device__ void init(const PieceCursor& c) {
+    cur = c;
+    have = cur.next(pc);
+    r0 = 0;
+    k = 0;
+  }
+  // First KV row and bookkeeping word of the next tile. Returns false when done.
+  __device__ bool next(int32_t& row, uint32_t& meta) {
+    if (!have) return false;
+    row = pc.kv_row + r0;
+    meta = (k << 2) | (r0 == 0 ? 1u : 0u) | (r0 + kTileRows >= pc.nrows ? 2u : 0u);
+    r0 += kTileRows;
+    if (r0 >= pc.nrows) {
+      have = cur.next(pc);
+      r0 = 0;
+      ++k;
+    }
+    return true;
+  }
+};
+
 // Global loads that stay where they are written (issued two tiles ahead of
 // their use; the compiler may not sink them next to the use).
 __device__ __forceinline__ uint4 ld_pinned_v4(const void* p) {
@@ -135,9 +179,11 @@ __device__ __forceinline__ uint32_t ld_pinned_u16(const void* p) {
 
 // Loads the warp's rows of the next tile (rows past the end of the cache or of
 // the CTA's tiles read as zero).
-__device__ __forceinline__ void load_mx_raw(const Stage1Params& p, TileWalker& rw, int warp, int lane, MxRaw& r) {
-  int32_t row0;
-  const bool have = rw.next(row0);
+__device__ __forceinline__ void load_mx_raw(const Stage1Params& p, MetaTileWalker& rw, int warp, int lane, MxRaw& r,
+                                            uint32_t& meta) {
+  int32_t row0 = 0;
+  meta = 0;
+  const bool have = rw.next(row0, meta);
   const int64_t gb = static_cast<int64_t>(row0) + 32 * warp;
   const uint8_t* kvb = static_cast<const uint8_t*>(p.kv) + gb * (kDqk / 2) + 16 * lane;
   const uint8_t* scb = static_cast<const uint8_t*>(p.kv_scale) + gb * (kDqk / kMxBlock) + 2 * lane;
@@ -262,48 +308,19 @@ __device__ __forceinline__ void convert_tile(const Cx& cx, uint32_t i, int warp,
 
 // Hands stage i % 2 to the UMMA issuer (generic-proxy writes made visible to
 // the tensor core first).
-__device__ __forceinline__ void publish_tile(const Cx& cx, uint32_t i, int lane) {
+__device__ __forceinline__ void publish_tile(const Cx& cx, uint32_t i, int warp, int lane, uint32_t meta) {
+  if (warp == 0 && lane == 0) reinterpret_cast<volatile uint32_t*>(cx.g + L::kOffMeta)[i & 3u] = meta;
   fence_async_smem();
   __syncwarp();
   if (lane == 0) mbar_arrive(cx.bar(L::kKvFull + (i & 1u)));
 }
 
-// Per-tile bookkeeping of the UMMA issuer.
-struct TileMeta {
-  uint32_t k;  // piece index within the CTA
-  bool first, last;
-};
-struct MetaWalker {
-  PieceCursor cur;
-  Piece pc;
-  int r0;
-  uint32_t k;
-  __device__ void init(const PieceCursor& c) {
-    cur = c;
-    cur.next(pc);
-    r0 = 0;
-    k = 0;
-  }
-  __device__ TileMeta next() {
-    const TileMeta m{k, r0 == 0, r0 + kTileRows >= pc.nrows};
-    r0 += kTileRows;
-    if (r0 >= pc.nrows) {
-      cur.next(pc);
-      r0 = 0;
-      ++k;
-    }
-    return m;
-  }
-};
-
 constexpr uint32_t kIdQK = umma_idesc(128, 32, 1, 0, false, false);  // A e5m2 K-major, B e4m3
 constexpr uint32_t kIdPV = umma_idesc(128, 32, 1, 0, true, true);    // A = V^T MN-major, B = P^T MN-major
 
-__device__ __forceinline__ bool issue_qk(const Cx& cx, uint32_t i, const TileMeta& t) {
+// Q.K^T of tile i into S[i % 2] (its stage, S buffer and q are ready).
+__device__ __forceinline__ void issue_qk(const Cx& cx, uint32_t i, const TileMeta& t) {
   const uint32_t b = i & 1u;
-  if (t.first && !cx.wait(L::kQFull, t.k & 1u)) return false;
-  if (!cx.wait(L::kKvFull + b, (i >> 1) & 1u)) return false;
-  if (i >= 2 && !cx.wait(L::kSEmpty + b, ((i - 2) >> 1) & 1u)) return false;
   tc_fence_after();
   const uint32_t stage = cx.s + L::kOffKv + b * kStageBytes, qbuf = cx.s + L::kOffQ;
   const uint32_t d = cx.tmem + kTmemS + 32 * b;
@@ -313,13 +330,11 @@ __device__ __forceinline__ bool issue_qk(const Cx& cx, uint32_t i, const TileMet
   for (int ks = 0; ks < 2; ++ks) umma_e4m3(d, rope_desc_a(stage + kVBytes, ks), qk_desc_b(qbuf, 16 + ks), kIdQK, 1u);
   umma_commit(cx.bar(L::kSFull + b));
   if (t.last) umma_commit(cx.bar(L::kQEmpty));
-  return true;
 }
 
-__device__ __forceinline__ bool issue_pv(const Cx& cx, uint32_t i, const TileMeta& t) {
+// P.V of tile i into O[piece % 2] (its P is written and O is free).
+__device__ __forceinline__ void issue_pv(const Cx& cx, uint32_t i, const TileMeta& t) {
   const uint32_t b = i & 1u;
-  if (!cx.wait(L::kPFull + b, (i >> 1) & 1u)) return false;
-  if (t.first && t.k >= 2 && !cx.wait(L::kOEmpty + (t.k & 1u), ((t.k >> 1) - 1) & 1u)) return false;
   tc_fence_after();
   const uint32_t stage = cx.s + L::kOffKv + b * kStageBytes, pbuf = cx.s + L::kOffP + b * kPBytes;
   const uint32_t obuf = cx.tmem + kTmemO + (t.k & 1u) * 128;
@@ -330,80 +345,87 @@ __device__ __forceinline__ bool issue_pv(const Cx& cx, uint32_t i, const TileMet
       umma_e4m3(obuf + 32 * mb, pv_desc_a(stage, mb, ks), pv_desc_b(pbuf, ks), kIdPV, (ks > 0 || !t.first) ? 1u : 0u);
   umma_commit(cx.bar(L::kPvDone + b));
   if (t.last) umma_commit(cx.bar(L::kOFull + (t.k & 1u)));
-  return true;
 }
 
 __device__ void converter_role(const Stage1Params& p, const Cx& cx, PieceCursor cur, int warp, int lane) {
-  const bool issuer = (warp == 0 && lane == 0);
   const uint32_t ntiles = static_cast<uint32_t>(count_tiles(cur));
   uint8_t* raw_w = cx.g + L::kOffRaw + warp * 32 * (kDqk / 2);
   uint8_t* sc_w = cx.g + L::kOffRawSc + warp * 32 * (kDqk / kMxBlock);
-  TileWalker rw;
+  MetaTileWalker rw;
   rw.init(cur);
-  MetaWalker mq, mp;
-  mq.init(cur);
-  mp.init(cur);
   MxRaw ra, rb;  // the even / odd tile in flight
-  load_mx_raw(p, rw, warp, lane, ra);
-  load_mx_raw(p, rw, warp, lane, rb);
-  bool ok = true;
+  uint32_t ma, mb;
+  load_mx_raw(p, rw, warp, lane, ra, ma);
+  load_mx_raw(p, rw, warp, lane, rb, mb);
   MX_PT_INIT
-  for (uint32_t i = 0; ok && i < ntiles; i += 2) {
+  for (uint32_t i = 0; i < ntiles; i += 2) {
     const bool two = i + 1 < ntiles;
     MX_PT(7);
     if (!wait_stage(cx, i)) break;
     MX_PT(3);
     dump_raw(raw_w, sc_w, lane, ra);
     __syncwarp();
-    MX_PT(4);
-    load_mx_raw(p, rw, warp, lane, ra);  // tile i + 2
+    const uint32_t m0 = ma;
+    load_mx_raw(p, rw, warp, lane, ra, ma);  // tile i + 2
     MX_PT(5);
     convert_tile(cx, i, warp, lane, raw_w, sc_w);
     MX_PT(0);
-    publish_tile(cx, i, lane);
+    publish_tile(cx, i, warp, lane, m0);
     MX_PT(6);
-    if (warp == 0) {
-      if (issuer) ok = issue_qk(cx, i, mq.next());
-      ok = __shfl_sync(0xffffffffu, ok, 0);
-      if (!ok) break;
-    }
-    MX_PT(1);
-    if (two) {
-      if (!wait_stage(cx, i + 1)) break;
-      MX_PT(3);
-      dump_raw(raw_w, sc_w, lane, rb);
-      __syncwarp();
-      MX_PT(4);
-      load_mx_raw(p, rw, warp, lane, rb);  // tile i + 3
-      MX_PT(5);
-      convert_tile(cx, i + 1, warp, lane, raw_w, sc_w);
-      MX_PT(0);
-      publish_tile(cx, i + 1, lane);
-      MX_PT(6);
-      if (warp == 0) {
-        if (issuer) ok = issue_qk(cx, i + 1, mq.next());
-        ok = __shfl_sync(0xffffffffu, ok, 0);
-        if (!ok) break;
-      }
-      MX_PT(1);
-    }
-    if (warp == 0) {
-      if (issuer) {
-        ok = issue_pv(cx, i, mp.next());
-        if (ok && two) ok = issue_pv(cx, i + 1, mp.next());
-      }
-      ok = __shfl_sync(0xffffffffu, ok, 0);
-      MX_PT(2);
-    }
-  }
-  if (warp == 0) {
-    // every issued tcgen05 operation completes before tensor memory is freed
-    if (issuer) {
-      umma_commit(cx.bar(L::kDrain));
-      mbar_wait_drain_tc(cx.bar(L::kDrain), 0);
-    }
+    if (!two) break;
+    if (!wait_stage(cx, i + 1)) break;
+    MX_PT(3);
+    dump_raw(raw_w, sc_w, lane, rb);
     __syncwarp();
+    const uint32_t m1 = mb;
+    load_mx_raw(p, rw, warp, lane, rb, mb);  // tile i + 3
+    MX_PT(5);
+    convert_tile(cx, i + 1, warp, lane, raw_w, sc_w);
+    MX_PT(0);
+    publish_tile(cx, i + 1, warp, lane, m1);
+    MX_PT(6);
   }
+}
+
+// Warp 8, lane 0: issues Q.K^T of tile qi and P.V of tile pi as soon as each
+// is ready (non-blocking tests, bounded overall), in tile order for each kind.
+__device__ void issuer_role(const Cx& cx, PieceCursor cur) {
+  const uint32_t n = static_cast<uint32_t>(count_tiles(cur));
+  const volatile uint32_t* meta = reinterpret_cast<const volatile uint32_t*>(cx.g + L::kOffMeta);
+  uint32_t qi = 0, pi = 0;
+  long long t0 = clock64();
+  while (pi < n) {
+    bool progressed = false;
+    if (pi < qi && mbar_test_wait(cx.bar(L::kPFull + (pi & 1u)), (pi >> 1) & 1u)) {
+      const TileMeta t = TileMeta::unpack(meta[pi & 3u]);
+      if (!t.first || t.k < 2 || mbar_test_wait(cx.bar(L::kOEmpty + (t.k & 1u)), ((t.k >> 1) - 1) & 1u)) {
+        issue_pv(cx, pi, t);
+        ++pi;
+        progressed = true;
+      }
+    }
+    if (qi < n && mbar_test_wait(cx.bar(L::kKvFull + (qi & 1u)), (qi >> 1) & 1u) &&
+        (qi < 2 || mbar_test_wait(cx.bar(L::kSEmpty + (qi & 1u)), ((qi - 2) >> 1) & 1u))) {
+      const TileMeta t = TileMeta::unpack(meta[qi & 3u]);
+      if (!t.first || mbar_test_wait(cx.bar(L::kQFull), t.k & 1u)) {
+        issue_qk(cx, qi, t);
+        ++qi;
+        progressed = true;
+      }
+    }
+    if (progressed) {
+      t0 = clock64();
+    } else if (*cx.abort_word) {
+      break;
+    } else if (clock64() - t0 > kWaitLimitCycles) {
+      *cx.abort_word = 1u;
+      atomicOr(cx.flags, kFlagTimeout);
+      break;
+    }
+  }
+  // every issued tcgen05 operation completes before tensor memory is freed
+  umma_commit(cx.bar(L::kDrain));
+  mbar_wait_drain_tc(cx.bar(L::kDrain), 0);
 }
 
 // 2^e for an integer e in [-127, 127] (exact).
@@ -548,18 +570,25 @@ __global__ void __launch_bounds__(kThreads, 1) stage1_mx_kernel(const Stage1Para
   extern __shared__ uint8_t smem_raw[];
   Cx cx;
   PieceCursor cur;
-  if (!cta_begin(p, cx, smem_raw, 0, cur)) return;
+  if (!cta_begin(p, cx, smem_raw, 8, cur)) return;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  if (warp < 4)
+  if (warp < 4) {
+    setmaxnreg_inc<kWorkRegs>();
     converter_role(p, cx, cur, warp, lane);
-  else
+  } else if (warp < 8) {
+    setmaxnreg_inc<kWorkRegs>();
     softmax_role<QF>(p, cx, cur, warp, lane);
-  cta_end(cx, 0);
+  } else {
+    setmaxnreg_dec<kIssueRegs>();
+    if (warp == 8 && lane == 0) issuer_role(cx, cur);
+    __syncwarp();
+  }
+  cta_end(cx, 8);
 }
 
 #ifdef MLA_PHASE_TIMING
 extern "C" int mla_debug_phase_cycles_mx(unsigned long long* host, int n, int reset) {
-  if (n > kPhaseCtas * 64) n = kPhaseCtas * 64;
+  if (n > kPhaseCtas * kPhaseWarps * 8) n = kPhaseCtas * kPhaseWarps * 8;
   if (cudaMemcpyFromSymbol(host, g_mx_phase, sizeof(unsigned long long) * n) != cudaSuccess) return -1;
   if (reset) {
     void* q = nullptr;
@@ -577,6 +606,12 @@ static cudaError_t launch_q(const Stage1Params& p, cudaStream_t stream) {
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (configured_device != dev) {
+    // the warpgroup register split adds up to the launch budget only at 168
+    // registers per thread; anything else would leave setmaxnreg waiting
+    cudaFuncAttributes fa;
+    e = cudaFuncGetAttributes(&fa, stage1_mx_kernel<QF>);
+    if (e != cudaSuccess) return e;
+    if (fa.numRegs != static_cast<int>(kLaunchRegs)) return cudaErrorInvalidKernelImage;
     e = cudaFuncSetAttribute(stage1_mx_kernel<QF>, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kAlloc);
     if (e != cudaSuccess) return e;
     configured_device = dev;
