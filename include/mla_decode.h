@@ -105,9 +105,12 @@ mla_status_t mla_plan(int32_t batch, int32_t total_q, int32_t total_kv, mla_dtyp
 
 /* Bytes of device workspace that mla_decode() needs for these sizes and this
  * partition count (0 = what mla_plan() would choose on the current device).
- * The workspace holds a 256-byte header (the device error flags) and the
- * per-split partial outputs: (num_splits + total_q) slots of 16x512 fp32 plus
- * 16 fp32 LSE values. Host only.                                              */
+ * The workspace holds a 256-byte header (the device error flags), one 32-bit
+ * counter per query token (padded to 256 bytes) and the per-split partial
+ * outputs: (num_splits + total_q) slots of 16x512 fp32 plus 16 fp32 LSE
+ * values. It must be zero-filled before its first use; every call leaves the
+ * counters at zero again, and mla_reset_device_error() restores them after an
+ * error. Host only.                                                          */
 mla_status_t mla_decode_workspace_size(int32_t batch, int32_t total_q, int32_t total_kv,
                                        mla_dtype_t kv_dtype, int32_t num_splits, size_t* bytes);
 
@@ -172,7 +175,9 @@ mla_status_t mla_dequant_rows(const void* kv, const void* kv_scale, mla_dtype_t 
  * MLA_ERR_DEVICE_CHECK (timeout wins); *flags may be NULL.                    */
 mla_status_t mla_get_device_error(const void* workspace, void* stream, uint32_t* flags);
 
-/* Clears the device error flags (flags are sticky until cleared). Async.      */
+/* Clears the device error flags (flags are sticky until cleared) and the token
+ * counters that a call stopped by an error may have left non-zero.
+ * Synchronises `stream` (it reads how many counters the last call used).      */
 mla_status_t mla_reset_device_error(void* workspace, void* stream);
 
 /* Milliseconds between two CUDA events (cudaEvent_t passed as void*) that

@@ -132,7 +132,8 @@ mla_status_t mla_decode(const void* q, const void* kv, const void* kv_scale, con
   uint8_t* ws = static_cast<uint8_t*>(opts->workspace);
   p.dev_flags = reinterpret_cast<uint32_t*>(ws);
   const int64_t slots = static_cast<int64_t>(splits) + total_q;
-  p.part_o = reinterpret_cast<float*>(ws + mla::kHeaderBytes);
+  p.tok_cnt = reinterpret_cast<uint32_t*>(ws + mla::kHeaderBytes);
+  p.part_o = reinterpret_cast<float*>(ws + mla::kHeaderBytes + mla::counter_bytes(total_q));
   p.part_lse = p.part_o + slots * mla::kHeads * mla::kDv;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   auto mark = [&](int i) {
@@ -144,7 +145,9 @@ mla_status_t mla_decode(const void* q, const void* kv, const void* kv_scale, con
     if (mla::launch_stage1(kv_dtype, opts->q_dtype, p, st) != cudaSuccess) return MLA_ERR_CUDA;
   }
   if (!mark(1)) return MLA_ERR_CUDA;
-  if (mla::launch_stage2(p, st) != cudaSuccess) return MLA_ERR_CUDA;
+  // the tensor-core kernels merge split tokens and zero empty segments themselves
+  const bool merged = mla::stage1_merges(kv_dtype) && total_kv > 0;
+  if (!merged && mla::launch_stage2(p, st) != cudaSuccess) return MLA_ERR_CUDA;
   if (!mark(2)) return MLA_ERR_CUDA;
   return MLA_OK;
 }
@@ -218,8 +221,14 @@ mla_status_t mla_get_device_error(const void* workspace, void* stream, uint32_t*
 
 mla_status_t mla_reset_device_error(void* workspace, void* stream) {
   if (!workspace) return MLA_ERR_INVALID_ARG;
-  if (cudaMemsetAsync(workspace, 0, sizeof(uint32_t), static_cast<cudaStream_t>(stream)) != cudaSuccess)
-    return MLA_ERR_CUDA;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  // header word 1: how many token counters the last call used (they may be
+  // left part-counted when a call stopped on an error)
+  uint32_t words[2] = {0u, 0u};
+  if (cudaMemcpyAsync(words, workspace, sizeof(words), cudaMemcpyDeviceToHost, st) != cudaSuccess) return MLA_ERR_CUDA;
+  if (cudaStreamSynchronize(st) != cudaSuccess) return MLA_ERR_CUDA;
+  const size_t n = mla::kHeaderBytes + mla::counter_bytes(words[1]);
+  if (cudaMemsetAsync(workspace, 0, n, st) != cudaSuccess) return MLA_ERR_CUDA;
   return MLA_OK;
 }
 
@@ -262,8 +271,9 @@ extern "C" mla_status_t mla_decode_static_workspace(const void* q, const void* k
   mla_decode_opts o = *opts;
   if (o.num_splits == 0) o.num_splits = plan_splits(o.total_q, o.batch, o.total_kv, sm_count_of_current_device());
   if (mla::workspace_bytes_for(o.num_splits, o.total_q) > MLA_STATIC_WORKSPACE_BYTES) return MLA_ERR_TOO_LARGE;
-  // the error flags are the only scratch that must start at zero
-  if (cudaMemsetAsync(g_static_ws_ptr[dev], 0, sizeof(uint32_t), static_cast<cudaStream_t>(stream)) != cudaSuccess)
+  // the error flags and the token counters are the scratch that must start at zero
+  if (cudaMemsetAsync(g_static_ws_ptr[dev], 0, mla::kHeaderBytes + mla::counter_bytes(o.total_q),
+                      static_cast<cudaStream_t>(stream)) != cudaSuccess)
     return MLA_ERR_CUDA;
   o.workspace = g_static_ws_ptr[dev];
   o.workspace_bytes = MLA_STATIC_WORKSPACE_BYTES;

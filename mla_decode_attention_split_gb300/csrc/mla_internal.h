@@ -12,9 +12,12 @@ constexpr int kDqk = 576;
 constexpr int kDv = 512;
 constexpr int kMxBlock = 32;
 
-// Workspace layout: [header 256 B: error flags][part_o: slots x 16 x 512 f32]
-// [part_lse: slots x 16 f32], slots = num_splits + total_q.
+// Workspace layout: [header 256 B: word 0 = error flags, word 1 = token count
+// of the last call that used the counters][token counters: total_q u32, padded
+// to 256 B][part_o: slots x 16 x 512 f32][part_lse: slots x 16 f32], slots =
+// num_splits + total_q. The counters are zero between calls.
 constexpr size_t kHeaderBytes = 256;
+inline size_t counter_bytes(int64_t total_q) { return static_cast<size_t>((total_q * 4 + 255) / 256) * 256; }
 
 struct Stage1Params {
   const void* q;
@@ -32,6 +35,7 @@ struct Stage1Params {
   float* part_o;      // [slots][16][512]
   float* part_lse;    // [slots][16] (log2 domain)
   uint32_t* dev_flags;
+  uint32_t* tok_cnt;  // [total_q] partials finished per token (kernels that merge in stage 1)
 };
 
 // KV formats / query formats as template tags (values match mla_dtype_t).
@@ -47,10 +51,12 @@ cudaError_t launch_stage2(const Stage1Params& p, cudaStream_t stream);
 cudaError_t launch_dequant(const void* kv, const void* kv_scale, int kv_fmt, int32_t total_kv, int32_t row0,
                            int32_t nrows, float* out, cudaStream_t stream);
 bool stage1_supported(int kv_fmt, int q_fmt);
+// Stage 1 merges the partials itself (the tensor-core kernels); otherwise stage 2 runs.
+inline bool stage1_merges(int kv_fmt) { return kv_fmt == kKvFp8 || kv_fmt == kKvMxfp4; }
 
 inline size_t workspace_bytes_for(int64_t num_splits, int64_t total_q) {
   const int64_t slots = num_splits + total_q;
-  return kHeaderBytes + static_cast<size_t>(slots) * kHeads * kDv * sizeof(float) +
+  return kHeaderBytes + counter_bytes(total_q) + static_cast<size_t>(slots) * kHeads * kDv * sizeof(float) +
          static_cast<size_t>(slots) * kHeads * sizeof(float);
 }
 

@@ -140,6 +140,8 @@ struct Piece {
   int32_t nrows;      // rows in the piece (>= 1)
   int32_t direct;     // the piece is the token's whole run: write the output
   int64_t slot;       // partial slot (c + token) when not direct
+  int64_t tok_vs;     // virtual start of the token's whole run
+  int32_t kvlen;      // its length (the segment's KV rows)
 };
 
 struct PieceCursor {
@@ -171,6 +173,8 @@ struct PieceCursor {
       pc.nrows = static_cast<int32_t>(stop - x);
       pc.direct = (row_in == 0 && stop == tok_vs + kvlen) ? 1 : 0;
       pc.slot = cta + pc.token;
+      pc.tok_vs = tok_vs;
+      pc.kvlen = static_cast<int32_t>(kvlen);
       x = stop;
       return true;
     }

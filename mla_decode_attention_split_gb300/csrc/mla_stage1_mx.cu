@@ -57,15 +57,17 @@ struct L {
   static constexpr int kOffRedMu = kOffRedMax + 2 * 4 * 16 * 4;      // [2][4][16] f32
   static constexpr int kOffRedL = kOffRedMu + 2 * 4 * 16 * 4;        // [4][16] f32
   static constexpr int kOffAmax = kOffRedL + 4 * 16 * 4;             // [4] u32
-  static constexpr int kOffScan = kOffAmax + 16;                     // 16 x i64
+  static constexpr int kOffMList = kOffAmax + 16;                    // MergeList (32 B)
+  static constexpr int kOffScan = kOffMList + 32;                    // 16 x i64
   static constexpr int kOffMeta = kOffScan + 16 * 8;                 // [4] u32: bookkeeping of tile i in slot i % 4
   static constexpr int kOffRaw = kOffMeta + 16;                  // [4 warps][32 rows][288 B] fp4x2
   static constexpr int kOffRawSc = kOffRaw + 4 * 32 * (kDqk / 2);    // [4 warps][32 rows][18 B] e8m0
   static constexpr int kOffBars = kOffRawSc + 4 * 32 * (kDqk / kMxBlock);
   enum {
     kKvFull = 0, kSFull = 2, kSEmpty = 4, kPFull = 6, kPvDone = 8, kQFull = 10, kQEmpty = 11, kOFull = 12,
-    kOEmpty = 14, kGrp = 16, kDrain = 18, kNumBars = 19
+    kOEmpty = 14, kGrp = 16, kDrain = 18, kMerge = 19, kNumBars = 20
   };
+  static constexpr int kMergeBytes = kStages * kStageBytes;  // the stages hold partials for the end-of-CTA merge
   static constexpr int kOffSlot = kOffBars + kNumBars * 8;
   static constexpr int kOffAbort = kOffSlot + 8;
   static constexpr int kBytes = kOffAbort + 8;
@@ -557,6 +559,7 @@ __device__ void softmax_role(const Stage1Params& p, const Cx& cx, PieceCursor cu
     tc_fence_before();
     __syncwarp();
     if (lane == 0) mbar_arrive(cx.bar(L::kOEmpty + (k & 1u)));
+    if (!pc.direct && !finish_partial(p, cx, sx, pc)) return;
     MX_PT(6);
     pc = nxt;
     have = have_next;
@@ -575,15 +578,18 @@ __global__ void __launch_bounds__(kThreads, 1) stage1_mx_kernel(const Stage1Para
   if (warp < 4) {
     setmaxnreg_inc<kWorkRegs>();
     converter_role(p, cx, cur, warp, lane);
+    setmaxnreg_dec<kLaunchRegs>();
   } else if (warp < 8) {
     setmaxnreg_inc<kWorkRegs>();
     softmax_role<QF>(p, cx, cur, warp, lane);
+    setmaxnreg_dec<kLaunchRegs>();
   } else {
     setmaxnreg_dec<kIssueRegs>();
     if (warp == 8 && lane == 0) issuer_role(cx, cur);
     __syncwarp();
+    setmaxnreg_inc<kLaunchRegs>();  // back to the launch budget for the common tail
   }
-  cta_end(cx, 8);
+  cta_end(p, cx, 8);
 }
 
 #ifdef MLA_PHASE_TIMING

@@ -53,12 +53,14 @@ struct L {
   static constexpr int kOffRedMax = kOffP + kPBytes;              // [2][4][16] f32
   static constexpr int kOffRedL = kOffRedMax + 2 * 4 * 16 * 4;    // [4][16] f32
   static constexpr int kOffAmax = kOffRedL + 4 * 16 * 4;          // [4] u32
-  static constexpr int kOffScan = kOffAmax + 16;                  // 16 x i64
+  static constexpr int kOffMList = kOffAmax + 16;                 // MergeList (32 B)
+  static constexpr int kOffScan = kOffMList + 32;                 // 16 x i64
   static constexpr int kOffBars = kOffScan + 16 * 8;
   enum {
     kKvFull = 0, kKvEmpty = 3, kSFull = 6, kSEmpty = 8, kRopeFull = 10, kPFull = 11, kPEmpty = 12, kQFull = 13,
-    kQEmpty = 14, kOFull = 15, kOEmpty = 17, kGrp = 19, kDrain = 21, kNumBars = 22
+    kQEmpty = 14, kOFull = 15, kOEmpty = 17, kGrp = 19, kDrain = 21, kMerge = 22, kNumBars = 23
   };
+  static constexpr int kMergeBytes = kStages * kStageBytes;  // the stages hold partials for the end-of-CTA merge
   static constexpr int kOffSlot = kOffBars + kNumBars * 8;
   static constexpr int kOffAbort = kOffSlot + 8;
   static constexpr int kBytes = kOffAbort + 8;
@@ -404,6 +406,7 @@ __device__ void softmax_role(const Stage1Params& p, const Cx& cx, PieceCursor cu
     tc_fence_before();
     __syncwarp();
     if (lane == 0) mbar_arrive(cx.bar(L::kOEmpty + (k & 1u)));
+    if (!pc.direct && !finish_partial(p, cx, sx, pc)) return;
     TC_PT(6);
     pc = nxt;
     have = have_next;
@@ -426,7 +429,7 @@ __global__ void __launch_bounds__(kThreads, 1) stage1_tc_kernel(const Stage1Para
     __syncwarp();
   } else
     softmax_role<QF>(p, cx, cur, warp, lane);
-  cta_end(cx, 1);
+  cta_end(p, cx, 1);
 }
 
 // ---------------------------------------------------------------------------

@@ -42,6 +42,7 @@ struct Ctx {
   volatile uint32_t* abort_word;
   uint32_t* flags;
   uint32_t tmem;
+  int64_t total;  // virtual rows of the whole launch
   __device__ __forceinline__ uint32_t bar(int i) const { return s + LL::kOffBars + 8u * i; }
   __device__ __forceinline__ bool wait(int i, uint32_t parity) const { return mbar_wait(bar(i), parity, abort_word, flags); }
 };
@@ -291,6 +292,134 @@ __device__ __forceinline__ void store_o(const Stage1Params& p, const Piece& pc, 
   }
 }
 
+// Output rows of tokens whose segment has no KV rows are zero. CTA c writes
+// them for segments c, c + P, c + 2P, ... (every CTA runs this, with or
+// without work of its own).
+template <int kThreads>
+__device__ __forceinline__ void zero_empty_tokens(const Stage1Params& p) {
+  for (int b = blockIdx.x; b < p.batch; b += gridDim.x) {
+    if (__ldg(p.kv_indptr + b + 1) != __ldg(p.kv_indptr + b)) continue;
+    const int64_t q0 = __ldg(p.qo_indptr + b), q1 = __ldg(p.qo_indptr + b + 1);
+    uint4* o = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.out) + q0 * kHeads * kDv);
+    const int64_t n = (q1 - q0) * (kHeads * kDv / 8);  // 16-byte units
+    for (int64_t i = threadIdx.x; i < n; i += kThreads) o[i] = make_uint4(0u, 0u, 0u, 0u);
+  }
+}
+
+// Merge of split tokens (the pages' stage 2). The CTA whose partial completes a
+// token's count merges it, at the very end of the CTA when its stage buffers
+// are free: with L = max_s lse_s, out = sum_s 2^(lse_s - L) O_s /
+// sum_s 2^(lse_s - L) over the partial slots c + token of the CTAs c0..c1 that
+// hold pieces of the token. A CTA holds at most two split pieces (the first
+// and the last of its range), so it merges at most two tokens.
+struct MergeList {
+  uint32_t n;                      // tokens this CTA merges (at most 2)
+  int32_t token[2], c0[2], c1[2];  // token and the CTAs that hold its pieces
+  uint32_t pad;
+};
+
+// After the 128 softmax threads wrote this CTA's partial of a split token:
+// publish it and count it on the token's counter; if it completes the count,
+// list the token for the end-of-CTA merge. The group barrier orders all 128
+// threads' writes before thread 0's gpu-scope fence, which is cumulative, so
+// only thread 0 waits for the writes to reach L2. Returns false on abort.
+template <class LL>
+__device__ __forceinline__ bool finish_partial(const Stage1Params& p, const Ctx<LL>& cx, SoftmaxCtx& sx,
+                                               const Piece& pc) {
+  if (!group_sync(cx, sx)) return false;
+  if (sx.wi == 0 && sx.lane == 0) {
+    __threadfence();
+    const int64_t P = p.num_splits;
+    const int64_t c0 = part_of_row(pc.tok_vs, cx.total, P), c1 = part_of_row(pc.tok_vs + pc.kvlen - 1, cx.total, P);
+    const uint32_t arrived = atomicAdd(p.tok_cnt + pc.token, 1u) + 1u;
+    MergeList* ml = reinterpret_cast<MergeList*>(cx.g + LL::kOffMList);
+    if (arrived == static_cast<uint32_t>(c1 - c0 + 1) && ml->n < 2) {
+      ml->token[ml->n] = pc.token;
+      ml->c0[ml->n] = static_cast<int32_t>(c0);
+      ml->c1[ml->n] = static_cast<int32_t>(c1);
+      ++ml->n;
+    }
+  }
+  return true;
+}
+
+// The end-of-CTA merges, by all kThreads threads. Slots come into the stage
+// buffers in batches of up to kSlots by bulk copies (one round trip a batch);
+// each thread keeps an online (running max) merge of its float4 elements.
+template <class LL>
+__device__ void merge_listed(const Stage1Params& p, const Ctx<LL>& cx) {
+  constexpr int kThr = LL::kThreads;
+  constexpr int kSlotBytes = kHeads * kDv * 4;  // 32 KB
+  constexpr int kSlots = LL::kMergeBytes / kSlotBytes < 6 ? LL::kMergeBytes / kSlotBytes : 6;
+  constexpr int kF = (kHeads * kDv / 4 + kThr - 1) / kThr;  // float4 elements per thread
+  static_assert(kSlots >= 1, "merge buffers");
+  const MergeList* ml = reinterpret_cast<const MergeList*>(cx.g + LL::kOffMList);
+  const uint32_t nm = ml->n;
+  const float* lsebuf = reinterpret_cast<const float*>(cx.g + LL::kOffQ);
+  uint32_t batch = 0;
+  for (uint32_t e = 0; e < nm; ++e) {
+    const int token = ml->token[e];
+    const int64_t c0 = ml->c0[e], np = static_cast<int64_t>(ml->c1[e]) - c0 + 1;
+    float acc[kF][4], mrun[kF], wsum[kF];
+#pragma unroll
+    for (int i = 0; i < kF; ++i) {
+      mrun[i] = -INFINITY;
+      wsum[i] = 0.f;
+      acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = 0.f;
+    }
+    for (int64_t s0 = 0; s0 < np; s0 += kSlots) {
+      const int nb = static_cast<int>(np - s0 < kSlots ? np - s0 : static_cast<int64_t>(kSlots));
+      if (threadIdx.x == 0) {
+        asm volatile("fence.proxy.async.global;" ::: "memory");  // partials written through the generic proxy
+        mbar_arrive_expect_tx(cx.bar(LL::kMerge), nb * (kSlotBytes + kHeads * 4));
+        for (int j = 0; j < nb; ++j) {
+          const int64_t slot = c0 + s0 + j + token;
+          bulk_g2s(cx.s + LL::kOffKv + j * kSlotBytes, p.part_o + slot * kHeads * kDv, kSlotBytes, cx.bar(LL::kMerge),
+                   policy_evict_first());
+          bulk_g2s(cx.s + LL::kOffQ + j * kHeads * 4, p.part_lse + slot * kHeads, kHeads * 4, cx.bar(LL::kMerge),
+                   policy_evict_first());
+        }
+      }
+      // all threads agree before any of them moves on (a lone timeout must not
+      // leave the others at the barrier below)
+      if (!__syncthreads_and(cx.wait(LL::kMerge, batch & 1u) ? 1 : 0)) return;
+      ++batch;
+      const float4* obuf = reinterpret_cast<const float4*>(cx.g + LL::kOffKv);
+#pragma unroll
+      for (int i = 0; i < kF; ++i) {
+        const int f = threadIdx.x + i * kThr;
+        if (f < kHeads * kDv / 4) {
+          const int h = f >> 7;  // 128 float4 per head
+          for (int j = 0; j < nb; ++j) {
+            const float lse = lsebuf[j * kHeads + h];
+            const float mn = fmaxf(mrun[i], lse);
+            const float sc = fast_exp2(mrun[i] - mn), w = fast_exp2(lse - mn);
+            const float4 v = obuf[j * (kSlotBytes / 16) + f];
+            acc[i][0] = acc[i][0] * sc + w * v.x;
+            acc[i][1] = acc[i][1] * sc + w * v.y;
+            acc[i][2] = acc[i][2] * sc + w * v.z;
+            acc[i][3] = acc[i][3] * sc + w * v.w;
+            wsum[i] = wsum[i] * sc + w;
+            mrun[i] = mn;
+          }
+        }
+      }
+      __syncthreads();  // the buffers are free for the next batch
+    }
+    __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(p.out) + static_cast<int64_t>(token) * kHeads * kDv;
+#pragma unroll
+    for (int i = 0; i < kF; ++i) {
+      const int f = threadIdx.x + i * kThr;
+      if (f < kHeads * kDv / 4) {
+        const float inv = 1.0f / wsum[i];
+        *reinterpret_cast<uint2*>(dst + 4 * f) =
+            make_uint2(pack_bf16x2(acc[i][0] * inv, acc[i][1] * inv), pack_bf16x2(acc[i][2] * inv, acc[i][3] * inv));
+      }
+    }
+    if (threadIdx.x == 0) p.tok_cnt[token] = 0u;
+  }
+}
+
 // Barrier setup, the block's partition and tensor-memory allocation, common to
 // both kernels. Returns false (before any allocation) when the CTA has no work
 // or the indptrs are invalid.
@@ -304,7 +433,9 @@ __device__ __forceinline__ bool cta_begin(const Stage1Params& p, Ctx<LL>& cx, ui
   cx.flags = p.dev_flags;
   if (threadIdx.x == 0) {
     LL::init_barriers(cx);
+    mbar_init(cx.bar(LL::kMerge), 1);
     *cx.abort_word = 0u;
+    reinterpret_cast<MergeList*>(cx.g + LL::kOffMList)->n = 0u;
     fence_mbar_init();
   }
   const int64_t parts = p.num_splits, c = blockIdx.x;
@@ -316,6 +447,9 @@ __device__ __forceinline__ bool cta_begin(const Stage1Params& p, Ctx<LL>& cx, ui
     if (threadIdx.x == 0) atomicOr(p.dev_flags, kFlagBadIndptr);
     return false;
   }
+  if (blockIdx.x == 0 && threadIdx.x == 0) p.dev_flags[1] = static_cast<uint32_t>(p.total_q);  // counters in use
+  zero_empty_tokens<LL::kThreads>(p);
+  cx.total = loc.total;
   const int64_t x0 = part_start(c, loc.total, parts), x1 = part_start(c + 1, loc.total, parts);
   if (x0 >= x1 || loc.seg < 0) return false;  // uniform across the block
   if ((threadIdx.x >> 5) == alloc_warp) tmem_alloc(cx.s + LL::kOffSlot, kTmemCols);
@@ -328,13 +462,14 @@ __device__ __forceinline__ bool cta_begin(const Stage1Params& p, Ctx<LL>& cx, ui
 }
 
 template <class LL>
-__device__ __forceinline__ void cta_end(const Ctx<LL>& cx, int alloc_warp) {
+__device__ __forceinline__ void cta_end(const Stage1Params& p, const Ctx<LL>& cx, int alloc_warp) {
   tc_fence_before();
   __syncthreads();
   if ((threadIdx.x >> 5) == alloc_warp) {
     tc_fence_after();
     tmem_dealloc(cx.tmem, kTmemCols);
   }
+  if (!*cx.abort_word) merge_listed(p, cx);
 }
 
 }  // namespace tc

@@ -63,7 +63,11 @@ def test_planner_host_logic(lib):
 def test_workspace_size(lib):
     n = m.workspace_size(4, 4, 4096, m.BF16, num_splits=32)
     slots = 32 + 4
-    assert n == 256 + slots * 16 * 512 * 4 + slots * 16 * 4
+    # header, 4 token counters padded to 256 B, partial outputs, partial LSEs
+    assert n == 256 + 256 + slots * 16 * 512 * 4 + slots * 16 * 4
+    n = m.workspace_size(4, 65, 4096, m.BF16, num_splits=32)
+    slots = 32 + 65
+    assert n == 256 + 512 + slots * 16 * 512 * 4 + slots * 16 * 4
     with pytest.raises(m.MlaError):
         m.workspace_size(4, 4, 4096, m.BF16, num_splits=-2)
 

@@ -157,6 +157,30 @@ def test_deterministic_bitwise(kv_dtype):
     assert torch.equal(a, b)
 
 
+@pytest.mark.parametrize("kv_dtype", [synth.FP8_E4M3, synth.MXFP4])
+def test_workspace_reuse_across_shapes(kv_dtype):
+    # split tokens are merged by the CTA that finishes their last partial, through
+    # per-token counters in the workspace that every call leaves at zero
+    wa = synth.Workload("reuse_a", 3, 1, 0, synth.BF16, kv_dtype, seed=12)
+    wb = synth.Workload("reuse_b", 5, 1, 0, synth.BF16, kv_dtype, seed=13)
+    a = synth.make_inputs(wa, "cuda", kv_lens=[4000, 10, 2500])
+    b = synth.make_inputs(wb, "cuda", kv_lens=[300, 0, 5000, 129, 1000])
+    ws = m.alloc_workspace(5, 5, 20000, kv_dtype, num_splits=40)
+    outs = []
+    for inp in (a, b, a, b):
+        out = torch.empty((inp.total_q, 16, 512), dtype=torch.bfloat16, device="cuda")
+        m.decode(inp.q, inp.kv, inp.kv_scale, inp.qo_indptr, inp.kv_indptr, out, inp.kv_dtype, workspace=ws,
+                 num_splits=40)
+        outs.append(out)
+    torch.cuda.synchronize()
+    assert m.device_error(ws)[0] == m.MLA_OK
+    assert int(torch.count_nonzero(ws[256:512])) == 0  # counters back at zero
+    assert torch.equal(outs[0], outs[2]) and torch.equal(outs[1], outs[3])
+    assert torch.equal(outs[0], run_decode(a, num_splits=40))
+    assert torch.equal(outs[1], run_decode(b, num_splits=40))
+    assert torch.count_nonzero(outs[1][1]) == 0  # the empty segment's token
+
+
 def test_bad_indptr_sets_device_flag_and_skips_work():
     w = synth.Workload("bad", 3, 1, 0, synth.BF16, synth.FP8_E4M3, seed=8)
     inp = synth.make_inputs(w, "cuda", kv_lens=[100, 100, 100])
