@@ -1,7 +1,7 @@
 #!/usr/bin/env python
 """Benchmark: MLA decode µs/call and KV-read GB/s against the GB300 HBM roofline.
 
-One step = one full decode call (stage 1 + stage 2) over the batch of the
+One step = one full decode call over the batch of the
 headline workload: fp8 e4m3 KV cache (per-tensor scale), batch 256 x 1 query
 token, kv_len 8192 per sequence, bf16 queries -- 1.21 GB of KV streamed per
 call, larger than the 129 MB L2, so consecutive calls read HBM.
@@ -33,7 +33,8 @@ sys.path.insert(0, ROOT)
 
 HEADLINE = "fp8kv_bs256_kv8192"
 METRIC = "MLA decode µs/call and KV-read GB/s vs GB300 HBM peak, per (batch, kv_len, dtype)"
-STAGE1_SOURCES = ["mla_stage1_tc.cu", "mla_tcgen05.cuh", "mla_device.cuh", "mla_partition.cuh", "mla_internal.h"]
+STAGE1_SOURCES = ["mla_stage1_tc.cu", "mla_tc_common.cuh", "mla_tcgen05.cuh", "mla_device.cuh", "mla_partition.cuh",
+                  "mla_internal.h"]
 
 
 def _stage1_source_sha() -> str:
@@ -351,12 +352,30 @@ def measure_e2e(m, torch, inp, out, ws, splits, stream, K, world, device, kvb):
             "path": "mla_decode_from_host: q, KV cache, scales and indptrs H2D from pinned host memory, out D2H"}
 
 
+def _kernel_name(synth, w) -> str:
+    k = {synth.FP8_E4M3: "stage1_tc_kernel (tcgen05, e4m3 codes)", synth.MXFP4: "stage1_mx_kernel (tcgen05, e5m2 rebase)",
+         synth.BF16: "mla_stage1_kernel (warp MMA)"}[w.kv_dtype]
+    return k + f" <{synth.DTYPE_NAMES[w.kv_dtype]} KV, {synth.DTYPE_NAMES[w.q_dtype]} q>"
+
+
+def _dtype_desc(synth, w) -> str:
+    q = "bf16 q as exact hi+lo e4m3" if w.q_dtype == synth.BF16 else "e4m3 q codes"
+    return {synth.FP8_E4M3: f"e4m3 x e4m3 -> f32 (fp8 KV codes; {q})",
+            synth.MXFP4: f"e5m2 x e4m3 -> f32 (mxfp4 KV rebased to e5m2 per row; {q})",
+            synth.BF16: "bf16 x bf16 -> f32"}[w.kv_dtype]
+
+
+def _launches_per_call(synth, w) -> int:
+    # the tensor-core kernels merge split tokens themselves; bf16 KV adds the stage-2 launch
+    return 1 if w.kv_dtype in (synth.FP8_E4M3, synth.MXFP4) else 2
+
+
 def build_line(args, w, inp, kvb, splits, world, K, W, value, ms_step, achieved, peak, peak_kind, s1_avg_s,
                stage2_ms, clocks, e2e):
     from mla_decode_attention_split_gb300 import synth
     line = {"metric": METRIC, "value": round(value, 1), "unit": "GB/s", "n_gpus": world, "steps": K, "warmup": W,
             "ms_per_step": round(ms_step, 4), "us_per_call": round(ms_step * 1e3, 2), "higher_is_better": True,
-            "scaling": "weak", "vs_baseline": None, "dtype": "e4m3 x e4m3 -> f32 (fp8 KV codes; bf16 q as exact hi+lo e4m3)",
+            "scaling": "weak", "vs_baseline": None, "dtype": _dtype_desc(synth, w),
             "data": "synthetic (seeded N(0,1), quantised as the pages' harness does)",
             "config": {"workload": w.name, "batch": w.batch, "q_len": w.q_len, "kv_len": w.kv_len,
                        "q_dtype": synth.DTYPE_NAMES[w.q_dtype], "kv_dtype": synth.DTYPE_NAMES[w.kv_dtype],
@@ -366,16 +385,14 @@ def build_line(args, w, inp, kvb, splits, world, K, W, value, ms_step, achieved,
                        "parallelism": f"{world} independent replicas (weak scaling)"},
             "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                          "frac": round(achieved / peak, 4), "traffic": _ncu_traffic(w.name),
-                         "kernel": ("stage1_tc_kernel (tcgen05)" if w.kv_dtype == synth.FP8_E4M3 else
-                                    "mla_stage1_kernel (warp MMA)") + f" <{synth.DTYPE_NAMES[w.kv_dtype]} KV, "
-                                   f"{synth.DTYPE_NAMES[w.q_dtype]} q>",
+                         "kernel": _kernel_name(synth, w),
                          "algorithmic_bytes": f"{kvb} per launch = {kvb // inp.total_kv} B x {inp.total_kv} KV rows",
                          "peak_kind": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)",
                          "stage1_us": round(s1_avg_s * 1e6, 2),
                          "stage2_us": round(sum(stage2_ms) / K * 1e3, 2)},
             "clocks": {"sm_mhz": clocks["sm_mhz"], "sm_max_mhz": clocks["sm_max_mhz"], "reasons": clocks["reasons"],
                        "samples_in_timed_region": clocks["samples"]},
-            "gpu_launches": 2 * K,
+            "gpu_launches": _launches_per_call(synth, w) * K,
             "e2e": e2e}
     return line
 
