@@ -80,6 +80,43 @@ struct TileWalker {
   }
 };
 
+// Per-tile bookkeeping of the UMMA issuer, packed in one word: bit 0 = first
+// tile of its piece, bit 1 = last tile of its piece, bits 2.. = piece index
+// within the CTA.
+struct TileMeta {
+  uint32_t k;
+  bool first, last;
+  __device__ static TileMeta unpack(uint32_t w) { return TileMeta{w >> 2, (w & 1u) != 0, (w & 2u) != 0}; }
+};
+
+// The CTA's tiles in order, with their bookkeeping words.
+struct MetaTileWalker {
+  PieceCursor cur;
+  Piece pc;
+  int r0 = 0;
+  uint32_t k = 0;
+  bool have = false;
+  __device__ void init(const PieceCursor& c) {
+    cur = c;
+    have = cur.next(pc);
+    r0 = 0;
+    k = 0;
+  }
+  // First KV row and bookkeeping word of the next tile. Returns false when done.
+  __device__ bool next(int32_t& row, uint32_t& meta) {
+    if (!have) return false;
+    row = pc.kv_row + r0;
+    meta = (k << 2) | (r0 == 0 ? 1u : 0u) | (r0 + kTileRows >= pc.nrows ? 2u : 0u);
+    r0 += kTileRows;
+    if (r0 >= pc.nrows) {
+      have = cur.next(pc);
+      r0 = 0;
+      ++k;
+    }
+    return true;
+  }
+};
+
 __device__ __forceinline__ int count_tiles(PieceCursor cur) {
   Piece t;
   int n = 0;
