@@ -366,8 +366,8 @@ def _dtype_desc(synth, w) -> str:
 
 
 def _launches_per_call(synth, w) -> int:
-    # the tensor-core kernels merge split tokens themselves; bf16 KV adds the stage-2 launch
-    return 1 if w.kv_dtype in (synth.FP8_E4M3, synth.MXFP4) else 2
+    # stage 1 merges split tokens itself: one launch per call
+    return 1
 
 
 def build_line(args, w, inp, kvb, splits, world, K, W, value, ms_step, achieved, peak, peak_kind, s1_avg_s,

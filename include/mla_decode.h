@@ -18,8 +18,10 @@
  * flash decoding: the KV rows of all segments are partitioned evenly over
  * `num_splits` CTAs (stage 1: fused QK^T + online softmax + PV with fp8/mxfp4
  * dequantisation in the operand path), and per-split partial outputs are merged
- * with LSE weights (stage 2), as in kernelbot-amd-mixed-mla-753817
+ * with LSE weights (the pages' stage 2), as in kernelbot-amd-mixed-mla-753817
  * (module docstring, `mla_flash_decode_stage1`, `mla_flash_decode_stage2`).
+ * The merge runs inside the same launch: the CTA that finishes a token's last
+ * partial merges it, so one decode call is one kernel launch.
  *
  * Conventions for every entry point:
  *   - Pointers named d_* or documented "device" are CUDA device pointers that
@@ -87,8 +89,9 @@ typedef struct {
                              256-byte aligned, owned by the caller                 */
   size_t workspace_bytes;
   void* profile_events[3]; /* optional cudaEvent_t handles (NULL = none), recorded
-                              on `stream` before stage 1, between stage 1 and
-                              stage 2, and after stage 2 (kernel timing)          */
+                              on `stream` before and after the decode launch
+                              (events 1 and 2 are recorded back to back: the
+                              merge runs inside the launch)                      */
 } mla_decode_opts;
 
 /* Split planner (the pages choose the split count from batch size and KV

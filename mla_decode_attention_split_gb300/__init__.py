@@ -140,7 +140,7 @@ def make_opts(batch, total_q, total_kv, *, q_dtype=BF16, q_scale=None, sm_scale=
 def decode(q, kv, kv_scale, qo_indptr, kv_indptr, out, kv_dtype: int, *, workspace, q_dtype: int = BF16,
            q_scale=None, sm_scale: float = 0.0, num_splits: int = 0, stream=None, events=None) -> None:
     """mla_decode() on torch CUDA tensors (layouts as in mla_decode.h). Asynchronous.
-    events: optional three CUDA events recorded around stage 1 and stage 2."""
+    events: optional three CUDA events recorded before and after the launch (1 and 2 back to back)."""
     opts = make_opts(qo_indptr.numel() - 1, q.shape[0], kv.shape[0], q_dtype=q_dtype, q_scale=q_scale,
                      sm_scale=sm_scale, num_splits=num_splits, workspace=workspace, events=events)
     _check(lib().mla_decode(_ptr(q), _ptr(kv), _ptr(kv_scale), _ptr(qo_indptr), _ptr(kv_indptr), _ptr(out),

@@ -141,13 +141,14 @@ mla_status_t mla_decode(const void* q, const void* kv, const void* kv_scale, con
            cudaEventRecord(static_cast<cudaEvent_t>(opts->profile_events[i]), st) == cudaSuccess;
   };
   if (!mark(0)) return MLA_ERR_CUDA;
+  // one launch: stage 1 also merges split tokens and zeroes tokens of empty
+  // segments; with no KV rows at all every output row is zero
   if (total_kv > 0) {
     if (mla::launch_stage1(kv_dtype, opts->q_dtype, p, st) != cudaSuccess) return MLA_ERR_CUDA;
+  } else if (cudaMemsetAsync(out, 0, static_cast<size_t>(total_q) * mla::kHeads * mla::kDv * 2, st) != cudaSuccess) {
+    return MLA_ERR_CUDA;
   }
   if (!mark(1)) return MLA_ERR_CUDA;
-  // the tensor-core kernels merge split tokens and zero empty segments themselves
-  const bool merged = mla::stage1_merges(kv_dtype) && total_kv > 0;
-  if (!merged && mla::launch_stage2(p, st) != cudaSuccess) return MLA_ERR_CUDA;
   if (!mark(2)) return MLA_ERR_CUDA;
   return MLA_OK;
 }

@@ -1,77 +1,11 @@
-// Stage 2 of split-K MLA decode: merge the per-piece partial outputs of each
-// query token with LSE weights, as in kernelbot-amd-mixed-mla-753817
-// (`mla_flash_decode_stage2`: L = max_s lse_s, w_s = 2^(lse_s - L),
-// out = sum_s w_s O_s / sum_s w_s) with LSEs kept in the log2 domain.
-// Tokens written directly by stage 1 are skipped; tokens of a segment with no
-// KV rows get zeros.
-//
-// Also the dequantisation check kernel, which pushes KV rows through stage 1's
-// operand path (same byte layout, same MMA) against an identity operand.
+// The dequantisation check kernel: it pushes KV rows through stage 1's
+// operand path (same byte layout, same MMA) against an identity operand, so
+// the decode of the stored codes can be compared bit for bit.
 #include "mla_device.cuh"
 #include "mla_internal.h"
 #include "mla_partition.cuh"
 
 namespace mla {
-
-constexpr int kThreads2 = 256;
-
-__global__ void __launch_bounds__(kThreads2) mla_stage2_kernel(const Stage1Params p) {
-  __shared__ int64_t sh[16];
-  const int token = blockIdx.x;
-  const SegLocate loc = block_locate<kThreads2, 2>(
-      p.qo_indptr, p.kv_indptr, p.batch, p.total_q, p.total_kv, [](int64_t) { return int64_t(0); }, token, sh);
-  if (!loc.ok) {
-    if (threadIdx.x == 0) atomicOr(p.dev_flags, kFlagBadIndptr);
-    return;
-  }
-  if (loc.seg < 0) return;
-  const int b = loc.seg;
-  const int32_t q0 = __ldg(p.qo_indptr + b);
-  const int64_t kvlen = __ldg(p.kv_indptr + b + 1) - __ldg(p.kv_indptr + b);
-  const int h = threadIdx.x >> 4, d0 = (threadIdx.x & 15) * 32;
-  uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.out) +
-                                        (static_cast<int64_t>(token) * kHeads + h) * kDv + d0);
-  if (kvlen == 0) {
-#pragma unroll
-    for (int k = 0; k < 4; ++k) dst[k] = make_uint4(0u, 0u, 0u, 0u);
-    return;
-  }
-  const int64_t vs = loc.seg_vs + static_cast<int64_t>(token - q0) * kvlen;
-  const int64_t P = p.num_splits;
-  const int64_t c0 = part_of_row(vs, loc.total, P), c1 = part_of_row(vs + kvlen - 1, loc.total, P);
-  if (c0 == c1) return;  // stage 1 wrote this token directly
-  float L = -INFINITY;
-  for (int64_t c = c0; c <= c1; ++c) L = fmaxf(L, __ldg(p.part_lse + (c + token) * kHeads + h));
-  float acc[32];
-#pragma unroll
-  for (int i = 0; i < 32; ++i) acc[i] = 0.f;
-  float wsum = 0.f;
-  for (int64_t c = c0; c <= c1; ++c) {
-    const float wgt = fast_exp2(__ldg(p.part_lse + (c + token) * kHeads + h) - L);
-    wsum += wgt;
-    const float4* src = reinterpret_cast<const float4*>(p.part_o + ((c + token) * kHeads + h) * kDv + d0);
-#pragma unroll
-    for (int k = 0; k < 8; ++k) {
-      const float4 v = __ldg(src + k);
-      acc[4 * k] += wgt * v.x;
-      acc[4 * k + 1] += wgt * v.y;
-      acc[4 * k + 2] += wgt * v.z;
-      acc[4 * k + 3] += wgt * v.w;
-    }
-  }
-  const float inv = 1.0f / wsum;
-  uint32_t w[16];
-#pragma unroll
-  for (int k = 0; k < 16; ++k) w[k] = pack_bf16x2(acc[2 * k] * inv, acc[2 * k + 1] * inv);
-#pragma unroll
-  for (int k = 0; k < 4; ++k) dst[k] = make_uint4(w[4 * k], w[4 * k + 1], w[4 * k + 2], w[4 * k + 3]);
-}
-
-cudaError_t launch_stage2(const Stage1Params& p, cudaStream_t stream) {
-  if (p.total_q == 0) return cudaSuccess;
-  mla_stage2_kernel<<<p.total_q, kThreads2, 0, stream>>>(p);
-  return cudaGetLastError();
-}
 
 // ---------------------------------------------------------------------------
 // Dequantisation check. One warp per 8 KV rows; lane (g, t) takes row g and

@@ -35,7 +35,7 @@ struct Stage1Params {
   float* part_o;      // [slots][16][512]
   float* part_lse;    // [slots][16] (log2 domain)
   uint32_t* dev_flags;
-  uint32_t* tok_cnt;  // [total_q] partials finished per token (kernels that merge in stage 1)
+  uint32_t* tok_cnt;  // [total_q] partials finished per token
 };
 
 // KV formats / query formats as template tags (values match mla_dtype_t).
@@ -47,12 +47,10 @@ cudaError_t launch_stage1(int kv_fmt, int q_fmt, const Stage1Params& p, cudaStre
 cudaError_t launch_stage1_tc_fp8(int q_fmt, const Stage1Params& p, cudaStream_t stream);
 // mxfp4 KV on the tcgen05 tensor cores (mla_stage1_mx.cu)
 cudaError_t launch_stage1_tc_mxfp4(int q_fmt, const Stage1Params& p, cudaStream_t stream);
-cudaError_t launch_stage2(const Stage1Params& p, cudaStream_t stream);
 cudaError_t launch_dequant(const void* kv, const void* kv_scale, int kv_fmt, int32_t total_kv, int32_t row0,
                            int32_t nrows, float* out, cudaStream_t stream);
 bool stage1_supported(int kv_fmt, int q_fmt);
-// Stage 1 merges the partials itself (the tensor-core kernels); otherwise stage 2 runs.
-inline bool stage1_merges(int kv_fmt) { return kv_fmt == kKvFp8 || kv_fmt == kKvMxfp4; }
+
 
 inline size_t workspace_bytes_for(int64_t num_splits, int64_t total_q) {
   const int64_t slots = num_splits + total_q;

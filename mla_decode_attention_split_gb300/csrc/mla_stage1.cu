@@ -28,6 +28,7 @@
 //    transposed in registers with byte/halfword permutes.
 #include "mla_device.cuh"
 #include "mla_internal.h"
+#include "mla_merge.cuh"
 #include "mla_partition.cuh"
 
 namespace mla {
@@ -748,6 +749,8 @@ __global__ void __launch_bounds__(kThreads1, 1) mla_stage1_kernel(const Stage1Pa
     if (threadIdx.x == 0) atomicOr(p.dev_flags, kFlagBadIndptr);
     return;
   }
+  if (blockIdx.x == 0 && threadIdx.x == 0) p.dev_flags[1] = static_cast<uint32_t>(p.total_q);  // counters in use
+  zero_empty_tokens<kThreads1>(p);
   const int64_t x0 = part_start(c, loc.total, parts), x1 = part_start(c + 1, loc.total, parts);
   if (x0 >= x1 || loc.seg < 0) return;
   PieceCursor cur{p.qo_indptr, p.kv_indptr, p.batch, x0, x1, loc.seg, loc.seg_vs, c};
@@ -755,6 +758,9 @@ __global__ void __launch_bounds__(kThreads1, 1) mla_stage1_kernel(const Stage1Pa
     score_role<KV, QF>(p, cx, cur, warp, lane);
   else
     output_role<KV, QF>(p, cx, cur, warp - 4, lane);
+  // split tokens: the CTA that completes a token's partials merges it
+  __syncthreads();
+  if (!*cx.abort_word) merge_split_tokens_at_end<kThreads1>(p, cur, loc.total, sh);
 }
 
 template <int KV, int QF>
