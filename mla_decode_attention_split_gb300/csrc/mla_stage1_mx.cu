@@ -318,10 +318,11 @@ __device__ void converter_role(const Stage1Params& p, const Cx& cx, PieceCursor 
   uint8_t* sc_w = cx.g + L::kOffRawSc + warp * 32 * (kDqk / kMxBlock);
   MetaTileWalker rw;
   rw.init(cur);
-  MxRaw ra, rb;  // the even / odd tile in flight
-  uint32_t ma, mb;
+  // one tile ahead in registers (a second set measured slower: the register
+  // pressure slowed the conversion more than the earlier loads gained)
+  MxRaw ra;
+  uint32_t ma;
   load_mx_raw(p, rw, warp, lane, ra, ma);
-  load_mx_raw(p, rw, warp, lane, rb, mb);
   MX_PT_INIT
   for (uint32_t i = 0; i < ntiles; i += 2) {
     const bool two = i + 1 < ntiles;
@@ -331,7 +332,7 @@ __device__ void converter_role(const Stage1Params& p, const Cx& cx, PieceCursor 
     dump_raw(raw_w, sc_w, lane, ra);
     __syncwarp();
     const uint32_t m0 = ma;
-    load_mx_raw(p, rw, warp, lane, ra, ma);  // tile i + 2
+    load_mx_raw(p, rw, warp, lane, ra, ma);  // tile i + 1
     MX_PT(5);
     convert_tile(cx, i, warp, lane, raw_w, sc_w);
     MX_PT(0);
@@ -340,10 +341,10 @@ __device__ void converter_role(const Stage1Params& p, const Cx& cx, PieceCursor 
     if (!two) break;
     if (!wait_stage(cx, i + 1)) break;
     MX_PT(3);
-    dump_raw(raw_w, sc_w, lane, rb);
+    dump_raw(raw_w, sc_w, lane, ra);
     __syncwarp();
-    const uint32_t m1 = mb;
-    load_mx_raw(p, rw, warp, lane, rb, mb);  // tile i + 3
+    const uint32_t m1 = ma;
+    load_mx_raw(p, rw, warp, lane, ra, ma);  // tile i + 2
     MX_PT(5);
     convert_tile(cx, i + 1, warp, lane, raw_w, sc_w);
     MX_PT(0);
@@ -465,11 +466,28 @@ __device__ void softmax_role(const Stage1Params& p, const Cx& cx, PieceCursor cu
       if (!group_sync(cx, sx)) return;
       MX_PT(2);
       bool grew = false;
-      float alpha[16], alpha_o[16];
+      float alpha[16], alpha_o[16], tm[16], tz[16];
+      {
+        const float4* rm4 = reinterpret_cast<const float4*>(rm);  // [4 warps][16 heads]
+        const float4* rz4 = reinterpret_cast<const float4*>(rz);
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const float4 a = rm4[q], b4 = rm4[4 + q], c4 = rm4[8 + q], d = rm4[12 + q];
+          tm[4 * q] = fmaxf(fmaxf(a.x, b4.x), fmaxf(c4.x, d.x));
+          tm[4 * q + 1] = fmaxf(fmaxf(a.y, b4.y), fmaxf(c4.y, d.y));
+          tm[4 * q + 2] = fmaxf(fmaxf(a.z, b4.z), fmaxf(c4.z, d.z));
+          tm[4 * q + 3] = fmaxf(fmaxf(a.w, b4.w), fmaxf(c4.w, d.w));
+          const float4 e = rz4[q], f4 = rz4[4 + q], g4 = rz4[8 + q], k4 = rz4[12 + q];
+          tz[4 * q] = fmaxf(fmaxf(e.x, f4.x), fmaxf(g4.x, k4.x));
+          tz[4 * q + 1] = fmaxf(fmaxf(e.y, f4.y), fmaxf(g4.y, k4.y));
+          tz[4 * q + 2] = fmaxf(fmaxf(e.z, f4.z), fmaxf(g4.z, k4.z));
+          tz[4 * q + 3] = fmaxf(fmaxf(e.w, f4.w), fmaxf(g4.w, k4.w));
+        }
+      }
 #pragma unroll
       for (int h = 0; h < 16; ++h) {
-        const float mn = fmaxf(m[h], fmaxf(fmaxf(rm[h], rm[16 + h]), fmaxf(rm[32 + h], rm[48 + h])));
-        const float un = fmaxf(mu[h], fmaxf(fmaxf(rz[h], rz[16 + h]), fmaxf(rz[32 + h], rz[48 + h])));
+        const float mn = fmaxf(m[h], tm[h]);
+        const float un = fmaxf(mu[h], tz[h]);
         alpha[h] = fast_exp2(m[h] - mn);
         alpha_o[h] = fast_exp2(mu[h] - un);
         grew |= un > mu[h];
@@ -478,10 +496,7 @@ __device__ void softmax_role(const Stage1Params& p, const Cx& cx, PieceCursor cu
       }
       float pv[16];
 #pragma unroll
-      for (int h = 0; h < 16; ++h) {
-        l[h] = l[h] * alpha[h] + fast_exp2(x[h] - m[h]);
-        pv[h] = fast_exp2(z[h] - mu[h]) * kPScale;
-      }
+      for (int h = 0; h < 16; ++h) pv[h] = fast_exp2(z[h] - mu[h]) * kPScale;
       MX_PT(3);
       // P buffer b is free once the P.V of tile i - 2 is done
       if (i >= 2 && !cx.wait(L::kPvDone + b, ((i - 2) >> 1) & 1u)) return;
@@ -497,6 +512,9 @@ __device__ void softmax_role(const Stage1Params& p, const Cx& cx, PieceCursor cu
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(cx.bar(L::kPFull + b));
+      // the row sums, off the P handoff
+#pragma unroll
+      for (int h = 0; h < 16; ++h) l[h] = l[h] * alpha[h] + fast_exp2(x[h] - m[h]);
       MX_PT(5);
       ++i;
     }
