@@ -456,11 +456,12 @@ __device__ void softmax_role(const Stage1Params& p, const Cx& cx, PieceCursor cu
       }
       float* rm = red_max + b * 64;
       float* rz = red_mu + b * 64;
-      const float wm = warp_reduce16<true>(x, lane);
-      const float wz = warp_reduce16<true>(z, lane);
-      if ((lane & 1) == 0) {
-        rm[sx.wi * 16 + (lane >> 1)] = wm;
-        rz[sx.wi * 16 + (lane >> 1)] = wz;
+      {
+        float wm[16], wz[16];
+        warp_max16(x, wm);
+        warp_max16(z, wz);
+        store16(rm + sx.wi * 16, wm, lane);
+        store16(rz + sx.wi * 16, wz, lane);
       }
       MX_PT(1);
       if (!group_sync(cx, sx)) return;

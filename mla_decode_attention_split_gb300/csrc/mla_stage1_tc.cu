@@ -333,9 +333,12 @@ __device__ void softmax_role(const Stage1Params& p, const Cx& cx, PieceCursor cu
         const float v = (__uint_as_float(sr[h]) + __uint_as_float(sr[16 + h]) * (1.0f / kLoScale)) * c;
         x[h] = valid ? v : -INFINITY;
       }
-      const float wm = warp_reduce16<true>(x, lane);
       float* rm = red_max + (n & 1u) * 64;
-      if ((lane & 1) == 0) rm[sx.wi * 16 + (lane >> 1)] = wm;
+      {
+        float wm[16];
+        warp_max16(x, wm);
+        store16(rm + sx.wi * 16, wm, lane);
+      }
       TC_PT(1);
       if (!group_sync(cx, sx)) return;
       TC_PT(2);

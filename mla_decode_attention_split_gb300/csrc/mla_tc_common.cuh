@@ -162,6 +162,23 @@ __device__ __forceinline__ float warp_reduce16(const float (&v)[16], int lane) {
   return kMax ? fmaxf(d, r1) : d + r1;
 }
 
+// Max of each of 16 per-head values over the 32 lanes of a warp (every lane
+// gets all 16): 16 independent warp reductions (redux.sync, sm_100 family).
+// NaN inputs are ignored, as fmaxf does.
+__device__ __forceinline__ void warp_max16(const float (&v)[16], float (&r)[16]) {
+#pragma unroll
+  for (int h = 0; h < 16; ++h) asm volatile("redux.sync.max.f32 %0, %1, 0xffffffff;" : "=f"(r[h]) : "f"(v[h]));
+}
+
+// Lane 0 stores 16 per-head values of the warp as 4 x 16 bytes (16-byte aligned dst).
+__device__ __forceinline__ void store16(float* dst, const float (&r)[16], int lane) {
+  if (lane == 0) {
+    float4* d = reinterpret_cast<float4*>(dst);
+#pragma unroll
+    for (int q = 0; q < 4; ++q) d[q] = make_float4(r[4 * q], r[4 * q + 1], r[4 * q + 2], r[4 * q + 3]);
+  }
+}
+
 // The 4 softmax warps: thread = tile row = tensor-memory lane.
 struct SoftmaxCtx {
   int row, wi, lane;
