@@ -157,9 +157,13 @@ def workload_by_name(synth, name):
     return synth.Workload(name, int(bs[2:]), 1, int(kvl[2:]), synth.BF16, kv_dtype)
 
 
-def time_workload(m, synth, torch, name, steps, warmup, flush_l2: bool):
-    """Per-call device time of one workload (stage-1 and total), median over steps."""
-    inp = synth.make_inputs(synth.WORKLOADS[name], "cuda")
+def time_workload(m, synth, torch, name, steps, warmup, flush_l2: bool, quantize_q: bool = False):
+    """Per-call device time of one workload (stage-1 and total), median over steps.
+    quantize_q: pass bf16 q and let the call quantise it (the pages' a8w8 flow)."""
+    w = synth.WORKLOADS[name]
+    if quantize_q:
+        w = synth.Workload(w.name, w.batch, w.q_len, w.kv_len, synth.BF16, w.kv_dtype, w.ragged_max, w.seed)
+    inp = synth.make_inputs(w, "cuda")
     out = torch.empty((inp.total_q, 16, 512), dtype=torch.bfloat16, device="cuda")
     ws = m.alloc_workspace(inp.batch, inp.total_q, inp.total_kv, inp.kv_dtype)
     flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device="cuda") if flush_l2 else None
@@ -169,7 +173,7 @@ def time_workload(m, synth, torch, name, steps, warmup, flush_l2: bool):
         if flush is not None:
             flush.fill_(i & 0xFF)
         m.decode(inp.q, inp.kv, inp.kv_scale, inp.qo_indptr, inp.kv_indptr, out, inp.kv_dtype, workspace=ws,
-                 q_dtype=inp.q_dtype, q_scale=inp.q_scale, events=ev)
+                 q_dtype=inp.q_dtype, q_scale=inp.q_scale, events=ev, quantize_q=quantize_q)
         torch.cuda.synchronize()
         if i >= warmup:
             tot.append(m.elapsed_ms(ev[0], ev[2]) * 1e3)
@@ -407,6 +411,10 @@ def finish(args, line, rank, world, w, m, synth, torch, inp):
                                    "warm": time_workload(m, synth, torch, name, 30, 5, False)}
                 except m.MlaError as e:
                     table[name] = {"unsupported": str(e)}
+            # the a8w8 workload with q quantised inside the call (one extra small launch)
+            qq = "a8w8_bs64_kv1024+in_call_q_quantisation"
+            table[qq] = {"cold": time_workload(m, synth, torch, "a8w8_bs64_kv1024", 30, 5, True, quantize_q=True),
+                         "warm": time_workload(m, synth, torch, "a8w8_bs64_kv1024", 30, 5, False, quantize_q=True)}
             line["workloads"] = table
         if not args.no_cpu_baseline:
             import oracle

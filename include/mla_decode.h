@@ -92,6 +92,16 @@ typedef struct {
                               on `stream` before and after the decode launch
                               (events 1 and 2 are recorded back to back: the
                               merge runs inside the launch)                      */
+  int32_t quantize_q;     /* nonzero: quantise bf16 q to e4m3 inside the call and
+                             run the a8w8 path, as the pages do before calling
+                             their a8w8 kernel (kernelbot-amd-mixed-mla-753817,
+                             `_quantize_fp8`): one per-tensor scale
+                             s = max(amax|q|, 1e-12) / 448 and codes
+                             RNE(q / s) saturated to +-448, all in fp32. Needs
+                             q_dtype == MLA_DTYPE_BF16 and an fp8 KV cache
+                             (else MLA_ERR_UNSUPPORTED); adds one small launch
+                             (the amax). The scale is kept in the workspace
+                             header.                                            */
 } mla_decode_opts;
 
 /* Split planner (the pages choose the split count from batch size and KV

@@ -37,7 +37,7 @@ class DecodeOpts(ctypes.Structure):
     _fields_ = [("batch", ctypes.c_int32), ("total_q", ctypes.c_int32), ("total_kv", ctypes.c_int32),
                 ("sm_scale", ctypes.c_float), ("q_dtype", ctypes.c_int), ("q_scale", ctypes.c_void_p),
                 ("num_splits", ctypes.c_int32), ("workspace", ctypes.c_void_p), ("workspace_bytes", ctypes.c_size_t),
-                ("profile_events", ctypes.c_void_p * 3)]
+                ("profile_events", ctypes.c_void_p * 3), ("quantize_q", ctypes.c_int32)]
 
 
 class DeviceBuffers(ctypes.Structure):
@@ -124,11 +124,12 @@ def alloc_workspace(batch: int, total_q: int, total_kv: int, kv_dtype: int, num_
 
 
 def make_opts(batch, total_q, total_kv, *, q_dtype=BF16, q_scale=None, sm_scale=0.0, num_splits=0,
-              workspace=None, events=None) -> DecodeOpts:
+              workspace=None, events=None, quantize_q=False) -> DecodeOpts:
     o = DecodeOpts(batch=batch, total_q=total_q, total_kv=total_kv, sm_scale=float(sm_scale), q_dtype=q_dtype,
                    q_scale=None if q_scale is None else q_scale.data_ptr(), num_splits=num_splits,
                    workspace=None if workspace is None else workspace.data_ptr(),
-                   workspace_bytes=0 if workspace is None else workspace.numel() * workspace.element_size())
+                   workspace_bytes=0 if workspace is None else workspace.numel() * workspace.element_size(),
+                   quantize_q=1 if quantize_q else 0)
     if events is not None:  # three torch.cuda.Event(enable_timing=True)
         for i, ev in enumerate(events):
             if ev is not None and not ev.cuda_event:
@@ -138,11 +139,14 @@ def make_opts(batch, total_q, total_kv, *, q_dtype=BF16, q_scale=None, sm_scale=
 
 
 def decode(q, kv, kv_scale, qo_indptr, kv_indptr, out, kv_dtype: int, *, workspace, q_dtype: int = BF16,
-           q_scale=None, sm_scale: float = 0.0, num_splits: int = 0, stream=None, events=None) -> None:
+           q_scale=None, sm_scale: float = 0.0, num_splits: int = 0, stream=None, events=None,
+           quantize_q: bool = False) -> None:
     """mla_decode() on torch CUDA tensors (layouts as in mla_decode.h). Asynchronous.
-    events: optional three CUDA events recorded before and after the launch (1 and 2 back to back)."""
+    events: optional three CUDA events recorded before and after the launch (1 and 2 back to back).
+    quantize_q: quantise bf16 q to e4m3 per tensor inside the call (the a8w8 mode; fp8 KV only)."""
     opts = make_opts(qo_indptr.numel() - 1, q.shape[0], kv.shape[0], q_dtype=q_dtype, q_scale=q_scale,
-                     sm_scale=sm_scale, num_splits=num_splits, workspace=workspace, events=events)
+                     sm_scale=sm_scale, num_splits=num_splits, workspace=workspace, events=events,
+                     quantize_q=quantize_q)
     _check(lib().mla_decode(_ptr(q), _ptr(kv), _ptr(kv_scale), _ptr(qo_indptr), _ptr(kv_indptr), _ptr(out),
                             kv_dtype, ctypes.byref(opts), _stream_handle(stream)), "mla_decode")
 

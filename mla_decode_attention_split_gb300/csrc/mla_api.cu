@@ -106,7 +106,9 @@ mla_status_t mla_decode(const void* q, const void* kv, const void* kv_scale, con
   if (kv_dtype != MLA_DTYPE_BF16 && !kv_scale) return MLA_ERR_INVALID_ARG;
   if (kv_dtype == MLA_DTYPE_MXFP4 && (reinterpret_cast<uintptr_t>(kv_scale) & 1u) != 0) return MLA_ERR_INVALID_ARG;
   if (opts->q_dtype == MLA_DTYPE_FP8_E4M3 && !opts->q_scale) return MLA_ERR_INVALID_ARG;
-  if (!mla::stage1_supported(kv_dtype, opts->q_dtype)) return MLA_ERR_UNSUPPORTED;
+  if (opts->quantize_q && opts->q_dtype != MLA_DTYPE_BF16) return MLA_ERR_UNSUPPORTED;
+  const int q_fmt = opts->quantize_q ? static_cast<int>(mla::kQBf16Quant) : static_cast<int>(opts->q_dtype);
+  if (!mla::stage1_supported(kv_dtype, q_fmt)) return MLA_ERR_UNSUPPORTED;
   int32_t splits = opts->num_splits;
   if (splits < 0 || splits > kMaxSplits) return MLA_ERR_INVALID_ARG;
   if (splits == 0) splits = plan_splits(total_q, batch, total_kv, sm_count_of_current_device());
@@ -120,7 +122,8 @@ mla_status_t mla_decode(const void* q, const void* kv, const void* kv_scale, con
   p.q = q;
   p.kv = kv;
   p.kv_scale = kv_scale;
-  p.q_scale = opts->q_scale;
+  p.q_scale = opts->quantize_q ? reinterpret_cast<const float*>(static_cast<uint32_t*>(opts->workspace) + mla::kHdrQScale)
+                               : opts->q_scale;
   p.qo_indptr = qo_indptr;
   p.kv_indptr = kv_indptr;
   p.batch = batch;
@@ -144,7 +147,10 @@ mla_status_t mla_decode(const void* q, const void* kv, const void* kv_scale, con
   // one launch: stage 1 also merges split tokens and zeroes tokens of empty
   // segments; with no KV rows at all every output row is zero
   if (total_kv > 0) {
-    if (mla::launch_stage1(kv_dtype, opts->q_dtype, p, st) != cudaSuccess) return MLA_ERR_CUDA;
+    if (opts->quantize_q &&
+        mla::launch_q_scale(q, static_cast<int64_t>(total_q) * mla::kHeads * mla::kDqk, p.dev_flags, st) != cudaSuccess)
+      return MLA_ERR_CUDA;
+    if (mla::launch_stage1(kv_dtype, q_fmt, p, st) != cudaSuccess) return MLA_ERR_CUDA;
   } else if (cudaMemsetAsync(out, 0, static_cast<size_t>(total_q) * mla::kHeads * mla::kDv * 2, st) != cudaSuccess) {
     return MLA_ERR_CUDA;
   }

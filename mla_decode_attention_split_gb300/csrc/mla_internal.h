@@ -40,7 +40,10 @@ struct Stage1Params {
 
 // KV formats / query formats as template tags (values match mla_dtype_t).
 enum KvFormat : int { kKvBf16 = 0, kKvFp8 = 1, kKvMxfp4 = 2 };
-enum QFormat : int { kQBf16 = 0, kQFp8 = 1 };
+enum QFormat : int { kQBf16 = 0, kQFp8 = 1, kQBf16Quant = 2 /* bf16 q quantised to e4m3 in setup */ };
+
+// Header words of the workspace.
+enum HeaderWord : int { kHdrFlags = 0, kHdrCounters = 1, kHdrQAmax = 2, kHdrQScale = 3, kHdrQBlocks = 4 };
 
 cudaError_t launch_stage1(int kv_fmt, int q_fmt, const Stage1Params& p, cudaStream_t stream);
 // fp8 KV on the tcgen05 tensor cores (mla_stage1_tc.cu)
@@ -50,6 +53,8 @@ cudaError_t launch_stage1_tc_mxfp4(int q_fmt, const Stage1Params& p, cudaStream_
 cudaError_t launch_dequant(const void* kv, const void* kv_scale, int kv_fmt, int32_t total_kv, int32_t row0,
                            int32_t nrows, float* out, cudaStream_t stream);
 bool stage1_supported(int kv_fmt, int q_fmt);
+// amax of bf16 q over n elements -> header word kHdrQScale = max(amax, 1e-12) / 448 (mla_qquant.cu)
+cudaError_t launch_q_scale(const void* q, int64_t n, uint32_t* header, cudaStream_t stream);
 
 
 inline size_t workspace_bytes_for(int64_t num_splits, int64_t total_q) {

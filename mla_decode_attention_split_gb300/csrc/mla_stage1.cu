@@ -794,6 +794,7 @@ extern "C" int mla_debug_phase_cycles(unsigned long long* host, int n, int reset
 #endif
 
 bool stage1_supported(int kv_fmt, int q_fmt) {
+  if (q_fmt == kQBf16Quant) return kv_fmt == kKvFp8;  // the in-call a8w8 mode
   return (kv_fmt == kKvFp8 || kv_fmt == kKvBf16 || kv_fmt == kKvMxfp4) && (q_fmt == kQBf16 || q_fmt == kQFp8);
 }
 

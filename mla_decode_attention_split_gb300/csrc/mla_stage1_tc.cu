@@ -498,6 +498,7 @@ static cudaError_t launch_q(const Stage1Params& p, cudaStream_t stream) {
 }  // namespace tc
 
 cudaError_t launch_stage1_tc_fp8(int q_fmt, const Stage1Params& p, cudaStream_t stream) {
+  if (q_fmt == kQBf16Quant) return tc::launch_q<kQBf16Quant>(p, stream);
   return q_fmt == kQBf16 ? tc::launch_q<kQBf16>(p, stream) : tc::launch_q<kQFp8>(p, stream);
 }
 

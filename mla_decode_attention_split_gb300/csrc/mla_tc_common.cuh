@@ -212,7 +212,28 @@ __device__ float setup_q(const Stage1Params& p, const Ctx<LL>& cx, SoftmaxCtx& s
                                        ((unit ^ (row & 7)) << 4) + (d & 15));
   };
   float c;
-  if (QF == kQBf16) {
+  if (QF == kQBf16Quant) {
+    // e4m3 codes of q / s (RNE, saturated), lo rows zero; s from the workspace
+    const uint16_t* src = static_cast<const uint16_t*>(p.q) + (static_cast<int64_t>(token) * kHeads + h) * kDqk + d0;
+    const float qs = __ldg(p.q_scale);
+#pragma unroll
+    for (int i = 0; i < 9; ++i) {
+      const uint4 v = __ldg(reinterpret_cast<const uint4*>(src) + i);
+      const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+      uint32_t code[2];
+#pragma unroll
+      for (int k = 0; k < 2; ++k) {
+        const float a = bf16_bits_to_f32(w[2 * k] & 0xFFFFu) / qs, b = bf16_bits_to_f32(w[2 * k] >> 16) / qs;
+        const float e = bf16_bits_to_f32(w[2 * k + 1] & 0xFFFFu) / qs, f = bf16_bits_to_f32(w[2 * k + 1] >> 16) / qs;
+        code[k] = f32x2_to_e4m3x2(a, b) | (f32x2_to_e4m3x2(e, f) << 16);
+      }
+      *qaddr(h, d0 + 8 * i) = code[0];
+      *qaddr(h, d0 + 8 * i + 4) = code[1];
+      *qaddr(16 + h, d0 + 8 * i) = 0u;
+      *qaddr(16 + h, d0 + 8 * i + 4) = 0u;
+    }
+    c = p.sm_scale * kLog2e * kvsc * qs;
+  } else if (QF == kQBf16) {
     const uint16_t* src = static_cast<const uint16_t*>(p.q) + (static_cast<int64_t>(token) * kHeads + h) * kDqk + d0;
     uint32_t w[36];
 #pragma unroll

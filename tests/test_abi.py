@@ -96,6 +96,17 @@ def test_argument_checks_fail_before_any_device_work(lib):
     st = L.mla_decode(ctypes.c_void_p(aligned), ctypes.c_void_p(aligned), None, ctypes.c_void_p(aligned),
                       ctypes.c_void_p(aligned), ctypes.c_void_p(aligned), m.BF16, ctypes.byref(opts), None)
     assert st == m.MLA_ERR_INVALID_ARG
+    # in-call q quantisation: bf16 q and fp8 KV only
+    opts.q_dtype, opts.quantize_q = m.FP8_E4M3, 1
+    st = L.mla_decode(ctypes.c_void_p(aligned), ctypes.c_void_p(aligned), ctypes.c_void_p(aligned),
+                      ctypes.c_void_p(aligned), ctypes.c_void_p(aligned), ctypes.c_void_p(aligned), m.FP8_E4M3,
+                      ctypes.byref(opts), None)
+    assert st in (m.MLA_ERR_UNSUPPORTED, m.MLA_ERR_INVALID_ARG)
+    opts.q_dtype = m.BF16
+    st = L.mla_decode(ctypes.c_void_p(aligned), ctypes.c_void_p(aligned), None, ctypes.c_void_p(aligned),
+                      ctypes.c_void_p(aligned), ctypes.c_void_p(aligned), m.BF16, ctypes.byref(opts), None)
+    assert st == m.MLA_ERR_UNSUPPORTED
+    opts.quantize_q = 0
     # missing workspace
     opts.q_dtype = m.BF16
     st = L.mla_decode(ctypes.c_void_p(aligned), ctypes.c_void_p(aligned), None, ctypes.c_void_p(aligned),

@@ -181,6 +181,32 @@ def test_workspace_reuse_across_shapes(kv_dtype):
     assert torch.count_nonzero(outs[1][1]) == 0  # the empty segment's token
 
 
+def test_in_call_q_quantisation_equals_caller_quantised_a8w8():
+    # quantize_q: the library computes the per-tensor scale and the e4m3 codes of the
+    # bf16 q itself; the result must equal the a8w8 path fed with the same codes
+    w = synth.Workload("qquant", 4, 1, 0, synth.BF16, synth.FP8_E4M3, seed=41)
+    inp = synth.make_inputs(w, "cuda", kv_lens=[500, 1300, 64, 2000])
+    # the rule in fp32 with IEEE division (fp64 then rounded to fp32 gives the
+    # correctly rounded fp32 quotient); the e4m3 cast rounds to nearest even
+    qd = inp.q.float().cpu().double()
+    scale = (torch.clamp(qd.abs().max(), min=1e-12) / 448.0).float().reshape(1)
+    codes = (qd / scale.double()).float().clamp(-448.0, 448.0).to(torch.float8_e4m3fn).view(torch.uint8).cuda()
+    scale = scale.cuda()
+    ref = run_decode(dataclasses.replace(inp, q=codes, q_scale=scale, q_dtype=synth.FP8_E4M3), num_splits=9)
+    ws = m.alloc_workspace(inp.batch, inp.total_q, inp.total_kv, inp.kv_dtype, num_splits=9)
+    for _ in range(2):  # the amax scratch in the header is left clean for the next call
+        out = torch.empty_like(ref)
+        m.decode(inp.q, inp.kv, inp.kv_scale, inp.qo_indptr, inp.kv_indptr, out, inp.kv_dtype, workspace=ws,
+                 num_splits=9, quantize_q=True)
+        torch.cuda.synchronize()
+        assert m.device_error(ws)[0] == m.MLA_OK
+        assert torch.equal(out, ref)
+    hdr = ws[:32].view(torch.int32).cpu()
+    assert int(hdr[2]) == 0 and int(hdr[4]) == 0
+    assert abs(float(ws[12:16].view(torch.float32).cpu()[0]) - float(scale.cpu()[0])) == 0.0
+    check(ref.float().cpu().numpy(), oracle_ref(dataclasses.replace(inp, q=codes, q_scale=scale, q_dtype=synth.FP8_E4M3)))
+
+
 def test_bad_indptr_sets_device_flag_and_skips_work():
     w = synth.Workload("bad", 3, 1, 0, synth.BF16, synth.FP8_E4M3, seed=8)
     inp = synth.make_inputs(w, "cuda", kv_lens=[100, 100, 100])
