@@ -187,6 +187,34 @@ def time_workload(m, synth, torch, name, steps, warmup, flush_l2: bool, quantize
             "l2": "flushed (256 MB write) before each call" if flush_l2 else "back-to-back"}
 
 
+def time_paged_workload(m, synth, torch, name, page_size, steps, warmup, flush_l2: bool):
+    """Per-call device time of a workload with its fp8 cache in pages of `page_size` rows,
+    scattered over the pool in random order (the page table built once, outside the timing)."""
+    w = synth.WORKLOADS[name]
+    pin = synth.make_paged_inputs(w, "cuda", kv_lens=synth.make_lengths(w), page_size=page_size)
+    out = torch.empty((pin.total_q, 16, 512), dtype=torch.bfloat16, device="cuda")
+    ws = m.alloc_paged_workspace(pin.batch, pin.total_q, pin.total_kv, synth.FP8_E4M3)
+    flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device="cuda") if flush_l2 else None
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
+    tot = []
+    for i in range(warmup + steps):
+        if flush is not None:
+            flush.fill_(i & 0xFF)
+        m.decode_paged(pin.q, pin.kv_pages, pin.kv_scale, pin.qo_indptr, pin.page_indptr, pin.page_indices,
+                       pin.last_page_len, page_size, out, synth.FP8_E4M3, total_kv=pin.total_kv, workspace=ws,
+                       q_dtype=pin.q_dtype, q_scale=pin.q_scale, events=ev)
+        torch.cuda.synchronize()
+        if i >= warmup:
+            tot.append(m.elapsed_ms(ev[0], ev[2]) * 1e3)
+    st, flags = m.device_error(ws)
+    assert st == m.MLA_OK, (name, page_size, flags)
+    us = statistics.median(tot)
+    kvb = pin.total_kv * synth.D_QK  # the rows read (the pool's spare pages are not)
+    return {"us_per_call": round(us, 2), "kv_gbs": round(kvb / (us * 1e-6) / 1e9, 1), "kv_bytes": kvb,
+            "page_size": page_size, "pages": pin.num_pages,
+            "l2": "flushed (256 MB write) before each call" if flush_l2 else "back-to-back"}
+
+
 def cpu_baseline(inp, synth, oracle, target_s=15.0):
     """The oracle as it stands, single-threaded, on a bounded sample of segments
     (all 16 heads each); throughput in KV-read GB/s of the sampled segments."""
@@ -415,6 +443,11 @@ def finish(args, line, rank, world, w, m, synth, torch, inp):
             qq = "a8w8_bs64_kv1024+in_call_q_quantisation"
             table[qq] = {"cold": time_workload(m, synth, torch, "a8w8_bs64_kv1024", 30, 5, True, quantize_q=True),
                          "warm": time_workload(m, synth, torch, "a8w8_bs64_kv1024", 30, 5, False, quantize_q=True)}
+            # the headline shape with the cache in pages scattered over a pool
+            for ps in (1, 16, 64):
+                key = f"fp8kv_bs256_kv8192+paged_ps{ps}"
+                table[key] = {"cold": time_paged_workload(m, synth, torch, "fp8kv_bs256_kv8192", ps, 30, 5, True),
+                              "warm": time_paged_workload(m, synth, torch, "fp8kv_bs256_kv8192", ps, 30, 5, False)}
             line["workloads"] = table
         if not args.no_cpu_baseline:
             import oracle

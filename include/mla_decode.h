@@ -75,6 +75,7 @@ typedef enum {
 /* Device error flags, as returned by mla_get_device_error().                  */
 #define MLA_DEVFLAG_TIMEOUT 0x1u
 #define MLA_DEVFLAG_BAD_INDPTR 0x2u
+#define MLA_DEVFLAG_BAD_PAGE 0x4u  /* mla_decode_paged: a page id >= num_pages */
 
 typedef struct {
   int32_t batch;          /* number of segments = len(qo_indptr) - 1, >= 1         */
@@ -149,6 +150,48 @@ mla_status_t mla_decode_workspace_size(int32_t batch, int32_t total_q, int32_t t
 mla_status_t mla_decode(const void* q, const void* kv, const void* kv_scale,
                         const int32_t* qo_indptr, const int32_t* kv_indptr, void* out,
                         mla_dtype_t kv_dtype, const mla_decode_opts* opts, void* stream);
+
+/* Paged KV cache: the page-table form of kernelbot-amd-mixed-mla-753817, which
+ * hands `kv_indices`, `kv_last_page_len` and `page_size` (1 there) to the
+ * vendor a8w8 decode. Segment b owns page-table entries
+ * [page_indptr[b], page_indptr[b+1]); its KV row i is row i % page_size of
+ * page page_indices[page_indptr[b] + i / page_size]. A segment with n_b > 0
+ * pages has (n_b - 1) * page_size + last_page_len[b] rows; with
+ * page_size == 1 it has n_b rows and last_page_len is not read (the pages pass
+ * the segment lengths there, which only that reading accepts). All arrays are
+ * device int32 and caller-owned.                                              */
+typedef struct {
+  const int32_t* page_indptr;   /* [batch+1], monotone, page_indptr[0] = 0       */
+  const int32_t* page_indices;  /* [page_indptr[batch]] page ids in [0, num_pages) */
+  const int32_t* last_page_len; /* [batch], each in [1, page_size]; may be NULL
+                                   when page_size == 1                           */
+  int32_t page_size;            /* KV rows per page, >= 1                        */
+  int32_t num_pages;            /* pages in the pool kv_pages points to          */
+} mla_paged_kv;
+
+/* Workspace bytes for mla_decode_paged(): mla_decode_workspace_size() plus
+ * room for the logical row offsets of the segments (batch+1 int32, padded to
+ * 256 bytes). total_kv is the logical row count (the sum of the segment
+ * lengths). Host only. Errors as mla_decode_workspace_size().                 */
+mla_status_t mla_decode_paged_workspace_size(int32_t batch, int32_t total_q, int32_t total_kv,
+                                             mla_dtype_t kv_dtype, int32_t num_splits, size_t* bytes);
+
+/* The decode over a paged KV cache (fp8 e4m3 only; other KV dtypes return
+ * MLA_ERR_UNSUPPORTED). Arguments as mla_decode(), except:
+ *   kv_pages  device, [num_pages][page_size][576] e4m3 codes, 16-byte aligned
+ *   paged     the page table (above), host struct of device pointers
+ *   opts->total_kv  the logical KV row count, sum of the segment lengths
+ * One extra small launch builds the logical row offsets from the page table
+ * into the workspace. If page_indptr is not monotone from 0, a last-page
+ * length is outside [1, page_size], or the lengths do not sum to
+ * opts->total_kv, no KV row is read and MLA_DEVFLAG_BAD_INDPTR is set. A page
+ * id outside [0, num_pages) sets MLA_DEVFLAG_BAD_PAGE; that row is not read
+ * and the output of its token is unspecified. Results are bitwise those of
+ * mla_decode() on the same rows laid out contiguously with the same
+ * num_splits. Errors as mla_decode(). Asynchronous on `stream`.              */
+mla_status_t mla_decode_paged(const void* q, const void* kv_pages, const void* kv_scale,
+                              const int32_t* qo_indptr, const mla_paged_kv* paged, void* out,
+                              mla_dtype_t kv_dtype, const mla_decode_opts* opts, void* stream);
 
 /* Device buffers (caller-owned) that mla_decode_from_host() stages into.      */
 typedef struct {

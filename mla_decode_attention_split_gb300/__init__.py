@@ -22,7 +22,8 @@ DEVFLAG_TIMEOUT, DEVFLAG_BAD_INDPTR = 0x1, 0x2
 
 EXPORTED = ("mla_plan", "mla_decode_workspace_size", "mla_decode", "mla_decode_from_host", "mla_dequant_rows",
             "mla_get_device_error", "mla_reset_device_error", "mla_event_elapsed_ms", "mla_decode_static_workspace",
-            "mla_status_string")
+            "mla_decode_paged_workspace_size", "mla_decode_paged", "mla_status_string")
+DEVFLAG_BAD_PAGE = 0x4
 MLA_ERR_TOO_LARGE = 7
 STATIC_WORKSPACE_BYTES = 16 * 1024 * 1024
 
@@ -44,6 +45,11 @@ class DeviceBuffers(ctypes.Structure):
     _fields_ = [("q", ctypes.c_void_p), ("kv", ctypes.c_void_p), ("kv_scale", ctypes.c_void_p),
                 ("q_scale", ctypes.c_void_p), ("qo_indptr", ctypes.c_void_p), ("kv_indptr", ctypes.c_void_p),
                 ("out", ctypes.c_void_p)]
+
+
+class PagedKV(ctypes.Structure):
+    _fields_ = [("page_indptr", ctypes.c_void_p), ("page_indices", ctypes.c_void_p),
+                ("last_page_len", ctypes.c_void_p), ("page_size", ctypes.c_int32), ("num_pages", ctypes.c_int32)]
 
 
 _lock = threading.Lock()
@@ -74,6 +80,8 @@ def lib():
             L.mla_reset_device_error.argtypes = [P, P]
             L.mla_event_elapsed_ms.argtypes = [P, P, ctypes.POINTER(ctypes.c_float)]
             L.mla_decode_static_workspace.argtypes = [P, P, P, P, P, P, st, ctypes.POINTER(DecodeOpts), P]
+            L.mla_decode_paged_workspace_size.argtypes = [i32, i32, i32, st, i32, ctypes.POINTER(ctypes.c_size_t)]
+            L.mla_decode_paged.argtypes = [P, P, P, P, ctypes.POINTER(PagedKV), P, st, ctypes.POINTER(DecodeOpts), P]
             L.mla_status_string.argtypes = [st]
             L.mla_status_string.restype = ctypes.c_char_p
             for name in EXPORTED[:-1]:
@@ -149,6 +157,39 @@ def decode(q, kv, kv_scale, qo_indptr, kv_indptr, out, kv_dtype: int, *, workspa
                      quantize_q=quantize_q)
     _check(lib().mla_decode(_ptr(q), _ptr(kv), _ptr(kv_scale), _ptr(qo_indptr), _ptr(kv_indptr), _ptr(out),
                             kv_dtype, ctypes.byref(opts), _stream_handle(stream)), "mla_decode")
+
+
+def paged_workspace_size(batch: int, total_q: int, total_kv: int, kv_dtype: int, num_splits: int = 0) -> int:
+    out = ctypes.c_size_t(0)
+    _check(lib().mla_decode_paged_workspace_size(batch, total_q, total_kv, kv_dtype, num_splits, ctypes.byref(out)),
+           "mla_decode_paged_workspace_size")
+    return out.value
+
+
+def alloc_paged_workspace(batch: int, total_q: int, total_kv: int, kv_dtype: int, num_splits: int = 0,
+                          device="cuda"):
+    """A zeroed device workspace for decode_paged (torch uint8 tensor)."""
+    import torch
+    n = paged_workspace_size(batch, total_q, total_kv, kv_dtype, num_splits)
+    return torch.zeros(n, dtype=torch.uint8, device=device)
+
+
+def decode_paged(q, kv_pages, kv_scale, qo_indptr, page_indptr, page_indices, last_page_len, page_size: int,
+                 out, kv_dtype: int, *, total_kv: int, workspace, q_dtype: int = BF16, q_scale=None,
+                 sm_scale: float = 0.0, num_splits: int = 0, stream=None, events=None,
+                 quantize_q: bool = False) -> None:
+    """mla_decode_paged() on torch CUDA tensors: kv_pages is [num_pages][page_size][576] e4m3 codes (uint8),
+    the page table is int32 (last_page_len may be None when page_size == 1); total_kv is the logical row count
+    (sum of the segment lengths). Asynchronous."""
+    opts = make_opts(qo_indptr.numel() - 1, q.shape[0], total_kv, q_dtype=q_dtype, q_scale=q_scale,
+                     sm_scale=sm_scale, num_splits=num_splits, workspace=workspace, events=events,
+                     quantize_q=quantize_q)
+    pg = PagedKV(page_indptr=page_indptr.data_ptr(), page_indices=page_indices.data_ptr(),
+                 last_page_len=None if last_page_len is None else last_page_len.data_ptr(),
+                 page_size=int(page_size), num_pages=int(kv_pages.shape[0]))
+    _check(lib().mla_decode_paged(_ptr(q), _ptr(kv_pages), _ptr(kv_scale), _ptr(qo_indptr), ctypes.byref(pg),
+                                  _ptr(out), kv_dtype, ctypes.byref(opts), _stream_handle(stream)),
+           "mla_decode_paged")
 
 
 def decode_from_host(h, dev, kv_dtype: int, *, q_dtype: int, workspace, sm_scale: float = 0.0,

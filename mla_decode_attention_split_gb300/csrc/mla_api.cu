@@ -91,16 +91,29 @@ mla_status_t mla_decode_workspace_size(int32_t batch, int32_t total_q, int32_t t
   return MLA_OK;
 }
 
-mla_status_t mla_decode(const void* q, const void* kv, const void* kv_scale, const int32_t* qo_indptr,
-                        const int32_t* kv_indptr, void* out, mla_dtype_t kv_dtype, const mla_decode_opts* opts,
-                        void* stream) {
+}  // extern "C"
+
+namespace {
+
+// Shared by mla_decode and mla_decode_paged. With a page table (pg != NULL)
+// kv_indptr is ignored: the logical row offsets are built on the device into
+// the workspace, after the part mla_decode_workspace_size covers.
+mla_status_t decode_impl(const void* q, const void* kv, const void* kv_scale, const int32_t* qo_indptr,
+                         const int32_t* kv_indptr, void* out, mla_dtype_t kv_dtype, const mla_decode_opts* opts,
+                         const mla_paged_kv* pg, void* stream) {
   if (!opts) return MLA_ERR_INVALID_ARG;
   const int32_t batch = opts->batch, total_q = opts->total_q, total_kv = opts->total_kv;
   if (batch < 1 || total_q < 0 || total_kv < 0) return MLA_ERR_INVALID_ARG;
   if (kv_dtype != MLA_DTYPE_BF16 && kv_dtype != MLA_DTYPE_FP8_E4M3 && kv_dtype != MLA_DTYPE_MXFP4)
     return MLA_ERR_INVALID_ARG;
   if (opts->q_dtype != MLA_DTYPE_BF16 && opts->q_dtype != MLA_DTYPE_FP8_E4M3) return MLA_ERR_INVALID_ARG;
-  if (!qo_indptr || !kv_indptr) return MLA_ERR_INVALID_ARG;
+  if (!qo_indptr || (!pg && !kv_indptr)) return MLA_ERR_INVALID_ARG;
+  if (pg) {
+    if (pg->page_size < 1 || pg->num_pages < 0 || !pg->page_indptr || !pg->page_indices ||
+        (pg->page_size > 1 && !pg->last_page_len) || (total_kv > 0 && pg->num_pages < 1))
+      return MLA_ERR_INVALID_ARG;
+    if (kv_dtype != MLA_DTYPE_FP8_E4M3) return MLA_ERR_UNSUPPORTED;
+  }
   if (total_q > 0 && (!q || !out || !aligned16(q) || !aligned16(out))) return MLA_ERR_INVALID_ARG;
   if (total_kv > 0 && (!kv || !aligned16(kv))) return MLA_ERR_INVALID_ARG;
   if (kv_dtype != MLA_DTYPE_BF16 && !kv_scale) return MLA_ERR_INVALID_ARG;
@@ -112,7 +125,8 @@ mla_status_t mla_decode(const void* q, const void* kv, const void* kv_scale, con
   int32_t splits = opts->num_splits;
   if (splits < 0 || splits > kMaxSplits) return MLA_ERR_INVALID_ARG;
   if (splits == 0) splits = plan_splits(total_q, batch, total_kv, sm_count_of_current_device());
-  const size_t need = mla::workspace_bytes_for(splits, total_q);
+  const size_t base = mla::workspace_bytes_for(splits, total_q);
+  const size_t need = base + (pg ? mla::paged_extra_bytes(batch) : 0);
   if (!opts->workspace || opts->workspace_bytes < need ||
       (reinterpret_cast<uintptr_t>(opts->workspace) & 255u) != 0)
     return MLA_ERR_WORKSPACE;
@@ -125,7 +139,12 @@ mla_status_t mla_decode(const void* q, const void* kv, const void* kv_scale, con
   p.q_scale = opts->quantize_q ? reinterpret_cast<const float*>(static_cast<uint32_t*>(opts->workspace) + mla::kHdrQScale)
                                : opts->q_scale;
   p.qo_indptr = qo_indptr;
-  p.kv_indptr = kv_indptr;
+  p.kv_indptr = pg ? reinterpret_cast<const int32_t*>(static_cast<uint8_t*>(opts->workspace) + base) : kv_indptr;
+  p.paged = pg ? 1 : 0;
+  p.page_indptr = pg ? pg->page_indptr : nullptr;
+  p.page_indices = pg ? pg->page_indices : nullptr;
+  p.page_size = pg ? pg->page_size : 0;
+  p.num_pages = pg ? pg->num_pages : 0;
   p.batch = batch;
   p.total_q = total_q;
   p.total_kv = total_kv;
@@ -147,6 +166,9 @@ mla_status_t mla_decode(const void* q, const void* kv, const void* kv_scale, con
   // one launch: stage 1 also merges split tokens and zeroes tokens of empty
   // segments; with no KV rows at all every output row is zero
   if (total_kv > 0) {
+    if (pg && mla::launch_paged_prepare(pg->page_indptr, pg->last_page_len, batch, pg->page_size,
+                                        const_cast<int32_t*>(p.kv_indptr), p.dev_flags, st) != cudaSuccess)
+      return MLA_ERR_CUDA;
     if (opts->quantize_q &&
         mla::launch_q_scale(q, static_cast<int64_t>(total_q) * mla::kHeads * mla::kDqk, p.dev_flags, st) != cudaSuccess)
       return MLA_ERR_CUDA;
@@ -157,6 +179,30 @@ mla_status_t mla_decode(const void* q, const void* kv, const void* kv_scale, con
   if (!mark(1)) return MLA_ERR_CUDA;
   if (!mark(2)) return MLA_ERR_CUDA;
   return MLA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+mla_status_t mla_decode(const void* q, const void* kv, const void* kv_scale, const int32_t* qo_indptr,
+                        const int32_t* kv_indptr, void* out, mla_dtype_t kv_dtype, const mla_decode_opts* opts,
+                        void* stream) {
+  return decode_impl(q, kv, kv_scale, qo_indptr, kv_indptr, out, kv_dtype, opts, nullptr, stream);
+}
+
+mla_status_t mla_decode_paged_workspace_size(int32_t batch, int32_t total_q, int32_t total_kv, mla_dtype_t kv_dtype,
+                                             int32_t num_splits, size_t* bytes) {
+  const mla_status_t st = mla_decode_workspace_size(batch, total_q, total_kv, kv_dtype, num_splits, bytes);
+  if (st == MLA_OK) *bytes += mla::paged_extra_bytes(batch);
+  return st;
+}
+
+mla_status_t mla_decode_paged(const void* q, const void* kv_pages, const void* kv_scale, const int32_t* qo_indptr,
+                              const mla_paged_kv* paged, void* out, mla_dtype_t kv_dtype,
+                              const mla_decode_opts* opts, void* stream) {
+  if (!paged) return MLA_ERR_INVALID_ARG;
+  return decode_impl(q, kv_pages, kv_scale, qo_indptr, nullptr, out, kv_dtype, opts, paged, stream);
 }
 
 mla_status_t mla_decode_from_host(const void* h_q, const void* h_kv, const void* h_kv_scale, const float* h_q_scale,
@@ -222,7 +268,7 @@ mla_status_t mla_get_device_error(const void* workspace, void* stream, uint32_t*
   if (cudaStreamSynchronize(st) != cudaSuccess) return MLA_ERR_CUDA;
   if (flags) *flags = f;
   if (f & MLA_DEVFLAG_TIMEOUT) return MLA_ERR_TIMEOUT;
-  if (f & MLA_DEVFLAG_BAD_INDPTR) return MLA_ERR_DEVICE_CHECK;
+  if (f & (MLA_DEVFLAG_BAD_INDPTR | MLA_DEVFLAG_BAD_PAGE)) return MLA_ERR_DEVICE_CHECK;
   return MLA_OK;
 }
 

@@ -14,6 +14,7 @@ constexpr long long kWaitLimitCycles = 2000000000LL;
 
 constexpr uint32_t kFlagTimeout = 0x1u;
 constexpr uint32_t kFlagBadIndptr = 0x2u;
+constexpr uint32_t kFlagBadPage = 0x4u;  // a paged-KV page id outside the page pool
 
 __device__ __forceinline__ uint32_t smem_addr(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -85,6 +86,20 @@ __device__ __forceinline__ void bulk_g2s(uint32_t dst_smem, const void* src, uin
       "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], %4;"
       ::"r"(dst_smem), "l"(src), "r"(bytes), "r"(bar), "l"(policy)
       : "memory");
+}
+
+// 16-byte asynchronous global -> shared copy (L1 bypassed) with an L2 policy.
+__device__ __forceinline__ void cp_async16(uint32_t dst_smem, const void* src, uint64_t policy) {
+  asm volatile("cp.async.cg.shared.global.L2::cache_hint [%0], [%1], 16, %2;" ::"r"(dst_smem), "l"(src), "l"(policy)
+               : "memory");
+}
+
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+
+// Waits until at most N of this thread's committed copy groups are pending.
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
 }
 
 __device__ __forceinline__ uint64_t policy_evict_first() {

@@ -36,6 +36,13 @@ struct Stage1Params {
   float* part_lse;    // [slots][16] (log2 domain)
   uint32_t* dev_flags;
   uint32_t* tok_cnt;  // [total_q] partials finished per token
+  // paged KV: kv is [num_pages][page_size][576]; kv_indptr then holds the
+  // logical row offsets built from the page table (mla_paged.cu)
+  const int32_t* page_indptr;   // [batch+1] page-table entries of each segment
+  const int32_t* page_indices;  // page ids
+  int32_t page_size;
+  int32_t num_pages;
+  int32_t paged;
 };
 
 // KV formats / query formats as template tags (values match mla_dtype_t).
@@ -55,6 +62,11 @@ cudaError_t launch_dequant(const void* kv, const void* kv_scale, int kv_fmt, int
 bool stage1_supported(int kv_fmt, int q_fmt);
 // amax of bf16 q over n elements -> header word kHdrQScale = max(amax, 1e-12) / 448 (mla_qquant.cu)
 cudaError_t launch_q_scale(const void* q, int64_t n, uint32_t* header, cudaStream_t stream);
+// paged KV: logical row offsets [batch+1] from the page table (mla_paged.cu)
+cudaError_t launch_paged_prepare(const int32_t* page_indptr, const int32_t* last_page_len, int32_t batch,
+                                 int32_t page_size, int32_t* kv_indptr_out, uint32_t* flags, cudaStream_t stream);
+// bytes after the decode workspace for the logical row offsets of a paged call
+inline size_t paged_extra_bytes(int64_t batch) { return static_cast<size_t>(((batch + 1) * 4 + 255) / 256) * 256; }
 
 
 inline size_t workspace_bytes_for(int64_t num_splits, int64_t total_q) {

@@ -142,6 +142,8 @@ struct Piece {
   int64_t slot;       // partial slot (c + token) when not direct
   int64_t tok_vs;     // virtual start of the token's whole run
   int32_t kvlen;      // its length (the segment's KV rows)
+  int32_t seg;        // segment index
+  int32_t k0;         // first KV row of the segment
 };
 
 struct PieceCursor {
@@ -175,6 +177,8 @@ struct PieceCursor {
       pc.slot = cta + pc.token;
       pc.tok_vs = tok_vs;
       pc.kvlen = static_cast<int32_t>(kvlen);
+      pc.seg = seg;
+      pc.k0 = k0;
       x = stop;
       return true;
     }

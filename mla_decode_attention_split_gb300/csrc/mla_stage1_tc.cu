@@ -25,7 +25,8 @@
 //    one is consumed. The 64 rope dims of each row (used by Q.K^T only) are
 //    loaded by the softmax threads into registers two tiles ahead and written
 //    into a single 8 KB slot as soon as the previous tile's Q.K^T is done.
-//  * Warp 0 issues the TMA loads, warp 1 owns tensor memory and issues QK(n)
+//  * Warp 0 issues the TMA loads (a paged cache: warps 0 and 6 gather rows
+//    with cp.async), warp 1 owns tensor memory and issues QK(n)
 //    then PV(n-1) so the tensor core overlaps the softmax of tile n, warps 2-5
 //    (one thread per tile row / tensor-memory lane) read S, reduce the per-head
 //    max across the 128 rows, write P into shared memory, rescale O in tensor
@@ -35,12 +36,14 @@
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
+#include <cstring>
+
 #include "mla_tc_common.cuh"
 
 namespace mla {
 namespace tc {
 
-constexpr int kThreads = 192;  // warp 0 TMA, warp 1 MMA, warps 2-5 softmax
+constexpr int kThreads = 224;  // warp 0 TMA (paged: warps 0 and 6 gather), warp 1 MMA, warps 2-5 softmax
 constexpr int kStages = 3;
 constexpr int kStageBytes = kVBytes;  // 64 KB: the 512 V dims of a tile
 
@@ -145,6 +148,53 @@ __device__ void producer(const Cx& cx, const CUtensorMap* map, PieceCursor cur, 
   }
 }
 
+// Warps 0 and 6 with a paged cache: rows of a tile may come from any page, so
+// the V bytes are gathered with 16-byte cp.async copies (lane l copies bytes
+// 16l..16l+15 of each row) straight into the 128B-swizzled layout the TMA
+// boxes would produce. The two warps take alternate tiles, so two tiles are in
+// flight; once a warp's tile has landed its lanes make the copies visible to
+// the tensor core (async proxy) and one arrival completes the kv_full barrier.
+// Rows past the piece, and rows whose page id is outside the pool, are not
+// copied.
+__device__ void producer_paged(const Stage1Params& p, const Cx& cx, PieceCursor cur, int lane, uint32_t parity) {
+  const uint64_t pol = policy_evict_first();
+  const uint8_t* kv = static_cast<const uint8_t*>(p.kv) + lane * 16;
+  const uint32_t unit = lane & 7, chunk_off = (lane >> 3) * kChunkBytes;
+  Piece pc;
+  uint32_t n = 0;
+  bool ok = true;
+  while (ok && cur.next(pc)) {
+    for (int r0 = 0; r0 < pc.nrows; r0 += kTileRows, ++n) {
+      if ((n & 1u) != parity) continue;
+      const uint32_t s = n % kStages, rnd = n / kStages;
+      if (rnd >= 1 && !cx.wait(L::kKvEmpty + s, (rnd - 1) & 1u)) {
+        ok = false;
+        break;
+      }
+      const int nr = min(kTileRows, pc.nrows - r0);
+      const int32_t i0 = pc.kv_row - pc.k0 + r0;
+      int64_t phys[4];  // tile rows lane, lane + 32, lane + 64, lane + 96
+#pragma unroll
+      for (int j = 0; j < 4; ++j) phys[j] = (32 * j + lane < nr) ? paged_row(p, pc.seg, i0 + 32 * j + lane) : -1;
+      const uint32_t dst = cx.s + L::kOffKv + s * kStageBytes + chunk_off;
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+#pragma unroll 8
+        for (int rr = 0; rr < 32; ++rr) {
+          const int64_t g = __shfl_sync(0xffffffffu, phys[j], rr);
+          const uint32_t r = 32 * j + rr;
+          if (g >= 0) cp_async16(dst + r * 128 + ((unit ^ (r & 7u)) << 4), kv + g * kDqk, pol);
+        }
+      }
+      cp_async_commit();
+      cp_async_wait<0>();
+      fence_async_smem();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(cx.bar(L::kKvFull + s));
+    }
+  }
+}
+
 // ---------------------------------------------------------------------------
 // Warp 1 (one thread): QK(n) into S[n % 2], then PV(n-1) into O[piece % 2].
 struct PendingPV {
@@ -236,12 +286,17 @@ __device__ void mma_issuer(const Cx& cx, PieceCursor cur) {
 // Warps 2-5. Thread = tile row = tensor-memory lane (32 * (warp % 4) + lane).
 
 // Rope dims (bytes 512..575) of one tile row, from global memory into registers;
-// rows past the end of the cache read as zero.
+// rows past the end of the cache (paged: past the piece) read as zero.
 __device__ __forceinline__ void load_rope(const Stage1Params& p, TileWalker& rw, int row, uint4 (&r)[4]) {
-  int32_t row0;
-  const bool have = rw.next(row0);
-  const int64_t g = static_cast<int64_t>(row0) + row;
-  if (have && g < p.total_kv) {
+  TileRef t;
+  int64_t g = -1;
+  if (rw.next(t)) {
+    if (!p.paged)
+      g = static_cast<int64_t>(t.row) + row < p.total_kv ? static_cast<int64_t>(t.row) + row : -1;
+    else if (row < t.nvalid)
+      g = paged_row(p, t.seg, t.row - t.k0 + row);
+  }
+  if (g >= 0) {
     const uint4* src = reinterpret_cast<const uint4*>(static_cast<const uint8_t*>(p.kv) + g * kDqk + 512);
 #pragma unroll
     for (int i = 0; i < 4; ++i) r[i] = __ldg(src + i);
@@ -425,8 +480,14 @@ __global__ void __launch_bounds__(kThreads, 1) stage1_tc_kernel(const Stage1Para
   PieceCursor cur;
   if (!cta_begin(p, cx, smem_raw, 1, cur)) return;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  if (warp == 0)
-    producer(cx, &kvmap, cur, lane);
+  if (warp == 0) {
+    if (p.paged)
+      producer_paged(p, cx, cur, lane, 0u);
+    else
+      producer(cx, &kvmap, cur, lane);
+  } else if (warp == 6) {
+    if (p.paged) producer_paged(p, cx, cur, lane, 1u);
+  }
   else if (warp == 1) {
     if (lane == 0) mma_issuer(cx, cur);
     __syncwarp();
@@ -488,9 +549,12 @@ static cudaError_t launch_q(const Stage1Params& p, cudaStream_t stream) {
     if (e != cudaSuccess) return e;
     configured_device = dev;
   }
-  CUtensorMap map;
-  e = make_kv_map(&map, p.kv, p.total_kv);
-  if (e != cudaSuccess) return e;
+  CUtensorMap map;  // unused with a paged cache (its rows are gathered with cp.async)
+  memset(&map, 0, sizeof(map));
+  if (!p.paged) {
+    e = make_kv_map(&map, p.kv, p.total_kv);
+    if (e != cudaSuccess) return e;
+  }
   stage1_tc_kernel<QF><<<p.num_splits, kThreads, L::kAlloc, stream>>>(p, map);
   return cudaGetLastError();
 }

@@ -58,6 +58,10 @@ __device__ __forceinline__ void mbar_wait_drain_tc(uint32_t bar, uint32_t parity
 }
 
 // Walks the CTA's tiles in order (one 128-row tile at a time).
+struct TileRef {
+  int32_t row, seg, k0, nvalid;
+};
+
 struct TileWalker {
   PieceCursor cur;
   Piece pc;
@@ -68,10 +72,14 @@ struct TileWalker {
     have = cur.next(pc);
     r0 = 0;
   }
-  // First KV row of the next tile. Returns false when done.
-  __device__ bool next(int32_t& row) {
+  // The next tile: its first KV row, segment, the segment's first row and
+  // how many of its rows belong to the piece. Returns false when done.
+  __device__ bool next(TileRef& t) {
     if (!have) return false;
-    row = pc.kv_row + r0;
+    t.row = pc.kv_row + r0;
+    t.seg = pc.seg;
+    t.k0 = pc.k0;
+    t.nvalid = pc.nrows - r0;
     r0 += kTileRows;
     if (r0 >= pc.nrows) {
       have = cur.next(pc);
@@ -80,6 +88,20 @@ struct TileWalker {
     return true;
   }
 };
+
+// Paged KV: the physical row of row i of segment seg, or -1 (with the error
+// flag raised) when the page table names a page outside the pool. The page
+// table entry read is inside [page_indptr[seg], page_indptr[seg+1]) because
+// i is below the segment's row count.
+__device__ __forceinline__ int64_t paged_row(const Stage1Params& p, int32_t seg, int32_t i) {
+  const int32_t pg = i / p.page_size;
+  const int32_t id = __ldg(p.page_indices + __ldg(p.page_indptr + seg) + pg);
+  if (static_cast<uint32_t>(id) >= static_cast<uint32_t>(p.num_pages)) {
+    atomicOr(p.dev_flags, kFlagBadPage);
+    return -1;
+  }
+  return static_cast<int64_t>(id) * p.page_size + (i - pg * p.page_size);
+}
 
 // Per-tile bookkeeping of the UMMA issuer, packed in one word: bit 0 = first
 // tile of its piece, bit 1 = last tile of its piece, bits 2.. = piece index

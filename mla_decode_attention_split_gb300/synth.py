@@ -202,3 +202,66 @@ def to_host_codes(inp: Inputs, segments: list[int] | None = None) -> dict:
 
 def sm_scale_default() -> float:
     return 1.0 / math.sqrt(D_QK)
+
+
+@dataclasses.dataclass
+class PagedInputs:
+    """A paged fp8 KV cache: a pool of pages and a page table (int32, device)."""
+    q: torch.Tensor
+    q_scale: torch.Tensor | None
+    kv_pages: torch.Tensor          # uint8 e4m3 codes [num_pages, page_size, 576]
+    kv_scale: torch.Tensor          # float32 [1]
+    qo_indptr: torch.Tensor
+    page_indptr: torch.Tensor       # [batch + 1]
+    page_indices: torch.Tensor      # [page_indptr[-1]]
+    last_page_len: torch.Tensor     # [batch]
+    page_size: int
+    total_kv: int                   # logical rows, the sum of the segment lengths
+    q_dtype: int
+    kv_dtype: int = FP8_E4M3
+
+    @property
+    def batch(self) -> int:
+        return self.qo_indptr.numel() - 1
+
+    @property
+    def total_q(self) -> int:
+        return self.q.shape[0]
+
+    @property
+    def num_pages(self) -> int:
+        return self.kv_pages.shape[0]
+
+
+def make_paged_inputs(w: Workload, device: str | torch.device = "cpu", *, kv_lens: list[int] | None = None,
+                      q_lens: list[int] | None = None, page_size: int = 1, spare_pages: int = 0,
+                      lengths_as_last: bool = False) -> PagedInputs:
+    """Seeded paged inputs: q as make_inputs, a pool of ceil(len/page_size) pages per
+    segment plus `spare_pages` unused ones (values ~N(0,1), one per-tensor fp8 scale),
+    handed out in a random order so a segment's pages are scattered over the pool.
+    With page_size 1 and lengths_as_last, last_page_len holds the segment lengths
+    (the argument form of kernelbot-amd-mixed-mla-753817's paged call); otherwise
+    each segment's last page holds the remaining rows."""
+    device = torch.device(device)
+    kv_lens = list(kv_lens) if kv_lens is not None else make_lengths(w)
+    base = make_inputs(dataclasses.replace(w, kv_dtype=BF16), device, kv_lens=[0] * len(kv_lens), q_lens=q_lens)
+    npages = [(n + page_size - 1) // page_size for n in kv_lens]
+    used = int(sum(npages))
+    num_pages = used + spare_pages
+    g = torch.Generator(device="cpu").manual_seed(w.seed + 2)
+    order = torch.randperm(num_pages, generator=g).to(torch.int32)
+    page_indices = order[:used].contiguous()
+    page_indptr = torch.tensor([0] + list(np.cumsum(npages)), dtype=torch.int32)
+    if page_size == 1 and lengths_as_last:
+        last = list(kv_lens)
+    else:
+        last = [n - (p - 1) * page_size if p > 0 else page_size for n, p in zip(kv_lens, npages)]
+    gk = torch.Generator(device=device).manual_seed(w.seed + 3)
+    kvf = torch.randn((max(num_pages, 1) * page_size, D_QK), generator=gk, device=device, dtype=torch.float32)
+    codes, scale = quantize_fp8_per_tensor(kvf)
+    del kvf
+    pool = codes[: num_pages * page_size].reshape(num_pages, page_size, D_QK).contiguous()
+    return PagedInputs(q=base.q, q_scale=base.q_scale, kv_pages=pool, kv_scale=scale, qo_indptr=base.qo_indptr,
+                       page_indptr=page_indptr.to(device), page_indices=page_indices.to(device),
+                       last_page_len=torch.tensor(last, dtype=torch.int32).to(device), page_size=page_size,
+                       total_kv=int(sum(kv_lens)), q_dtype=w.q_dtype)

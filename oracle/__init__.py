@@ -159,3 +159,42 @@ def lse_combine(o, lse):
     lse_out = np.empty(1, dtype=np.float64)
     _load().orc_lse_combine(nsplit, dv, _ptr(o), _ptr(lse), _ptr(out), _ptr(lse_out))
     return out, float(lse_out[0])
+
+
+def paged_rows(kv_pages, page_indptr, page_indices, last_page_len, page_size):
+    """The KV rows a page table names, laid out contiguously, with their row offsets.
+
+    The page-table form is that of kernelbot-amd-mixed-mla-753817, which hands
+    ``kv_indices``, ``kv_last_page_len`` and ``page_size`` to the vendor a8w8
+    decode: segment b owns table entries [page_indptr[b], page_indptr[b+1]);
+    its row i is row i % page_size of page page_indices[page_indptr[b] + i // page_size].
+    A segment of n > 0 pages has (n - 1) * page_size + last_page_len[b] rows; with
+    page_size 1 it has n rows (the pages pass the segment lengths as
+    ``kv_last_page_len`` there, which only this reading accepts).
+
+    kv_pages: [num_pages, page_size, ...]; returns (rows [total, ...], kv_indptr [batch + 1]).
+    Pure index work, written as plain loops."""
+    pages = np.asarray(kv_pages)
+    pip = [int(x) for x in np.asarray(page_indptr).reshape(-1)]
+    idx = [int(x) for x in np.asarray(page_indices).reshape(-1)]
+    batch = len(pip) - 1
+    assert pip[0] == 0 and all(pip[b + 1] >= pip[b] for b in range(batch))
+    rows, kv_indptr = [], [0]
+    for b in range(batch):
+        n = pip[b + 1] - pip[b]
+        if n == 0:
+            length = 0
+        elif page_size == 1:
+            length = n
+        else:
+            last = int(np.asarray(last_page_len).reshape(-1)[b])
+            assert 1 <= last <= page_size
+            length = (n - 1) * page_size + last
+        for i in range(length):
+            page = idx[pip[b] + i // page_size]
+            assert 0 <= page < pages.shape[0]
+            rows.append(pages[page, i % page_size])
+        kv_indptr.append(kv_indptr[-1] + length)
+    shape = (0,) + pages.shape[2:]
+    out = np.stack(rows) if rows else np.zeros(shape, dtype=pages.dtype)
+    return out, np.asarray(kv_indptr, dtype=np.int32)

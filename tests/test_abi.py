@@ -116,3 +116,34 @@ def test_argument_checks_fail_before_any_device_work(lib):
     st = L.mla_dequant_rows(ctypes.c_void_p(aligned), None, m.FP8_E4M3, 10, 5, 6, ctypes.c_void_p(aligned), None)
     assert st == m.MLA_ERR_INVALID_ARG
     assert L.mla_get_device_error(None, None, None) == m.MLA_ERR_INVALID_ARG
+
+
+def test_paged_workspace_size_and_argument_checks(lib):
+    L = lib
+    base = m.workspace_size(4, 4, 4096, m.FP8_E4M3, num_splits=32)
+    # room for the logical row offsets: batch + 1 int32, padded to 256 bytes
+    assert m.paged_workspace_size(4, 4, 4096, m.FP8_E4M3, num_splits=32) == base + 256
+    assert m.paged_workspace_size(64, 64, 4096, m.FP8_E4M3, num_splits=32) == \
+        m.workspace_size(64, 64, 4096, m.FP8_E4M3, num_splits=32) + 512
+    buf = (ctypes.c_uint8 * 64)()
+    a = ctypes.c_void_p((ctypes.addressof(buf) + 15) & ~15)
+    opts = m.DecodeOpts(batch=1, total_q=1, total_kv=10, sm_scale=0.0, q_dtype=m.BF16, q_scale=None, num_splits=1,
+                        workspace=None, workspace_bytes=0)
+    pg = m.PagedKV(page_indptr=a.value, page_indices=a.value, last_page_len=a.value, page_size=4, num_pages=3)
+    args = lambda dt: (a, a, a, a, ctypes.byref(pg), a, dt, ctypes.byref(opts), None)  # noqa: E731
+    assert L.mla_decode_paged(a, a, a, a, None, a, m.FP8_E4M3, ctypes.byref(opts), None) == m.MLA_ERR_INVALID_ARG
+    pg.page_size = 0
+    assert L.mla_decode_paged(*args(m.FP8_E4M3)) == m.MLA_ERR_INVALID_ARG
+    pg.page_size, pg.last_page_len = 4, None  # last-page lengths are needed when page_size > 1
+    assert L.mla_decode_paged(*args(m.FP8_E4M3)) == m.MLA_ERR_INVALID_ARG
+    pg.page_size = 1  # ... but not with one row per page
+    assert L.mla_decode_paged(*args(m.FP8_E4M3)) == m.MLA_ERR_WORKSPACE
+    pg.num_pages = 0
+    assert L.mla_decode_paged(*args(m.FP8_E4M3)) == m.MLA_ERR_INVALID_ARG
+    pg.num_pages = 3
+    for dt in (m.BF16, m.MXFP4):  # the paged path is the fp8 tensor-core kernel
+        assert L.mla_decode_paged(*args(dt)) == m.MLA_ERR_UNSUPPORTED
+    # a workspace sized for the contiguous call is too small for the paged one
+    n = m.workspace_size(1, 1, 10, m.FP8_E4M3, num_splits=1)
+    opts.workspace, opts.workspace_bytes = 256, n
+    assert L.mla_decode_paged(*args(m.FP8_E4M3)) == m.MLA_ERR_WORKSPACE
