@@ -166,7 +166,8 @@ typedef struct {
   const int32_t* last_page_len; /* [batch], each in [1, page_size]; may be NULL
                                    when page_size == 1                           */
   int32_t page_size;            /* KV rows per page, >= 1                        */
-  int32_t num_pages;            /* pages in the pool kv_pages points to          */
+  int32_t num_pages;            /* pages in the pool kv_pages points to;
+                                   num_pages * page_size < 2^31                  */
 } mla_paged_kv;
 
 /* Workspace bytes for mla_decode_paged(): mla_decode_workspace_size() plus

@@ -110,7 +110,8 @@ mla_status_t decode_impl(const void* q, const void* kv, const void* kv_scale, co
   if (!qo_indptr || (!pg && !kv_indptr)) return MLA_ERR_INVALID_ARG;
   if (pg) {
     if (pg->page_size < 1 || pg->num_pages < 0 || !pg->page_indptr || !pg->page_indices ||
-        (pg->page_size > 1 && !pg->last_page_len) || (total_kv > 0 && pg->num_pages < 1))
+        (pg->page_size > 1 && !pg->last_page_len) || (total_kv > 0 && pg->num_pages < 1) ||
+        static_cast<int64_t>(pg->num_pages) * pg->page_size > INT32_MAX)
       return MLA_ERR_INVALID_ARG;
     if (kv_dtype != MLA_DTYPE_FP8_E4M3) return MLA_ERR_UNSUPPORTED;
   }
@@ -144,6 +145,9 @@ mla_status_t decode_impl(const void* q, const void* kv, const void* kv_scale, co
   p.page_indptr = pg ? pg->page_indptr : nullptr;
   p.page_indices = pg ? pg->page_indices : nullptr;
   p.page_size = pg ? pg->page_size : 0;
+  p.page_shift = -1;
+  for (int32_t sh = 0; sh < 31 && pg; ++sh)
+    if ((int32_t{1} << sh) == pg->page_size) p.page_shift = sh;
   p.num_pages = pg ? pg->num_pages : 0;
   p.batch = batch;
   p.total_q = total_q;

@@ -41,6 +41,7 @@ struct Stage1Params {
   const int32_t* page_indptr;   // [batch+1] page-table entries of each segment
   const int32_t* page_indices;  // page ids
   int32_t page_size;
+  int32_t page_shift;  // log2(page_size) when it is a power of two, else -1
   int32_t num_pages;
   int32_t paged;
 };

@@ -144,6 +144,8 @@ struct Piece {
   int32_t kvlen;      // its length (the segment's KV rows)
   int32_t seg;        // segment index
   int32_t k0;         // first KV row of the segment
+  int32_t lead;       // rows before the piece that its first tile also covers (see align8)
+  int32_t pbase;      // paged KV: the segment's first page-table entry (0 otherwise)
 };
 
 struct PieceCursor {
@@ -154,6 +156,12 @@ struct PieceCursor {
   int32_t seg;        // current segment
   int64_t seg_vs;     // its virtual start
   int64_t cta;
+  // nonzero: a piece's rows are taken from the multiple of 8 (counted from the
+  // segment's first row) at or before its start; the extra `lead` rows belong
+  // to the same segment and are masked by the consumer
+  int32_t align8;
+  // paged KV: page_indptr, read with the segment's other offsets (else null)
+  const int32_t* pip;
 
   __device__ __forceinline__ bool next(Piece& pc) {
     while (x < end && seg < batch) {
@@ -170,15 +178,18 @@ struct PieceCursor {
       const int64_t tok_vs = seg_vs + ti * kvlen;
       const int64_t row_in = x - tok_vs;
       const int64_t stop = min(end, tok_vs + kvlen);
+      const int32_t lead = align8 ? static_cast<int32_t>(row_in & 7) : 0;
       pc.token = static_cast<int32_t>(q0 + ti);
-      pc.kv_row = static_cast<int32_t>(k0 + row_in);
-      pc.nrows = static_cast<int32_t>(stop - x);
+      pc.kv_row = static_cast<int32_t>(k0 + row_in) - lead;
+      pc.nrows = static_cast<int32_t>(stop - x) + lead;
+      pc.lead = lead;
       pc.direct = (row_in == 0 && stop == tok_vs + kvlen) ? 1 : 0;
       pc.slot = cta + pc.token;
       pc.tok_vs = tok_vs;
       pc.kvlen = static_cast<int32_t>(kvlen);
       pc.seg = seg;
       pc.k0 = k0;
+      pc.pbase = pip ? __ldg(pip + seg) : 0;
       x = stop;
       return true;
     }

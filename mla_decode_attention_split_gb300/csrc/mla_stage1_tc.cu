@@ -25,8 +25,9 @@
 //    one is consumed. The 64 rope dims of each row (used by Q.K^T only) are
 //    loaded by the softmax threads into registers two tiles ahead and written
 //    into a single 8 KB slot as soon as the previous tile's Q.K^T is done.
-//  * Warp 0 issues the TMA loads (a paged cache: warps 0 and 6 gather rows
-//    with cp.async), warp 1 owns tensor memory and issues QK(n)
+//  * Warp 0 issues the TMA loads (a paged cache: runs of consecutive pool
+//    rows by TMA, other rows by cp.async), warp 1 owns tensor memory and
+//    issues QK(n)
 //    then PV(n-1) so the tensor core overlaps the softmax of tile n, warps 2-5
 //    (one thread per tile row / tensor-memory lane) read S, reduce the per-head
 //    max across the 128 rows, write P into shared memory, rescale O in tensor
@@ -36,14 +37,14 @@
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
-#include <cstring>
+#include <type_traits>
 
 #include "mla_tc_common.cuh"
 
 namespace mla {
 namespace tc {
 
-constexpr int kThreads = 224;  // warp 0 TMA (paged: warps 0 and 6 gather), warp 1 MMA, warps 2-5 softmax
+constexpr int kThreads = 256;  // warp 0 TMA, warp 1 MMA, warps 2-5 softmax, 6-7 only in the merge
 constexpr int kStages = 3;
 constexpr int kStageBytes = kVBytes;  // 64 KB: the 512 V dims of a tile
 
@@ -148,49 +149,133 @@ __device__ void producer(const Cx& cx, const CUtensorMap* map, PieceCursor cur, 
   }
 }
 
-// Warps 0 and 6 with a paged cache: rows of a tile may come from any page, so
-// the V bytes are gathered with 16-byte cp.async copies (lane l copies bytes
-// 16l..16l+15 of each row) straight into the 128B-swizzled layout the TMA
-// boxes would produce. The two warps take alternate tiles, so two tiles are in
-// flight; once a warp's tile has landed its lanes make the copies visible to
-// the tensor core (async proxy) and one arrival completes the kv_full barrier.
-// Rows past the piece, and rows whose page id is outside the pool, are not
-// copied.
-__device__ void producer_paged(const Stage1Params& p, const Cx& cx, PieceCursor cur, int lane, uint32_t parity) {
+// Warp 0 with a paged cache. Rows of a tile that are consecutive rows of the
+// pool (a run inside one page, or
+// pages laid out in order) come in by TMA: each maximal run of whole 8-row
+// groups is one box per 128-byte chunk, 8 to 128 rows high (one tensor map per
+// height), landing in the same 128B-swizzled layout as the contiguous path's
+// 128-row boxes. The rows of the other groups are gathered with 16-byte
+// cp.async copies (lane l copies bytes 16l..16l+15 of each row) into that
+// layout; once they have landed every lane makes them visible to the tensor
+// core (async proxy) before the warp's arrival on kv_full. The page ids of
+// the next tile are loaded while the current tile is issued. Rows past the
+// piece, and rows whose page id is outside the pool, are not copied.
+struct PagedMaps {
+  CUtensorMap box[16];  // box[h]: 128 bytes x 8 (h + 1) rows of the pool
+};
+
+struct PagedDrain {
+  uint32_t issued, tma_hist, n_last;  // tiles issued, which of the last ones used TMA, the last tile
+};
+
+__device__ PagedDrain producer_paged(const Stage1Params& p, const Cx& cx, const PagedMaps* maps, PieceCursor cur,
+                                     int lane) {
   const uint64_t pol = policy_evict_first();
   const uint8_t* kv = static_cast<const uint8_t*>(p.kv) + lane * 16;
   const uint32_t unit = lane & 7, chunk_off = (lane >> 3) * kChunkBytes;
-  Piece pc;
-  uint32_t n = 0;
-  bool ok = true;
-  while (ok && cur.next(pc)) {
-    for (int r0 = 0; r0 < pc.nrows; r0 += kTileRows, ++n) {
-      if ((n & 1u) != parity) continue;
-      const uint32_t s = n % kStages, rnd = n / kStages;
-      if (rnd >= 1 && !cx.wait(L::kKvEmpty + s, (rnd - 1) & 1u)) {
-        ok = false;
-        break;
-      }
-      const int nr = min(kTileRows, pc.nrows - r0);
-      const int32_t i0 = pc.kv_row - pc.k0 + r0;
-      int64_t phys[4];  // tile rows lane, lane + 32, lane + 64, lane + 96
+  if (lane < 16) prefetch_tensormap(&maps->box[lane]);
+  TileWalker tw;
+  tw.init(cur);
+  PagedRow id[4], id_next[4];  // page ids of this tile and the next (loaded two tiles ahead)
+  bool have = paged_tile_ids(p, tw, lane, id);
+  bool have_next = have && paged_tile_ids(p, tw, lane, id_next);
+  uint32_t issued = 0, tma_hist = 0, n_last = 0;
+  TC_PT_INIT
+  for (uint32_t n = 0; have; ++n) {
+    const uint32_t s = n % kStages, rnd = n / kStages;
+    if (rnd >= 1 && !cx.wait(L::kKvEmpty + s, (rnd - 1) & 1u)) break;
+    TC_PT(0);
+    int32_t phys[4];      // tile rows lane + 32 j
+    uint32_t contig = 0;  // bit g: rows 8g..8g+7 are consecutive rows of the pool
+    uint32_t linked = 0;  // bit g: row 8g follows row 8g-1 in the pool
+    int32_t last_prev = -1;
 #pragma unroll
-      for (int j = 0; j < 4; ++j) phys[j] = (32 * j + lane < nr) ? paged_row(p, pc.seg, i0 + 32 * j + lane) : -1;
-      const uint32_t dst = cx.s + L::kOffKv + s * kStageBytes + chunk_off;
+    for (int j = 0; j < 4; ++j) {
+      phys[j] = phys_row(p, id[j]);
+      int32_t prev = __shfl_up_sync(0xffffffffu, phys[j], 1);
+      if (lane == 0) prev = last_prev;
+      last_prev = __shfl_sync(0xffffffffu, phys[j], 31);
+      const bool follows = phys[j] >= 0 && prev >= 0 && phys[j] == prev + 1;
+      const uint32_t b = __ballot_sync(0xffffffffu, phys[j] >= 0 && ((lane & 7) == 0 || follows));
+      const uint32_t l = __ballot_sync(0xffffffffu, follows);
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        if (((b >> (8 * q)) & 0xFFu) == 0xFFu) contig |= 1u << (4 * j + q);
+        if ((l >> (8 * q)) & 1u) linked |= 1u << (4 * j + q);
+      }
+    }
+    const uint32_t bar = cx.bar(L::kKvFull + s);
+    const uint32_t stage = cx.s + L::kOffKv + s * kStageBytes;
+    TC_PT(4);
+    if (contig) {
+      if (lane == 0) mbar_expect_tx(bar, static_cast<uint32_t>(__popc(contig)) * kVChunks * 1024u);
+      __syncwarp();
+      // runs: a contiguous group starts one unless it continues the previous contiguous group
+      uint32_t starts = contig & ~((contig << 1) & linked);
+      while (starts) {
+        const int g0 = __ffs(starts) - 1;
+        starts &= starts - 1;
+        const uint32_t after = ~(contig >> g0);  // run = contiguous groups g0.. linked to their predecessor
+        int len = 1;
+        while (g0 + len < 16 && !((after >> len) & 1u) && ((linked >> (g0 + len)) & 1u)) ++len;
+        int32_t y = 0;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const int32_t v = __shfl_sync(0xffffffffu, phys[j], (g0 & 3) * 8);
+          if ((g0 >> 2) == j) y = v;
+        }
+        if (lane < kVChunks)
+          tma_load_2d(stage + lane * kChunkBytes + g0 * 1024, &maps->box[len - 1], lane * 128, y, bar, pol);
+      }
+    }
+    TC_PT(5);
+  if (contig != 0xFFFFu) {
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
 #pragma unroll 8
         for (int rr = 0; rr < 32; ++rr) {
-          const int64_t g = __shfl_sync(0xffffffffu, phys[j], rr);
+          const int32_t g = __shfl_sync(0xffffffffu, phys[j], rr);
           const uint32_t r = 32 * j + rr;
-          if (g >= 0) cp_async16(dst + r * 128 + ((unit ^ (r & 7u)) << 4), kv + g * kDqk, pol);
+          if (g >= 0 && !((contig >> (r >> 3)) & 1u))
+            cp_async16(stage + chunk_off + r * 128 + ((unit ^ (r & 7u)) << 4), kv + static_cast<int64_t>(g) * kDqk,
+                       pol);
         }
       }
       cp_async_commit();
+    }
+    TC_PT(1);
+    if (contig == 0xFFFFu) {  // all by TMA: the barrier completes when the boxes land
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar);
+    }
+#pragma unroll
+    for (int j = 0; j < 4; ++j) id[j] = id_next[j];
+    have = have_next;
+    have_next = have && paged_tile_ids(p, tw, lane, id_next);  // two tiles ahead
+    TC_PT(2);
+    if (contig != 0xFFFFu) {
       cp_async_wait<0>();
       fence_async_smem();
       __syncwarp();
-      if (lane == 0) mbar_arrive(cx.bar(L::kKvFull + s));
+      if (lane == 0) mbar_arrive(bar);
+    }
+    tma_hist = (tma_hist << 1) | (contig ? 1u : 0u);
+    ++issued;
+    n_last = n;
+    TC_PT(3);
+  }
+  return PagedDrain{issued, tma_hist, n_last};
+}
+
+// When the CTA stopped early (a bounded wait ran out) the consumer may not
+// have waited for every tile: the producer's last TMA tiles (one per stage,
+// the older ones were released through kv_empty) land before the CTA exits.
+// Called after all roles have returned.
+__device__ void drain_paged(const Cx& cx, const PagedDrain& d) {
+  for (uint32_t k = 0; k < 3 && k < d.issued; ++k) {
+    if ((d.tma_hist >> k) & 1u) {
+      const uint32_t nn = d.n_last - k;
+      mbar_wait_drain_tc(cx.bar(L::kKvFull + nn % kStages), (nn / kStages) & 1u);
     }
   }
 }
@@ -286,18 +371,33 @@ __device__ void mma_issuer(const Cx& cx, PieceCursor cur) {
 // Warps 2-5. Thread = tile row = tensor-memory lane (32 * (warp % 4) + lane).
 
 // Rope dims (bytes 512..575) of one tile row, from global memory into registers;
-// rows past the end of the cache (paged: past the piece) read as zero.
+// rows past the end of the cache read as zero.
 __device__ __forceinline__ void load_rope(const Stage1Params& p, TileWalker& rw, int row, uint4 (&r)[4]) {
-  TileRef t;
-  int64_t g = -1;
-  if (rw.next(t)) {
-    if (!p.paged)
-      g = static_cast<int64_t>(t.row) + row < p.total_kv ? static_cast<int64_t>(t.row) + row : -1;
-    else if (row < t.nvalid)
-      g = paged_row(p, t.seg, t.row - t.k0 + row);
-  }
-  if (g >= 0) {
+  int32_t row0;
+  const bool have = rw.next(row0);
+  const int64_t g = static_cast<int64_t>(row0) + row;
+  if (have && g < p.total_kv) {
     const uint4* src = reinterpret_cast<const uint4*>(static_cast<const uint8_t*>(p.kv) + g * kDqk + 512);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) r[i] = __ldg(src + i);
+  } else {
+#pragma unroll
+    for (int i = 0; i < 4; ++i) r[i] = make_uint4(0u, 0u, 0u, 0u);
+  }
+}
+
+// Paged cache: the page id of this thread's row of the next tile (its load is
+// consumed one tile later), and the rope bytes of a row from its page id.
+__device__ __forceinline__ PagedRow next_rope_id(const Stage1Params& p, TileWalker& rw, int row) {
+  TileRef t;
+  return (rw.next(t) && row < t.nvalid) ? page_of(p, t.pbase, t.row - t.k0 + row) : page_of_none();
+}
+
+__device__ __forceinline__ void load_rope_paged(const Stage1Params& p, PagedRow id, uint4 (&r)[4]) {
+  const int32_t g = phys_row(p, id);
+  if (g >= 0) {
+    const uint4* src =
+        reinterpret_cast<const uint4*>(static_cast<const uint8_t*>(p.kv) + static_cast<int64_t>(g) * kDqk + 512);
 #pragma unroll
     for (int i = 0; i < 4; ++i) r[i] = __ldg(src + i);
   } else {
@@ -314,7 +414,7 @@ __device__ __forceinline__ void store_rope(const Cx& cx, const SoftmaxCtx& sx, c
   if (sx.lane == 0) mbar_arrive(cx.bar(L::kRopeFull));
 }
 
-template <int QF>
+template <int QF, bool kPaged>
 __device__ void softmax_role(const Stage1Params& p, const Cx& cx, PieceCursor cur, int warp, int lane) {
   SoftmaxCtx sx;
   sx.lane = lane;
@@ -331,13 +431,26 @@ __device__ void softmax_role(const Stage1Params& p, const Cx& cx, PieceCursor cu
   bool have = ahead.next(pc);
   if (!have) return;
   // rope of tiles 0 and 1 into registers; tile 0 into the slot; tile 2 loads
+  // (a paged cache: the rope warp does this)
   TileWalker rw;
-  rw.init(cur);
   uint4 rb0[4], rb1[4];  // rope of the even / odd tile in flight
-  load_rope(p, rw, sx.row, rb0);
-  load_rope(p, rw, sx.row, rb1);
-  store_rope(cx, sx, rb0);
-  load_rope(p, rw, sx.row, rb0);
+  PagedRow rid = page_of_none();  // paged: the page id of this row of the tile after the next rope load
+  rw.init(cur);
+  if constexpr (!kPaged) {
+    load_rope(p, rw, sx.row, rb0);
+    load_rope(p, rw, sx.row, rb1);
+    store_rope(cx, sx, rb0);
+    load_rope(p, rw, sx.row, rb0);
+  } else {
+    rid = next_rope_id(p, rw, sx.row);
+    load_rope_paged(p, rid, rb0);
+    rid = next_rope_id(p, rw, sx.row);
+    load_rope_paged(p, rid, rb1);
+    store_rope(cx, sx, rb0);
+    rid = next_rope_id(p, rw, sx.row);
+    load_rope_paged(p, rid, rb0);
+    rid = next_rope_id(p, rw, sx.row);
+  }
   float c = setup_q<L, QF>(p, cx, sx, pc.token, 0, kvsc);
   if (c < 0.f) return;
   uint32_t n = 0, k = 0;
@@ -365,12 +478,23 @@ __device__ void softmax_role(const Stage1Params& p, const Cx& cx, PieceCursor cu
       TC_PT(0);
       // Q.K^T(n) is done: the rope slot takes tile n+1, its registers tile n+3
       if (tiles_left > 0) {
-        if (n & 1u) {
-          store_rope(cx, sx, rb0);
-          load_rope(p, rw, sx.row, rb0);
+        if constexpr (kPaged) {  // the page id was loaded one tile earlier
+          if (n & 1u) {
+            store_rope(cx, sx, rb0);
+            load_rope_paged(p, rid, rb0);
+          } else {
+            store_rope(cx, sx, rb1);
+            load_rope_paged(p, rid, rb1);
+          }
+          rid = next_rope_id(p, rw, sx.row);
         } else {
-          store_rope(cx, sx, rb1);
-          load_rope(p, rw, sx.row, rb1);
+          if (n & 1u) {
+            store_rope(cx, sx, rb0);
+            load_rope(p, rw, sx.row, rb0);
+          } else {
+            store_rope(cx, sx, rb1);
+            load_rope(p, rw, sx.row, rb1);
+          }
         }
       }
       --tiles_left;
@@ -381,7 +505,7 @@ __device__ void softmax_role(const Stage1Params& p, const Cx& cx, PieceCursor cu
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(cx.bar(L::kSEmpty + s));
-      const bool valid = sx.row < nr;
+      const bool valid = sx.row < nr && (r0 > 0 || sx.row >= pc.lead);
       float x[16];
 #pragma unroll
       for (int h = 0; h < 16; ++h) {
@@ -473,26 +597,38 @@ __device__ void softmax_role(const Stage1Params& p, const Cx& cx, PieceCursor cu
   }
 }
 
-template <int QF>
-__global__ void __launch_bounds__(kThreads, 1) stage1_tc_kernel(const Stage1Params p, const __grid_constant__ CUtensorMap kvmap) {
+template <bool kPaged>
+using KvMaps = std::conditional_t<kPaged, PagedMaps, CUtensorMap>;
+
+template <int QF, bool kPaged>
+__global__ void __launch_bounds__(kThreads, 1) stage1_tc_kernel(const Stage1Params p,
+                                                                const __grid_constant__ KvMaps<kPaged> kvmap) {
   extern __shared__ uint8_t smem_raw[];
   Cx cx;
   PieceCursor cur;
   if (!cta_begin(p, cx, smem_raw, 1, cur)) return;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  // tiles start at multiples of 8 rows of their segment, so that with a paged
+  // cache the 8-row groups line up with pages of 8k rows; the contiguous cache
+  // uses the same tiles, so both forms give identical results
+  cur.align8 = 1;
+  if constexpr (kPaged) cur.pip = p.page_indptr;
+  PagedDrain drain{0u, 0u, 0u};
   if (warp == 0) {
-    if (p.paged)
-      producer_paged(p, cx, cur, lane, 0u);
+    if constexpr (kPaged)
+      drain = producer_paged(p, cx, &kvmap, cur, lane);
     else
       producer(cx, &kvmap, cur, lane);
-  } else if (warp == 6) {
-    if (p.paged) producer_paged(p, cx, cur, lane, 1u);
-  }
-  else if (warp == 1) {
+  } else if (warp == 1) {
     if (lane == 0) mma_issuer(cx, cur);
     __syncwarp();
-  } else
-    softmax_role<QF>(p, cx, cur, warp, lane);
+  } else if (warp < 6) {
+    softmax_role<QF, kPaged>(p, cx, cur, warp, lane);
+  }
+  if constexpr (kPaged) {
+    __syncthreads();
+    if (*cx.abort_word) drain_paged(cx, drain);
+  }
   cta_end(p, cx, 1);
 }
 
@@ -512,12 +648,14 @@ static EncodeFn encode_fn() {
   return fn;
 }
 
-static cudaError_t make_kv_map(CUtensorMap* map, const void* kv, int64_t total_kv) {
+// box_rows = 128 (a whole tile) for a contiguous cache; 8, 16, .., 128 for the
+// pool of a paged one.
+static cudaError_t make_kv_map(CUtensorMap* map, const void* kv, int64_t total_kv, uint32_t box_rows) {
   EncodeFn fn = encode_fn();
   if (!fn) return cudaErrorNotSupported;
   const cuuint64_t dims[2] = {static_cast<cuuint64_t>(kDqk), static_cast<cuuint64_t>(total_kv)};
   const cuuint64_t strides[1] = {static_cast<cuuint64_t>(kDqk)};
-  const cuuint32_t box[2] = {128, static_cast<cuuint32_t>(kTileRows)};
+  const cuuint32_t box[2] = {128, box_rows};
   const cuuint32_t es[2] = {1, 1};
   const CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(kv), dims, strides, box, es,
                         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -538,32 +676,53 @@ extern "C" int mla_debug_phase_cycles_tc(unsigned long long* host, int n, int re
 }
 #endif
 
-template <int QF>
+template <int QF, bool kPaged>
 static cudaError_t launch_q(const Stage1Params& p, cudaStream_t stream) {
   static int configured_device = -1;
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (configured_device != dev) {
-    e = cudaFuncSetAttribute(stage1_tc_kernel<QF>, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kAlloc);
+    e = cudaFuncSetAttribute(stage1_tc_kernel<QF, kPaged>, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kAlloc);
     if (e != cudaSuccess) return e;
     configured_device = dev;
   }
-  CUtensorMap map;  // unused with a paged cache (its rows are gathered with cp.async)
-  memset(&map, 0, sizeof(map));
-  if (!p.paged) {
-    e = make_kv_map(&map, p.kv, p.total_kv);
+  if constexpr (kPaged) {
+    // the 16 maps of a pool are encoded once per (device, pool) and reused
+    thread_local int cached_dev = -1;
+    thread_local const void* cached_kv = nullptr;
+    thread_local int64_t cached_rows = -1;
+    thread_local PagedMaps maps;
+    const int64_t rows = static_cast<int64_t>(p.num_pages) * p.page_size;
+    if (cached_dev != dev || cached_kv != p.kv || cached_rows != rows) {
+      cached_dev = -1;
+      for (uint32_t h = 0; h < 16; ++h) {
+        e = make_kv_map(&maps.box[h], p.kv, rows, 8 * (h + 1));
+        if (e != cudaSuccess) return e;
+      }
+      cached_dev = dev;
+      cached_kv = p.kv;
+      cached_rows = rows;
+    }
+    stage1_tc_kernel<QF, kPaged><<<p.num_splits, kThreads, L::kAlloc, stream>>>(p, maps);
+  } else {
+    CUtensorMap map;
+    e = make_kv_map(&map, p.kv, p.total_kv, kTileRows);
     if (e != cudaSuccess) return e;
+    stage1_tc_kernel<QF, kPaged><<<p.num_splits, kThreads, L::kAlloc, stream>>>(p, map);
   }
-  stage1_tc_kernel<QF><<<p.num_splits, kThreads, L::kAlloc, stream>>>(p, map);
   return cudaGetLastError();
 }
 
 }  // namespace tc
 
 cudaError_t launch_stage1_tc_fp8(int q_fmt, const Stage1Params& p, cudaStream_t stream) {
-  if (q_fmt == kQBf16Quant) return tc::launch_q<kQBf16Quant>(p, stream);
-  return q_fmt == kQBf16 ? tc::launch_q<kQBf16>(p, stream) : tc::launch_q<kQFp8>(p, stream);
+  if (p.paged) {
+    if (q_fmt == kQBf16Quant) return tc::launch_q<kQBf16Quant, true>(p, stream);
+    return q_fmt == kQBf16 ? tc::launch_q<kQBf16, true>(p, stream) : tc::launch_q<kQFp8, true>(p, stream);
+  }
+  if (q_fmt == kQBf16Quant) return tc::launch_q<kQBf16Quant, false>(p, stream);
+  return q_fmt == kQBf16 ? tc::launch_q<kQBf16, false>(p, stream) : tc::launch_q<kQFp8, false>(p, stream);
 }
 
 }  // namespace mla

@@ -59,7 +59,7 @@ __device__ __forceinline__ void mbar_wait_drain_tc(uint32_t bar, uint32_t parity
 
 // Walks the CTA's tiles in order (one 128-row tile at a time).
 struct TileRef {
-  int32_t row, seg, k0, nvalid;
+  int32_t row, seg, k0, nvalid, pbase;
 };
 
 struct TileWalker {
@@ -72,6 +72,17 @@ struct TileWalker {
     have = cur.next(pc);
     r0 = 0;
   }
+  // First KV row of the next tile. Returns false when done.
+  __device__ bool next(int32_t& row) {
+    if (!have) return false;
+    row = pc.kv_row + r0;
+    r0 += kTileRows;
+    if (r0 >= pc.nrows) {
+      have = cur.next(pc);
+      r0 = 0;
+    }
+    return true;
+  }
   // The next tile: its first KV row, segment, the segment's first row and
   // how many of its rows belong to the piece. Returns false when done.
   __device__ bool next(TileRef& t) {
@@ -80,6 +91,7 @@ struct TileWalker {
     t.seg = pc.seg;
     t.k0 = pc.k0;
     t.nvalid = pc.nrows - r0;
+    t.pbase = pc.pbase;
     r0 += kTileRows;
     if (r0 >= pc.nrows) {
       have = cur.next(pc);
@@ -89,18 +101,44 @@ struct TileWalker {
   }
 };
 
-// Paged KV: the physical row of row i of segment seg, or -1 (with the error
-// flag raised) when the page table names a page outside the pool. The page
-// table entry read is inside [page_indptr[seg], page_indptr[seg+1]) because
-// i is below the segment's row count.
-__device__ __forceinline__ int64_t paged_row(const Stage1Params& p, int32_t seg, int32_t i) {
-  const int32_t pg = i / p.page_size;
-  const int32_t id = __ldg(p.page_indices + __ldg(p.page_indptr + seg) + pg);
-  if (static_cast<uint32_t>(id) >= static_cast<uint32_t>(p.num_pages)) {
+// Paged KV, in two steps so that the page-table load is in flight while other
+// work proceeds. page_of issues the load of the page id of row i of the
+// segment whose first page-table entry is pbase (the entry read is inside
+// [page_indptr[seg], page_indptr[seg+1]) because i is below the segment's row
+// count); phys_row turns it into the
+// physical row, or -1: for a row outside the piece (page_of_none), and, with
+// the error flag raised, for a page id outside the pool.
+struct PagedRow {
+  int32_t id, slot;  // slot < 0: no row
+};
+
+__device__ __forceinline__ PagedRow page_of(const Stage1Params& p, int32_t pbase, int32_t i) {
+  const int32_t pg = p.page_shift >= 0 ? (i >> p.page_shift) : i / p.page_size;
+  return PagedRow{__ldg(p.page_indices + pbase + pg), i - pg * p.page_size};
+}
+
+__device__ __forceinline__ PagedRow page_of_none() { return PagedRow{0, -1}; }
+
+// (The pool holds fewer than 2^31 rows: the host checks num_pages * page_size.)
+__device__ __forceinline__ int32_t phys_row(const Stage1Params& p, PagedRow r) {
+  if (r.slot < 0) return -1;
+  if (static_cast<uint32_t>(r.id) >= static_cast<uint32_t>(p.num_pages)) {
     atomicOr(p.dev_flags, kFlagBadPage);
     return -1;
   }
-  return static_cast<int64_t>(id) * p.page_size + (i - pg * p.page_size);
+  return r.id * p.page_size + r.slot;
+}
+
+// The page ids of tile rows lane + 32 j (j = 0..3) of the next tile.
+__device__ __forceinline__ bool paged_tile_ids(const Stage1Params& p, TileWalker& tw, int lane, PagedRow (&id)[4]) {
+  TileRef t;
+  const bool have = tw.next(t);
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const int row = 32 * j + lane;
+    id[j] = (have && row < t.nvalid) ? page_of(p, t.pbase, t.row - t.k0 + row) : page_of_none();
+  }
+  return have;
 }
 
 // Per-tile bookkeeping of the UMMA issuer, packed in one word: bit 0 = first

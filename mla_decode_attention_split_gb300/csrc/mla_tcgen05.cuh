@@ -101,6 +101,12 @@ __device__ __forceinline__ void setmaxnreg_dec() {
 }
 
 // ---- tiled TMA load (2-D), completion through mbarrier tx bytes -----------
+// Brings a tensor map (a __grid_constant__ kernel parameter) into the TMA
+// unit's descriptor cache ahead of its first use.
+__device__ __forceinline__ void prefetch_tensormap(const CUtensorMap* map) {
+  asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
+}
+
 __device__ __forceinline__ void tma_load_2d(uint32_t dst_smem, const CUtensorMap* map, int32_t x, int32_t y,
                                             uint32_t bar, uint64_t policy) {
   asm volatile(
