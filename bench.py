@@ -19,6 +19,7 @@ same workload and metric, one bounded sample per step, on the host cores.
 from __future__ import annotations
 
 import argparse
+import dataclasses
 import datetime
 import hashlib
 import json
@@ -187,11 +188,14 @@ def time_workload(m, synth, torch, name, steps, warmup, flush_l2: bool, quantize
             "l2": "flushed (256 MB write) before each call" if flush_l2 else "back-to-back"}
 
 
-def time_paged_workload(m, synth, torch, name, page_size, steps, warmup, flush_l2: bool):
+def time_paged_workload(m, synth, torch, name, page_size, steps, warmup, flush_l2: bool, in_order: bool = False):
     """Per-call device time of a workload with its fp8 cache in pages of `page_size` rows,
-    scattered over the pool in random order (the page table built once, outside the timing)."""
+    scattered over the pool in random order, or in pool order (the pages' identity table)
+    when in_order. The page table is built once, outside the timing."""
     w = synth.WORKLOADS[name]
     pin = synth.make_paged_inputs(w, "cuda", kv_lens=synth.make_lengths(w), page_size=page_size)
+    if in_order:
+        pin = dataclasses.replace(pin, page_indices=torch.sort(pin.page_indices).values.contiguous())
     out = torch.empty((pin.total_q, 16, 512), dtype=torch.bfloat16, device="cuda")
     ws = m.alloc_paged_workspace(pin.batch, pin.total_q, pin.total_kv, synth.FP8_E4M3)
     flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device="cuda") if flush_l2 else None
@@ -211,7 +215,7 @@ def time_paged_workload(m, synth, torch, name, page_size, steps, warmup, flush_l
     us = statistics.median(tot)
     kvb = pin.total_kv * synth.D_QK  # the rows read (the pool's spare pages are not)
     return {"us_per_call": round(us, 2), "kv_gbs": round(kvb / (us * 1e-6) / 1e9, 1), "kv_bytes": kvb,
-            "page_size": page_size, "pages": pin.num_pages,
+            "page_size": page_size, "pages": pin.num_pages, "page_order": "pool order" if in_order else "random",
             "l2": "flushed (256 MB write) before each call" if flush_l2 else "back-to-back"}
 
 
@@ -444,10 +448,12 @@ def finish(args, line, rank, world, w, m, synth, torch, inp):
             table[qq] = {"cold": time_workload(m, synth, torch, "a8w8_bs64_kv1024", 30, 5, True, quantize_q=True),
                          "warm": time_workload(m, synth, torch, "a8w8_bs64_kv1024", 30, 5, False, quantize_q=True)}
             # the headline shape with the cache in pages scattered over a pool
-            for ps in (1, 16, 64):
-                key = f"fp8kv_bs256_kv8192+paged_ps{ps}"
-                table[key] = {"cold": time_paged_workload(m, synth, torch, "fp8kv_bs256_kv8192", ps, 30, 5, True),
-                              "warm": time_paged_workload(m, synth, torch, "fp8kv_bs256_kv8192", ps, 30, 5, False)}
+            for ps, in_order in ((1, True), (1, False), (16, False), (64, False)):
+                key = f"fp8kv_bs256_kv8192+paged_ps{ps}_{'in_order' if in_order else 'random'}"
+                table[key] = {"cold": time_paged_workload(m, synth, torch, "fp8kv_bs256_kv8192", ps, 30, 5, True,
+                                                          in_order),
+                              "warm": time_paged_workload(m, synth, torch, "fp8kv_bs256_kv8192", ps, 30, 5, False,
+                                                          in_order)}
             line["workloads"] = table
         if not args.no_cpu_baseline:
             import oracle

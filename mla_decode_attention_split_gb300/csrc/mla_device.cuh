@@ -93,6 +93,11 @@ __device__ __forceinline__ void bulk_g2s(uint32_t dst_smem, const void* src, uin
       : "memory");
 }
 
+// Brings the cache line holding addr into L2 (a hint: nothing is waited for).
+__device__ __forceinline__ void prefetch_l2(const void* addr) {
+  asm volatile("prefetch.global.L2 [%0];" ::"l"(addr));
+}
+
 // 16-byte asynchronous global -> shared copy (L1 bypassed) with an L2 policy.
 __device__ __forceinline__ void cp_async16(uint32_t dst_smem, const void* src, uint64_t policy) {
   asm volatile("cp.async.cg.shared.global.L2::cache_hint [%0], [%1], 16, %2;" ::"r"(dst_smem), "l"(src), "l"(policy)

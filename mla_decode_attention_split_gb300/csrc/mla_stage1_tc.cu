@@ -150,16 +150,16 @@ __device__ void producer(const Cx& cx, const CUtensorMap* map, PieceCursor cur, 
 }
 
 // Warp 0 with a paged cache. Rows of a tile that are consecutive rows of the
-// pool (a run inside one page, or
-// pages laid out in order) come in by TMA: each maximal run of whole 8-row
-// groups is one box per 128-byte chunk, 8 to 128 rows high (one tensor map per
-// height), landing in the same 128B-swizzled layout as the contiguous path's
-// 128-row boxes. The rows of the other groups are gathered with 16-byte
-// cp.async copies (lane l copies bytes 16l..16l+15 of each row) into that
-// layout; once they have landed every lane makes them visible to the tensor
-// core (async proxy) before the warp's arrival on kv_full. The page ids of
-// the next tile are loaded while the current tile is issued. Rows past the
-// piece, and rows whose page id is outside the pool, are not copied.
+// pool (a run inside one page, or pages laid out in order) come in by TMA:
+// each maximal run of whole 8-row groups is one box per 128-byte chunk, 8 to
+// 128 rows high (one tensor map per height), landing in the same
+// 128B-swizzled layout as the contiguous path's 128-row boxes. The rows of the
+// other groups are gathered with 16-byte cp.async copies (lane l copies bytes
+// 16l..16l+15 of each row) into that layout; once they have landed every lane
+// makes them visible to the tensor core (async proxy) before the warp's
+// arrival on kv_full. The page ids of a tile are loaded two tiles ahead and
+// its runs are worked out before its stage is free. Rows past the piece, and rows whose page id is
+// outside the pool, are not copied.
 struct PagedMaps {
   CUtensorMap box[16];  // box[h]: 128 bytes x 8 (h + 1) rows of the pool
 };
@@ -179,12 +179,10 @@ __device__ PagedDrain producer_paged(const Stage1Params& p, const Cx& cx, const 
   PagedRow id[4], id_next[4];  // page ids of this tile and the next (loaded two tiles ahead)
   bool have = paged_tile_ids(p, tw, lane, id);
   bool have_next = have && paged_tile_ids(p, tw, lane, id_next);
-  uint32_t issued = 0, tma_hist = 0, n_last = 0;
-  TC_PT_INIT
+  PagedDrain d{0u, 0u, 0u};
   for (uint32_t n = 0; have; ++n) {
     const uint32_t s = n % kStages, rnd = n / kStages;
-    if (rnd >= 1 && !cx.wait(L::kKvEmpty + s, (rnd - 1) & 1u)) break;
-    TC_PT(0);
+    // the tile's rows and runs are worked out before its stage is free
     int32_t phys[4];      // tile rows lane + 32 j
     uint32_t contig = 0;  // bit g: rows 8g..8g+7 are consecutive rows of the pool
     uint32_t linked = 0;  // bit g: row 8g follows row 8g-1 in the pool
@@ -204,32 +202,38 @@ __device__ PagedDrain producer_paged(const Stage1Params& p, const Cx& cx, const 
         if ((l >> (8 * q)) & 1u) linked |= 1u << (4 * j + q);
       }
     }
+    // runs: a contiguous group starts one unless it continues the previous
+    // contiguous group; lane g < 16 holds the first pool row and the length
+    // (in groups) of the run that starts at group g
+    const uint32_t starts = contig & ~((contig << 1) & linked);
+    int32_t run_y = 0, run_len = 0;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int32_t v = __shfl_sync(0xffffffffu, phys[j], (lane & 3) * 8);
+      if ((lane >> 2) == j) run_y = v;
+    }
+    if (lane < 16 && ((starts >> lane) & 1u)) {
+      run_len = 1;
+      while (lane + run_len < 16 && ((contig >> (lane + run_len)) & 1u) && ((linked >> (lane + run_len)) & 1u))
+        ++run_len;
+    }
+    if (rnd >= 1 && !cx.wait(L::kKvEmpty + s, (rnd - 1) & 1u)) break;
     const uint32_t bar = cx.bar(L::kKvFull + s);
     const uint32_t stage = cx.s + L::kOffKv + s * kStageBytes;
-    TC_PT(4);
     if (contig) {
       if (lane == 0) mbar_expect_tx(bar, static_cast<uint32_t>(__popc(contig)) * kVChunks * 1024u);
       __syncwarp();
-      // runs: a contiguous group starts one unless it continues the previous contiguous group
-      uint32_t starts = contig & ~((contig << 1) & linked);
-      while (starts) {
-        const int g0 = __ffs(starts) - 1;
-        starts &= starts - 1;
-        const uint32_t after = ~(contig >> g0);  // run = contiguous groups g0.. linked to their predecessor
-        int len = 1;
-        while (g0 + len < 16 && !((after >> len) & 1u) && ((linked >> (g0 + len)) & 1u)) ++len;
-        int32_t y = 0;
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          const int32_t v = __shfl_sync(0xffffffffu, phys[j], (g0 & 3) * 8);
-          if ((g0 >> 2) == j) y = v;
-        }
+      uint32_t left = starts;
+      while (left) {
+        const int g0 = __ffs(left) - 1;
+        left &= left - 1;
+        const int32_t y = __shfl_sync(0xffffffffu, run_y, g0);
+        const int32_t len = __shfl_sync(0xffffffffu, run_len, g0);
         if (lane < kVChunks)
           tma_load_2d(stage + lane * kChunkBytes + g0 * 1024, &maps->box[len - 1], lane * 128, y, bar, pol);
       }
     }
-    TC_PT(5);
-  if (contig != 0xFFFFu) {
+    if (contig != 0xFFFFu) {
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
 #pragma unroll 8
@@ -242,9 +246,7 @@ __device__ PagedDrain producer_paged(const Stage1Params& p, const Cx& cx, const 
         }
       }
       cp_async_commit();
-    }
-    TC_PT(1);
-    if (contig == 0xFFFFu) {  // all by TMA: the barrier completes when the boxes land
+    } else {  // all by TMA: the barrier completes when the boxes land
       __syncwarp();
       if (lane == 0) mbar_arrive(bar);
     }
@@ -252,19 +254,31 @@ __device__ PagedDrain producer_paged(const Stage1Params& p, const Cx& cx, const 
     for (int j = 0; j < 4; ++j) id[j] = id_next[j];
     have = have_next;
     have_next = have && paged_tile_ids(p, tw, lane, id_next);  // two tiles ahead
-    TC_PT(2);
     if (contig != 0xFFFFu) {
       cp_async_wait<0>();
       fence_async_smem();
       __syncwarp();
       if (lane == 0) mbar_arrive(bar);
     }
-    tma_hist = (tma_hist << 1) | (contig ? 1u : 0u);
-    ++issued;
-    n_last = n;
-    TC_PT(3);
+    d.tma_hist = (d.tma_hist << 1) | (contig ? 1u : 0u);
+    ++d.issued;
+    d.n_last = n;
   }
-  return PagedDrain{issued, tma_hist, n_last};
+  return d;
+}
+
+// Warp 6 with a paged cache: at the CTA's start, pulls the page-table entries of
+// all its pieces into L2 (one prefetch per 128-byte line, addresses inside each
+// piece's range of the table), so that the producer's and the softmax warps'
+// page-id loads, issued a tile or two ahead, do not wait on DRAM.
+__device__ void prefetch_page_ids(const Stage1Params& p, PieceCursor cur, int lane) {
+  Piece pc;
+  while (cur.next(pc)) {
+    const int32_t i0 = pc.kv_row - pc.k0, i1 = i0 + pc.nrows - 1;
+    const int32_t e0 = pc.pbase + (p.page_shift >= 0 ? i0 >> p.page_shift : i0 / p.page_size);
+    const int32_t e1 = pc.pbase + (p.page_shift >= 0 ? i1 >> p.page_shift : i1 / p.page_size);
+    for (int32_t e = (e0 & ~31) + 32 * lane; e <= e1; e += 32 * 32) prefetch_l2(p.page_indices + (e < e0 ? e0 : e));
+  }
 }
 
 // When the CTA stopped early (a bounded wait ran out) the consumer may not
@@ -624,6 +638,8 @@ __global__ void __launch_bounds__(kThreads, 1) stage1_tc_kernel(const Stage1Para
     __syncwarp();
   } else if (warp < 6) {
     softmax_role<QF, kPaged>(p, cx, cur, warp, lane);
+  } else if (warp == 6) {
+    if constexpr (kPaged) prefetch_page_ids(p, cur, lane);
   }
   if constexpr (kPaged) {
     __syncthreads();
