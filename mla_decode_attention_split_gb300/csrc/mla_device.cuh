@@ -93,6 +93,16 @@ __device__ __forceinline__ void bulk_g2s(uint32_t dst_smem, const void* src, uin
       : "memory");
 }
 
+// Programmatic dependent launch. A kernel launched with programmatic stream
+// serialization may start while the kernel before it in the stream still
+// runs; griddep_wait blocks until that kernel has completed and its writes are
+// visible (a no-op for a normal launch). griddep_launch_dependents lets the
+// next such kernel start early.
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void griddep_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // Brings the cache line holding addr into L2 (a hint: nothing is waited for).
 __device__ __forceinline__ void prefetch_l2(const void* addr) {
   asm volatile("prefetch.global.L2 [%0];" ::"l"(addr));

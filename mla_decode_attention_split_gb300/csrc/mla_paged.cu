@@ -28,6 +28,7 @@ __global__ void __launch_bounds__(kPrepThreads) mla_paged_prepare_kernel(const i
                                                                          int page_size, int32_t* __restrict__ kvp,
                                                                          uint32_t* flags) {
   __shared__ int64_t sh[kPrepThreads / 32 + 1];
+  griddep_launch_dependents();  // stage 1 may start; it waits for this grid before reading the offsets
   const int tid = threadIdx.x;
   const int per = (batch + kPrepThreads - 1) / kPrepThreads;
   const int lo = min(tid * per, batch), hi = min(lo + per, batch);

@@ -16,6 +16,7 @@ __global__ void __launch_bounds__(kAmaxThreads) mla_q_amax_kernel(const uint4* _
                                                                    uint32_t* hdr) {
   __shared__ uint32_t wmax[kAmaxThreads / 32];
   __shared__ bool last;
+  griddep_launch_dependents();  // stage 1 may start; it waits for this grid before reading the scale
   uint32_t m = 0;
   for (int64_t i = blockIdx.x * static_cast<int64_t>(kAmaxThreads) + threadIdx.x; i < n16;
        i += static_cast<int64_t>(gridDim.x) * kAmaxThreads) {
@@ -46,8 +47,10 @@ __global__ void __launch_bounds__(kAmaxThreads) mla_q_amax_kernel(const uint4* _
 
 cudaError_t launch_q_scale(const void* q, int64_t n, uint32_t* header, cudaStream_t stream) {
   const int64_t n16 = n / 8;  // 8 bf16 per 16 bytes; n = total_q x 16 x 576 is a multiple of 8
-  int64_t blocks = (n16 + kAmaxThreads * 8 - 1) / (kAmaxThreads * 8);
-  blocks = blocks < 1 ? 1 : (blocks > 1024 ? 1024 : blocks);
+  // one 16-byte load per thread up to 8 blocks per SM of a 152-SM part, so the
+  // loads are in flight together rather than one after another per thread
+  int64_t blocks = (n16 + kAmaxThreads - 1) / kAmaxThreads;
+  blocks = blocks < 1 ? 1 : (blocks > 1216 ? 1216 : blocks);
   mla_q_amax_kernel<<<static_cast<int>(blocks), kAmaxThreads, 0, stream>>>(static_cast<const uint4*>(q), n16, header);
   return cudaGetLastError();
 }

@@ -692,6 +692,29 @@ extern "C" int mla_debug_phase_cycles_tc(unsigned long long* host, int n, int re
 }
 #endif
 
+// The launch. When a small kernel of this call runs just before (the q amax,
+// or the paged row offsets), stage 1 is launched as its programmatic
+// dependent: its CTAs start their set-up and KV loads while that kernel
+// finishes, and wait for it only where they read what it writes.
+template <int QF, bool kPaged>
+static cudaError_t launch_after(const Stage1Params& p, cudaStream_t stream, const KvMaps<kPaged>& maps) {
+  if (!p.after_kernel) {
+    stage1_tc_kernel<QF, kPaged><<<p.num_splits, kThreads, L::kAlloc, stream>>>(p, maps);
+    return cudaGetLastError();
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(p.num_splits));
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = L::kAlloc;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, stage1_tc_kernel<QF, kPaged>, p, maps);
+}
+
 template <int QF, bool kPaged>
 static cudaError_t launch_q(const Stage1Params& p, cudaStream_t stream) {
   static int configured_device = -1;
@@ -720,14 +743,13 @@ static cudaError_t launch_q(const Stage1Params& p, cudaStream_t stream) {
       cached_kv = p.kv;
       cached_rows = rows;
     }
-    stage1_tc_kernel<QF, kPaged><<<p.num_splits, kThreads, L::kAlloc, stream>>>(p, maps);
+    return launch_after<QF, kPaged>(p, stream, maps);
   } else {
     CUtensorMap map;
     e = make_kv_map(&map, p.kv, p.total_kv, kTileRows);
     if (e != cudaSuccess) return e;
-    stage1_tc_kernel<QF, kPaged><<<p.num_splits, kThreads, L::kAlloc, stream>>>(p, map);
+    return launch_after<QF, kPaged>(p, stream, map);
   }
-  return cudaGetLastError();
 }
 
 }  // namespace tc

@@ -260,6 +260,20 @@ __device__ __forceinline__ bool group_sync(const Ctx<LL>& cx, SoftmaxCtx& sx) {
 // rows 0-15 = e4m3(q 2^shift), rows 16-31 = e4m3(16 (q 2^shift - hi))).
 // Returns the score scale (exp2 domain, times `kvsc`) or a negative value on
 // abort. Piece kk >= 1 waits until the previous piece's last Q.K^T is done.
+// x / s rounded to nearest even, from inv = RN(1 / s), by one residual
+// correction (Markstein's theorem; P. Markstein, "IA-64 and Elementary
+// Functions", 2000, ch. 8): with q0 = RN(x inv) and the exact residual
+// r = x - q0 s from an FMA, RN(q0 + r inv) is the correctly rounded quotient
+// when neither the quotient nor the residual leaves the normal range. Here
+// |x / s| <= 448 (s is the tensor's amax / 448); quotients below the normal
+// range are far under the smallest e4m3 subnormal, so their code is 0 either
+// way.
+__device__ __forceinline__ float quotient_rn(float x, float s, float inv) {
+  const float q0 = x * inv;
+  const float r = fmaf(-q0, s, x);
+  return fmaf(r, inv, q0);
+}
+
 template <class LL, int QF>
 __device__ float setup_q(const Stage1Params& p, const Ctx<LL>& cx, SoftmaxCtx& sx, int token, uint32_t kk, float kvsc) {
   if (kk >= 1 && !cx.wait(LL::kQEmpty, (kk - 1) & 1u)) return -1.f;
@@ -273,18 +287,25 @@ __device__ float setup_q(const Stage1Params& p, const Ctx<LL>& cx, SoftmaxCtx& s
   };
   float c;
   if (QF == kQBf16Quant) {
-    // e4m3 codes of q / s (RNE, saturated), lo rows zero; s from the workspace
+    // e4m3 codes of q / s (RNE, saturated), lo rows zero; s from the workspace,
+    // written by the amax kernel that may still run (programmatic launch)
+    if (kk == 0) griddep_wait();
     const uint16_t* src = static_cast<const uint16_t*>(p.q) + (static_cast<int64_t>(token) * kHeads + h) * kDqk + d0;
-    const float qs = __ldg(p.q_scale);
+    const float qs = *static_cast<const volatile float*>(p.q_scale);
+    const float inv = 1.0f / qs;  // correctly rounded, once
+    uint4 v[9];
+#pragma unroll
+    for (int i = 0; i < 9; ++i) v[i] = __ldg(reinterpret_cast<const uint4*>(src) + i);
 #pragma unroll
     for (int i = 0; i < 9; ++i) {
-      const uint4 v = __ldg(reinterpret_cast<const uint4*>(src) + i);
-      const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+      const uint32_t w[4] = {v[i].x, v[i].y, v[i].z, v[i].w};
       uint32_t code[2];
 #pragma unroll
       for (int k = 0; k < 2; ++k) {
-        const float a = bf16_bits_to_f32(w[2 * k] & 0xFFFFu) / qs, b = bf16_bits_to_f32(w[2 * k] >> 16) / qs;
-        const float e = bf16_bits_to_f32(w[2 * k + 1] & 0xFFFFu) / qs, f = bf16_bits_to_f32(w[2 * k + 1] >> 16) / qs;
+        const float a = quotient_rn(bf16_bits_to_f32(w[2 * k] & 0xFFFFu), qs, inv);
+        const float b = quotient_rn(bf16_bits_to_f32(w[2 * k] >> 16), qs, inv);
+        const float e = quotient_rn(bf16_bits_to_f32(w[2 * k + 1] & 0xFFFFu), qs, inv);
+        const float f = quotient_rn(bf16_bits_to_f32(w[2 * k + 1] >> 16), qs, inv);
         code[k] = f32x2_to_e4m3x2(a, b) | (f32x2_to_e4m3x2(e, f) << 16);
       }
       *qaddr(h, d0 + 8 * i) = code[0];
@@ -548,6 +569,9 @@ __device__ void merge_listed(const Stage1Params& p, const Ctx<LL>& cx) {
 template <class LL>
 __device__ __forceinline__ bool cta_begin(const Stage1Params& p, Ctx<LL>& cx, uint8_t* smem_raw, int alloc_warp,
                                           PieceCursor& cur) {
+  // a paged call's row offsets come from the kernel before this one, which may
+  // still run (programmatic launch)
+  if (p.paged) griddep_wait();
   const uint32_t raw = smem_addr(smem_raw);
   cx.s = (raw + 1023u) & ~1023u;
   cx.g = smem_raw + (cx.s - raw);

@@ -207,6 +207,56 @@ def test_in_call_q_quantisation_equals_caller_quantised_a8w8():
     check(ref.float().cpu().numpy(), oracle_ref(dataclasses.replace(inp, q=codes, q_scale=scale, q_dtype=synth.FP8_E4M3)))
 
 
+@pytest.mark.parametrize("amax_bits", [0x3F80, 0x3FFF, 0x42C9, 0x3B01])
+def test_in_call_q_quantisation_codes_over_every_mantissa(amax_bits):
+    # Every bf16 value within 13 binades below the tensor maximum (both signs) is
+    # quantised in the call and must get the code of the fp32 rule RNE(q / s).
+    # Each value sits at dim 0 of one (token, head); every segment holds two KV
+    # rows that differ only in dim 0, so the output of that head is a mix of the
+    # two V rows whose weight depends on that one code alone.
+    amax = torch.tensor([amax_bits], dtype=torch.int16).view(torch.bfloat16).float()
+    e = int(((amax_bits >> 7) & 0xFF))
+    vals = []
+    for be in range(e - 12, e + 1):
+        for mant in range(128):
+            bits = (be << 7) | mant
+            if bits <= amax_bits:
+                vals.append(bits)
+    bits = torch.tensor(vals + [b | 0x8000 for b in vals], dtype=torch.int32).to(torch.int16)
+    qv = bits.view(torch.bfloat16)
+    ntok = (qv.numel() + 15) // 16
+    qv = torch.cat([qv, torch.zeros(ntok * 16 - qv.numel(), dtype=torch.bfloat16)])
+    q = torch.zeros((ntok, 16, 576), dtype=torch.bfloat16)
+    q[:, :, 0] = qv.view(ntok, 16)
+    kvf = torch.zeros((2 * ntok, 576))
+    kvf[1::2, 0] = 3.0          # K differs in dim 0 only
+    kvf[0::2, 1:512] = -1.0     # V rows: -1 and +1 (dims 1..511)
+    kvf[1::2, 1:512] = 1.0
+    kv, kv_scale = synth.quantize_fp8_per_tensor(kvf)
+    qo = torch.arange(ntok + 1, dtype=torch.int32)
+    kvp = 2 * qo
+    inp = synth.Inputs(q=q.cuda(), q_scale=None, kv=kv.cuda(), kv_scale=kv_scale.cuda(), qo_indptr=qo.cuda(),
+                       kv_indptr=kvp.cuda(), q_dtype=synth.BF16, kv_dtype=synth.FP8_E4M3)
+    qd = q.double()
+    scale = (torch.clamp(qd.abs().max(), min=1e-12) / 448.0).float().reshape(1)
+    assert float(qd.abs().max()) == float(amax[0])
+    codes = (qd / scale.double()).float().clamp(-448.0, 448.0).to(torch.float8_e4m3fn).view(torch.uint8)
+    sm = 1.0 / float(amax[0])  # scores within +-3: the head's output moves with every code
+    ref = run_decode(dataclasses.replace(inp, q=codes.cuda(), q_scale=scale.cuda(), q_dtype=synth.FP8_E4M3),
+                     num_splits=7, sm_scale=sm)
+    out = torch.empty_like(ref)
+    ws = m.alloc_workspace(inp.batch, inp.total_q, inp.total_kv, inp.kv_dtype, num_splits=7)
+    m.decode(inp.q, inp.kv, inp.kv_scale, inp.qo_indptr, inp.kv_indptr, out, inp.kv_dtype, workspace=ws,
+             num_splits=7, sm_scale=sm, quantize_q=True)
+    torch.cuda.synchronize()
+    assert m.device_error(ws)[0] == m.MLA_OK
+    # the mix weight moves with the code: distinct codes give distinct outputs
+    o = ref[:, :, 1].float().cpu().reshape(-1)[: len(vals) * 2]
+    c = codes[:, :, 0].reshape(-1)[: len(vals) * 2].int()
+    assert len(set(o.tolist())) >= 0.5 * len(set(c.tolist()))
+    assert torch.equal(out, ref)
+
+
 def test_bad_indptr_sets_device_flag_and_skips_work():
     w = synth.Workload("bad", 3, 1, 0, synth.BF16, synth.FP8_E4M3, seed=8)
     inp = synth.make_inputs(w, "cuda", kv_lens=[100, 100, 100])
