@@ -145,7 +145,7 @@ mla_status_t decode_impl(const void* q, const void* kv, const void* kv_scale, co
   p.page_indptr = pg ? pg->page_indptr : nullptr;
   p.page_indices = pg ? pg->page_indices : nullptr;
   p.page_size = pg ? pg->page_size : 0;
-  p.after_kernel = (pg || opts->quantize_q) ? 1 : 0;
+  p.wait_late = (!pg && opts->quantize_q) ? 1 : 0;
   p.page_shift = -1;
   for (int32_t sh = 0; sh < 31 && pg; ++sh)
     if ((int32_t{1} << sh) == pg->page_size) p.page_shift = sh;

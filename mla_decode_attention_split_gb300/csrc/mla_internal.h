@@ -44,7 +44,7 @@ struct Stage1Params {
   int32_t page_shift;  // log2(page_size) when it is a power of two, else -1
   int32_t num_pages;
   int32_t paged;
-  int32_t after_kernel;  // a kernel of this call runs just before stage 1 (launched as its dependent)
+  int32_t wait_late;  // the kernel just before is this call's q amax: wait for it only before reading the scale
 };
 
 // KV formats / query formats as template tags (values match mla_dtype_t).

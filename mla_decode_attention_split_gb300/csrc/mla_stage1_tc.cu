@@ -692,16 +692,13 @@ extern "C" int mla_debug_phase_cycles_tc(unsigned long long* host, int n, int re
 }
 #endif
 
-// The launch. When a small kernel of this call runs just before (the q amax,
-// or the paged row offsets), stage 1 is launched as its programmatic
-// dependent: its CTAs start their set-up and KV loads while that kernel
-// finishes, and wait for it only where they read what it writes.
+// The launch: a programmatic dependent of the kernel before it in the stream.
+// Its CTAs are placed and set up (barriers) while that kernel ends, and wait
+// for it before they read global memory (with in-call q quantisation, where
+// that kernel is the amax, they stream KV first and wait before reading the
+// scale).
 template <int QF, bool kPaged>
 static cudaError_t launch_after(const Stage1Params& p, cudaStream_t stream, const KvMaps<kPaged>& maps) {
-  if (!p.after_kernel) {
-    stage1_tc_kernel<QF, kPaged><<<p.num_splits, kThreads, L::kAlloc, stream>>>(p, maps);
-    return cudaGetLastError();
-  }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(p.num_splits));
   cfg.blockDim = dim3(kThreads);

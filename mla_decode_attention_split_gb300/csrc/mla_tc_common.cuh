@@ -569,9 +569,6 @@ __device__ void merge_listed(const Stage1Params& p, const Ctx<LL>& cx) {
 template <class LL>
 __device__ __forceinline__ bool cta_begin(const Stage1Params& p, Ctx<LL>& cx, uint8_t* smem_raw, int alloc_warp,
                                           PieceCursor& cur) {
-  // a paged call's row offsets come from the kernel before this one, which may
-  // still run (programmatic launch)
-  if (p.paged) griddep_wait();
   const uint32_t raw = smem_addr(smem_raw);
   cx.s = (raw + 1023u) & ~1023u;
   cx.g = smem_raw + (cx.s - raw);
@@ -584,6 +581,13 @@ __device__ __forceinline__ bool cta_begin(const Stage1Params& p, Ctx<LL>& cx, ui
     reinterpret_cast<MergeList*>(cx.g + LL::kOffMList)->n = 0u;
     fence_mbar_init();
   }
+  // Launched as a programmatic dependent, the CTA may start while the kernel
+  // before it in the stream still runs. Nothing in global memory is touched
+  // before that kernel has completed, except with in-call q quantisation:
+  // there the kernel before is this call's amax kernel, which writes only the
+  // scale, and the q set-up waits for it instead.
+  griddep_launch_dependents();
+  if (!p.wait_late) griddep_wait();
   const int64_t parts = p.num_splits, c = blockIdx.x;
   int64_t* sh = reinterpret_cast<int64_t*>(cx.g + LL::kOffScan);
   const SegLocate loc = block_locate<LL::kThreads, 1>(
