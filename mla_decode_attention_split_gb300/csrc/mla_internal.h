@@ -5,6 +5,8 @@
 #include <cstdint>
 #include <cuda_runtime.h>
 
+#include <utility>
+
 namespace mla {
 
 constexpr int kHeads = 16;
@@ -70,6 +72,26 @@ cudaError_t launch_paged_prepare(const int32_t* page_indptr, const int32_t* last
 // bytes after the decode workspace for the logical row offsets of a paged call
 inline size_t paged_extra_bytes(int64_t batch) { return static_cast<size_t>(((batch + 1) * 4 + 255) / 256) * 256; }
 
+
+// Launches a stage-1 kernel as a programmatic dependent of the kernel before it
+// in the stream (programmatic stream serialization): its CTAs may be placed
+// while that kernel ends; each waits (griddepcontrol.wait) before it touches
+// global memory that the kernel before may write.
+template <class... KArgs, class... Args>
+inline cudaError_t launch_dependent(void (*kernel)(KArgs...), int grid, int block, int smem, cudaStream_t stream,
+                                    Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(grid));
+  cfg.blockDim = dim3(static_cast<unsigned>(block));
+  cfg.dynamicSmemBytes = static_cast<size_t>(smem);
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
 
 inline size_t workspace_bytes_for(int64_t num_splits, int64_t total_q) {
   const int64_t slots = num_splits + total_q;

@@ -740,6 +740,10 @@ __global__ void __launch_bounds__(kThreads1, 1) mla_stage1_kernel(const Stage1Pa
     *cx.abort_word = 0u;
     fence_mbar_init();
   }
+  // launched as a programmatic dependent: wait for the kernel before in the
+  // stream before touching global memory
+  griddep_launch_dependents();
+  griddep_wait();
   const int64_t parts = p.num_splits, c = blockIdx.x;
   int64_t* sh = reinterpret_cast<int64_t*>(smem + S::kOffScan);
   const SegLocate loc = block_locate<kThreads1, 1>(
@@ -776,8 +780,7 @@ static cudaError_t launch_t(const Stage1Params& p, cudaStream_t stream) {
     if (e != cudaSuccess) return e;
     configured_device = dev;
   }
-  mla_stage1_kernel<KV, QF><<<p.num_splits, kThreads1, bytes, stream>>>(p);
-  return cudaGetLastError();
+  return launch_dependent(mla_stage1_kernel<KV, QF>, p.num_splits, kThreads1, bytes, stream, p);
 }
 
 #ifdef MLA_PHASE_TIMING

@@ -604,8 +604,7 @@ static cudaError_t launch_q(const Stage1Params& p, cudaStream_t stream) {
     if (e != cudaSuccess) return e;
     configured_device = dev;
   }
-  stage1_mx_kernel<QF><<<p.num_splits, kThreads, L::kAlloc, stream>>>(p);
-  return cudaGetLastError();
+  return launch_dependent(stage1_mx_kernel<QF>, p.num_splits, kThreads, L::kAlloc, stream, p);
 }
 
 }  // namespace mx

@@ -692,24 +692,12 @@ extern "C" int mla_debug_phase_cycles_tc(unsigned long long* host, int n, int re
 }
 #endif
 
-// The launch: a programmatic dependent of the kernel before it in the stream.
-// Its CTAs are placed and set up (barriers) while that kernel ends, and wait
-// for it before they read global memory (with in-call q quantisation, where
-// that kernel is the amax, they stream KV first and wait before reading the
-// scale).
+// The launch: a programmatic dependent of the kernel before it in the stream
+// (with in-call q quantisation that kernel is the amax: the CTAs stream KV
+// first and wait before reading the scale).
 template <int QF, bool kPaged>
 static cudaError_t launch_after(const Stage1Params& p, cudaStream_t stream, const KvMaps<kPaged>& maps) {
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(static_cast<unsigned>(p.num_splits));
-  cfg.blockDim = dim3(kThreads);
-  cfg.dynamicSmemBytes = L::kAlloc;
-  cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, stage1_tc_kernel<QF, kPaged>, p, maps);
+  return launch_dependent(stage1_tc_kernel<QF, kPaged>, p.num_splits, kThreads, L::kAlloc, stream, p, maps);
 }
 
 template <int QF, bool kPaged>
