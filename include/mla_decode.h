@@ -31,7 +31,17 @@
  *   - Calls that launch work are asynchronous: MLA_OK means "enqueued". A launch
  *     failure returns MLA_ERR_CUDA. No call synchronises unless documented.
  *   - The library allocates no device memory per call. It keeps only a cached
- *     per-device SM count and the kernels' shared-memory attributes.
+ *     per-device SM count, the kernels' shared-memory attributes and (per host
+ *     thread) the tensor maps of the last paged pool.
+ *   - Decode kernels are launched as programmatic dependents of the kernel
+ *     before them in `stream` (programmatic stream serialization): their CTAs
+ *     may be placed while that kernel ends, and they wait for it to complete
+ *     before reading or writing global memory. Stream order is kept as for a
+ *     normal launch. A kernel the caller launches after a decode call with the
+ *     same attribute must itself wait (griddepcontrol.wait /
+ *     cudaGridDependencySynchronize) before it reads `out`.
+ *   - Calls make no allocation or synchronisation inside, so they can be
+ *     captured into a CUDA graph.
  *   - No C++ exception crosses this interface.
  */
 #ifndef MLA_DECODE_H
