@@ -113,6 +113,16 @@ typedef struct {
                              (else MLA_ERR_UNSUPPORTED); adds one small launch
                              (the amax). The scale is kept in the workspace
                              header.                                            */
+  int32_t token_pairs;    /* nonzero: the query tokens of each segment are taken
+                             in pairs (the last one alone if q_len is odd) that
+                             share one pass over the segment's KV rows, for
+                             multi-token decode (q_len > 1). fp8 KV only (else
+                             MLA_ERR_UNSUPPORTED), not with a page table. The
+                             workspace must be sized by
+                             mla_decode_pairs_workspace_size(). Each token's
+                             arithmetic is unchanged: with num_splits = 1 the
+                             output equals that of the call without pairs bit
+                             for bit.                                           */
 } mla_decode_opts;
 
 /* Split planner (the pages choose the split count from batch size and KV
@@ -160,6 +170,13 @@ mla_status_t mla_decode_workspace_size(int32_t batch, int32_t total_q, int32_t t
 mla_status_t mla_decode(const void* q, const void* kv, const void* kv_scale,
                         const int32_t* qo_indptr, const int32_t* kv_indptr, void* out,
                         mla_dtype_t kv_dtype, const mla_decode_opts* opts, void* stream);
+
+/* Bytes of device workspace for a call with opts->token_pairs set: as
+ * mla_decode_workspace_size(), with 2 * num_splits + total_q partial slots
+ * (a piece of a token pair writes two partials). Host only. Errors as
+ * mla_decode_workspace_size().                                               */
+mla_status_t mla_decode_pairs_workspace_size(int32_t batch, int32_t total_q, int32_t total_kv,
+                                             mla_dtype_t kv_dtype, int32_t num_splits, size_t* bytes);
 
 /* Paged KV cache: the page-table form of kernelbot-amd-mixed-mla-753817, which
  * hands `kv_indices`, `kv_last_page_len` and `page_size` (1 there) to the

@@ -28,7 +28,7 @@ __device__ __forceinline__ void zero_empty_tokens(const Stage1Params& p) {
 
 // The merge of one token from global memory by kThreads threads: thread t
 // keeps a running-max merge of float4 elements t, t + kThreads, ... of the
-// 16 x 512 output; partial slots c + token, c = c0..c1, two per round trip.
+// 16 x 512 output; partial slots G c + token, c = c0..c1, two per round trip.
 // Partials come from L2 (other SMs wrote them), not L1.
 template <int kThreads>
 __device__ void merge_token_global(const Stage1Params& p, int token, int64_t c0, int64_t c1) {
@@ -42,7 +42,7 @@ __device__ void merge_token_global(const Stage1Params& p, int token, int64_t c0,
   }
   for (int64_t c = c0; c <= c1; c += 2) {
     const bool two = c + 1 <= c1;
-    const int64_t s0 = c + token, s1 = two ? s0 + 1 : s0;
+    const int64_t s0 = p.group * c + token, s1 = two ? s0 + p.group : s0;
     const float4* o0 = reinterpret_cast<const float4*>(p.part_o + s0 * kHeads * kDv);
     const float4* o1 = reinterpret_cast<const float4*>(p.part_o + s1 * kHeads * kDv);
     float4 v0[kF], v1[kF];

@@ -1,12 +1,19 @@
 // Even partition of all query-token x KV-row work over the stage-1 CTAs.
 //
-// Each query token t of segment b owns a run of "virtual rows", one per KV row
-// of its segment: token-major, segment order. The total is
-//   T = sum_b q_len_b * kv_len_b.
-// CTA c of P processes virtual rows [c*T/P, (c+1)*T/P). A run of one token
-// inside one CTA is a "piece"; its partial result goes to workspace slot
-// c + t (unique, since along the virtual-row axis each new piece increments c,
-// t or both). A token whose run lies inside a single CTA is written directly.
+// The query tokens of a segment are taken in groups of G (G = 1, or 2 when a
+// kernel shares one pass over the KV rows between two tokens; a segment's
+// last group may be smaller). Each group of segment b owns a run of "virtual
+// rows", one per KV row of its segment: group-major, segment order. The total
+// is
+//   T = sum_b ceil(q_len_b / G) * kv_len_b.
+// CTA c of P processes virtual rows [c*T/P, (c+1)*T/P). A run of one group
+// inside one CTA is a "piece"; the partial result of its token t goes to
+// workspace slot G c + t. Slots are unique: along the virtual-row axis a new
+// piece either moves to the next CTA (G c grows by G, at least the group's
+// token count) or to the next group (t grows by the previous group's token
+// count), so the slot ranges of successive pieces never overlap; there are
+// G P + total_q slots. A group whose run lies inside a single CTA is written
+// directly.
 //
 // Both kernels recompute T and locate their position with one block-wide scan
 // over the indptr arrays; the scan also validates them (monotone, first entry
@@ -67,9 +74,14 @@ __device__ __forceinline__ int64_t block_exclusive_scan_i64(int64_t v, int64_t* 
 // mode 1: locate the segment containing virtual row target(T) (target < T).
 // mode 2: locate the segment containing query token `token`.
 // All kThreads threads of the block must call this.
+// Virtual rows of a segment with q query tokens and kv KV rows, tokens in groups of g.
+__device__ __forceinline__ int64_t seg_vrows(int32_t q, int32_t kv, int32_t g) {
+  return static_cast<int64_t>((q + g - 1) / g) * static_cast<int64_t>(kv);
+}
+
 template <int kThreads, int kMode, class Target>
 __device__ SegLocate block_locate(const int32_t* __restrict__ qo, const int32_t* __restrict__ kvp, int batch,
-                                  int total_q, int total_kv, Target target, int token, int64_t* sh) {
+                                  int total_q, int total_kv, int group, Target target, int token, int64_t* sh) {
   const int tid = threadIdx.x;
   const int per = (batch + kThreads - 1) / kThreads;
   const int lo = min(tid * per, batch), hi = min(lo + per, batch);
@@ -79,7 +91,7 @@ __device__ SegLocate block_locate(const int32_t* __restrict__ qo, const int32_t*
     const int32_t q0 = __ldg(qo + b), q1 = __ldg(qo + b + 1);
     const int32_t k0 = __ldg(kvp + b), k1 = __ldg(kvp + b + 1);
     valid &= (q1 >= q0) & (k1 >= k0);
-    local += static_cast<int64_t>(q1 - q0) * static_cast<int64_t>(k1 - k0);
+    local += seg_vrows(q1 - q0, k1 - k0, group);
   }
   if (tid == 0) {
     valid &= (__ldg(qo) == 0) & (__ldg(kvp) == 0) & (__ldg(qo + batch) == total_q) &
@@ -100,8 +112,7 @@ __device__ SegLocate block_locate(const int32_t* __restrict__ qo, const int32_t*
       if (lo < hi && x >= excl && x < excl + local) {
         int64_t vs = excl;
         for (int b = lo; b < hi; ++b) {
-          const int64_t v = static_cast<int64_t>(__ldg(qo + b + 1) - __ldg(qo + b)) *
-                            static_cast<int64_t>(__ldg(kvp + b + 1) - __ldg(kvp + b));
+          const int64_t v = seg_vrows(__ldg(qo + b + 1) - __ldg(qo + b), __ldg(kvp + b + 1) - __ldg(kvp + b), group);
           if (x < vs + v) {
             res[0] = b;
             res[1] = vs;
@@ -120,7 +131,7 @@ __device__ SegLocate block_locate(const int32_t* __restrict__ qo, const int32_t*
             res[1] = vs;
             break;
           }
-          vs += static_cast<int64_t>(q1 - q0) * static_cast<int64_t>(__ldg(kvp + b + 1) - __ldg(kvp + b));
+          vs += seg_vrows(q1 - q0, __ldg(kvp + b + 1) - __ldg(kvp + b), group);
         }
       }
     }
@@ -135,12 +146,13 @@ __device__ SegLocate block_locate(const int32_t* __restrict__ qo, const int32_t*
 // Walks the pieces of one CTA's range in order. Every thread of the CTA runs
 // an identical cursor, so all roles see the same sequence of pieces.
 struct Piece {
-  int32_t token;      // query token index
+  int32_t token;      // first query token of the group
+  int32_t ntok;       // tokens in the group (1..G)
   int32_t kv_row;     // first absolute KV row of the piece
   int32_t nrows;      // rows in the piece (>= 1)
-  int32_t direct;     // the piece is the token's whole run: write the output
-  int64_t slot;       // partial slot (c + token) when not direct
-  int64_t tok_vs;     // virtual start of the token's whole run
+  int32_t direct;     // the piece is the group's whole run: write the output
+  int64_t slot;       // partial slot of the first token (G c + token; token i: + i) when not direct
+  int64_t tok_vs;     // virtual start of the group's whole run
   int32_t kvlen;      // its length (the segment's KV rows)
   int32_t seg;        // segment index
   int32_t k0;         // first KV row of the segment
@@ -162,13 +174,16 @@ struct PieceCursor {
   int32_t align8;
   // paged KV: page_indptr, read with the segment's other offsets (else null)
   const int32_t* pip;
+  // tokens per group (values below 1 count as 1)
+  int32_t group;
 
   __device__ __forceinline__ bool next(Piece& pc) {
+    const int32_t G = group > 1 ? group : 1;
     while (x < end && seg < batch) {
       const int32_t q0 = __ldg(qo + seg), q1 = __ldg(qo + seg + 1);
       const int32_t k0 = __ldg(kvp + seg), k1 = __ldg(kvp + seg + 1);
       const int64_t kvlen = k1 - k0;
-      const int64_t vlen = static_cast<int64_t>(q1 - q0) * kvlen;
+      const int64_t vlen = seg_vrows(q1 - q0, k1 - k0, G);
       if (x >= seg_vs + vlen) {  // past this segment (or it is empty)
         seg_vs += vlen;
         ++seg;
@@ -179,12 +194,13 @@ struct PieceCursor {
       const int64_t row_in = x - tok_vs;
       const int64_t stop = min(end, tok_vs + kvlen);
       const int32_t lead = align8 ? static_cast<int32_t>(row_in & 7) : 0;
-      pc.token = static_cast<int32_t>(q0 + ti);
+      pc.token = static_cast<int32_t>(q0 + G * ti);
+      pc.ntok = min(G, q1 - pc.token);
       pc.kv_row = static_cast<int32_t>(k0 + row_in) - lead;
       pc.nrows = static_cast<int32_t>(stop - x) + lead;
       pc.lead = lead;
       pc.direct = (row_in == 0 && stop == tok_vs + kvlen) ? 1 : 0;
-      pc.slot = cta + pc.token;
+      pc.slot = G * cta + pc.token;
       pc.tok_vs = tok_vs;
       pc.kvlen = static_cast<int32_t>(kvlen);
       pc.seg = seg;

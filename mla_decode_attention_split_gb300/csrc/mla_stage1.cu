@@ -747,7 +747,7 @@ __global__ void __launch_bounds__(kThreads1, 1) mla_stage1_kernel(const Stage1Pa
   const int64_t parts = p.num_splits, c = blockIdx.x;
   int64_t* sh = reinterpret_cast<int64_t*>(smem + S::kOffScan);
   const SegLocate loc = block_locate<kThreads1, 1>(
-      p.qo_indptr, p.kv_indptr, p.batch, p.total_q, p.total_kv,
+      p.qo_indptr, p.kv_indptr, p.batch, p.total_q, p.total_kv, p.group,
       [=](int64_t total) { return part_start(c, total, parts); }, 0, sh);
   if (!loc.ok) {
     if (threadIdx.x == 0) atomicOr(p.dev_flags, kFlagBadIndptr);
@@ -758,6 +758,7 @@ __global__ void __launch_bounds__(kThreads1, 1) mla_stage1_kernel(const Stage1Pa
   const int64_t x0 = part_start(c, loc.total, parts), x1 = part_start(c + 1, loc.total, parts);
   if (x0 >= x1 || loc.seg < 0) return;
   PieceCursor cur{p.qo_indptr, p.kv_indptr, p.batch, x0, x1, loc.seg, loc.seg_vs, c};
+  cur.group = p.group;
   if (warp < 4)
     score_role<KV, QF>(p, cx, cur, warp, lane);
   else

@@ -57,8 +57,8 @@ struct L {
   static constexpr int kOffRedMu = kOffRedMax + 2 * 4 * 16 * 4;      // [2][4][16] f32
   static constexpr int kOffRedL = kOffRedMu + 2 * 4 * 16 * 4;        // [4][16] f32
   static constexpr int kOffAmax = kOffRedL + 4 * 16 * 4;             // [4] u32
-  static constexpr int kOffMList = kOffAmax + 16;                    // MergeList (32 B)
-  static constexpr int kOffScan = kOffMList + 32;                    // 16 x i64
+  static constexpr int kOffMList = kOffAmax + 16;                    // MergeList (64 B)
+  static constexpr int kOffScan = kOffMList + 64;                    // 16 x i64
   static constexpr int kOffMeta = kOffScan + 16 * 8;                 // [4] u32: bookkeeping of tile i in slot i % 4
   static constexpr int kOffRaw = kOffMeta + 16;                  // [4 warps][32 rows][288 B] fp4x2
   static constexpr int kOffRawSc = kOffRaw + 4 * 32 * (kDqk / 2);    // [4 warps][32 rows][18 B] e8m0

@@ -57,8 +57,8 @@ struct L {
   static constexpr int kOffRedMax = kOffP + kPBytes;              // [2][4][16] f32
   static constexpr int kOffRedL = kOffRedMax + 2 * 4 * 16 * 4;    // [4][16] f32
   static constexpr int kOffAmax = kOffRedL + 4 * 16 * 4;          // [4] u32
-  static constexpr int kOffMList = kOffAmax + 16;                 // MergeList (32 B)
-  static constexpr int kOffScan = kOffMList + 32;                 // 16 x i64
+  static constexpr int kOffMList = kOffAmax + 16;                 // MergeList (64 B)
+  static constexpr int kOffScan = kOffMList + 64;                 // 16 x i64
   static constexpr int kOffBars = kOffScan + 16 * 8;
   enum {
     kKvFull = 0, kKvEmpty = 3, kSFull = 6, kSEmpty = 8, kRopeFull = 10, kPFull = 11, kPEmpty = 12, kQFull = 13,
@@ -666,7 +666,7 @@ static EncodeFn encode_fn() {
 
 // box_rows = 128 (a whole tile) for a contiguous cache; 8, 16, .., 128 for the
 // pool of a paged one.
-static cudaError_t make_kv_map(CUtensorMap* map, const void* kv, int64_t total_kv, uint32_t box_rows) {
+cudaError_t make_kv_map(CUtensorMap* map, const void* kv, int64_t total_kv, uint32_t box_rows) {
   EncodeFn fn = encode_fn();
   if (!fn) return cudaErrorNotSupported;
   const cuuint64_t dims[2] = {static_cast<cuuint64_t>(kDqk), static_cast<cuuint64_t>(total_kv)};

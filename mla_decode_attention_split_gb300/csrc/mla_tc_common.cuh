@@ -274,15 +274,18 @@ __device__ __forceinline__ float quotient_rn(float x, float s, float inv) {
   return fmaf(r, inv, q0);
 }
 
-template <class LL, int QF>
-__device__ float setup_q(const Stage1Params& p, const Ctx<LL>& cx, SoftmaxCtx& sx, int token, uint32_t kk, float kvsc) {
-  if (kk >= 1 && !cx.wait(LL::kQEmpty, (kk - 1) & 1u)) return -1.f;
+// q of one token into rows row0..row0+31 of the Q buffer (chunks of
+// kChunk bytes); returns the score scale or a negative value on abort.
+template <class LL, int QF, int kChunk>
+__device__ float fill_q(const Stage1Params& p, const Ctx<LL>& cx, SoftmaxCtx& sx, int token, int row0, uint32_t kk,
+                        float kvsc) {
   const int t = 32 * sx.wi + sx.lane;  // 0..127
   const int h = t >> 3, d0 = 72 * (t & 7);
   uint8_t* qb = cx.g + LL::kOffQ;
-  auto qaddr = [&](int row, int d) -> uint32_t* {
+  auto qaddr = [&](int r, int d) -> uint32_t* {
+    const int row = row0 + r;
     const int unit = (d & 127) >> 4;
-    return reinterpret_cast<uint32_t*>(qb + (d >> 7) * kQChunkBytes + (row >> 3) * 1024 + (row & 7) * 128 +
+    return reinterpret_cast<uint32_t*>(qb + (d >> 7) * kChunk + (row >> 3) * 1024 + (row & 7) * 128 +
                                        ((unit ^ (row & 7)) << 4) + (d & 15));
   };
   float c;
@@ -328,7 +331,8 @@ __device__ float setup_q(const Stage1Params& p, const Ctx<LL>& cx, SoftmaxCtx& s
     mx = max(mx & 0xFFFFu, mx >> 16);
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-    uint32_t* am = reinterpret_cast<uint32_t*>(cx.g + LL::kOffAmax);
+    // per-warp maxima; rows 32.. of a two-token Q buffer use their own four words
+    uint32_t* am = reinterpret_cast<uint32_t*>(cx.g + LL::kOffAmax) + 4 * (row0 >> 5);
     if (sx.lane == 0) am[sx.wi] = mx;
     if (!group_sync(cx, sx)) return -1.f;
     mx = max(max(am[0], am[1]), max(am[2], am[3]));
@@ -361,6 +365,14 @@ __device__ float setup_q(const Stage1Params& p, const Ctx<LL>& cx, SoftmaxCtx& s
     }
     c = p.sm_scale * kLog2e * kvsc * __ldg(p.q_scale);
   }
+  return c;
+}
+
+// q of one token -> the Q buffer, handed to the MMA warp (see fill_q).
+template <class LL, int QF>
+__device__ float setup_q(const Stage1Params& p, const Ctx<LL>& cx, SoftmaxCtx& sx, int token, uint32_t kk, float kvsc) {
+  if (kk >= 1 && !cx.wait(LL::kQEmpty, (kk - 1) & 1u)) return -1.f;
+  const float c = fill_q<LL, QF, kQChunkBytes>(p, cx, sx, token, 0, kk, kvsc);
   fence_async_smem();
   __syncwarp();
   if (sx.lane == 0) mbar_arrive(cx.bar(LL::kQFull));
@@ -452,14 +464,16 @@ __device__ __forceinline__ void store_o(const Stage1Params& p, const Piece& pc, 
 // Merge of split tokens (the pages' stage 2). The CTA whose partial completes a
 // token's count merges it, at the very end of the CTA when its stage buffers
 // are free: with L = max_s lse_s, out = sum_s 2^(lse_s - L) O_s /
-// sum_s 2^(lse_s - L) over the partial slots c + token of the CTAs c0..c1 that
+// sum_s 2^(lse_s - L) over the partial slots G c + token of the CTAs c0..c1 that
 // hold pieces of the token. A CTA holds at most two split pieces (the first
-// and the last of its range), so it merges at most two tokens.
+// and the last of its range) of at most two tokens each, so it merges at most
+// four tokens.
 struct MergeList {
-  uint32_t n;                      // tokens this CTA merges (at most 2)
-  int32_t token[2], c0[2], c1[2];  // token and the CTAs that hold its pieces
-  uint32_t pad;
+  uint32_t n;                      // tokens this CTA merges (at most 4)
+  int32_t token[4], c0[4], c1[4];  // token and the CTAs that hold its pieces
+  uint32_t pad[3];
 };
+static_assert(sizeof(MergeList) == 64, "merge list slot");
 
 // After the 128 softmax threads wrote this CTA's partial of a split token:
 // publish it and count it on the token's counter; if it completes the count,
@@ -474,13 +488,15 @@ __device__ __forceinline__ bool finish_partial(const Stage1Params& p, const Ctx<
     __threadfence();
     const int64_t P = p.num_splits;
     const int64_t c0 = part_of_row(pc.tok_vs, cx.total, P), c1 = part_of_row(pc.tok_vs + pc.kvlen - 1, cx.total, P);
-    const uint32_t arrived = atomicAdd(p.tok_cnt + pc.token, 1u) + 1u;
     MergeList* ml = reinterpret_cast<MergeList*>(cx.g + LL::kOffMList);
-    if (arrived == static_cast<uint32_t>(c1 - c0 + 1) && ml->n < 2) {
-      ml->token[ml->n] = pc.token;
-      ml->c0[ml->n] = static_cast<int32_t>(c0);
-      ml->c1[ml->n] = static_cast<int32_t>(c1);
-      ++ml->n;
+    for (int i = 0; i < pc.ntok; ++i) {  // every token of the group
+      const uint32_t arrived = atomicAdd(p.tok_cnt + pc.token + i, 1u) + 1u;
+      if (arrived == static_cast<uint32_t>(c1 - c0 + 1) && ml->n < 4) {
+        ml->token[ml->n] = pc.token + i;
+        ml->c0[ml->n] = static_cast<int32_t>(c0);
+        ml->c1[ml->n] = static_cast<int32_t>(c1);
+        ++ml->n;
+      }
     }
   }
   return true;
@@ -516,7 +532,7 @@ __device__ void merge_listed(const Stage1Params& p, const Ctx<LL>& cx) {
         asm volatile("fence.proxy.async.global;" ::: "memory");  // partials written through the generic proxy
         mbar_arrive_expect_tx(cx.bar(LL::kMerge), nb * (kSlotBytes + kHeads * 4));
         for (int j = 0; j < nb; ++j) {
-          const int64_t slot = c0 + s0 + j + token;
+          const int64_t slot = p.group * (c0 + s0 + j) + token;
           bulk_g2s(cx.s + LL::kOffKv + j * kSlotBytes, p.part_o + slot * kHeads * kDv, kSlotBytes, cx.bar(LL::kMerge),
                    policy_evict_first());
           bulk_g2s(cx.s + LL::kOffQ + j * kHeads * 4, p.part_lse + slot * kHeads, kHeads * 4, cx.bar(LL::kMerge),
@@ -591,7 +607,7 @@ __device__ __forceinline__ bool cta_begin(const Stage1Params& p, Ctx<LL>& cx, ui
   const int64_t parts = p.num_splits, c = blockIdx.x;
   int64_t* sh = reinterpret_cast<int64_t*>(cx.g + LL::kOffScan);
   const SegLocate loc = block_locate<LL::kThreads, 1>(
-      p.qo_indptr, p.kv_indptr, p.batch, p.total_q, p.total_kv,
+      p.qo_indptr, p.kv_indptr, p.batch, p.total_q, p.total_kv, p.group,
       [=](int64_t total) { return part_start(c, total, parts); }, 0, sh);
   if (!loc.ok) {
     if (threadIdx.x == 0) atomicOr(p.dev_flags, kFlagBadIndptr);
@@ -608,6 +624,7 @@ __device__ __forceinline__ bool cta_begin(const Stage1Params& p, Ctx<LL>& cx, ui
   tc_fence_after();
   cx.tmem = *reinterpret_cast<volatile uint32_t*>(cx.g + LL::kOffSlot);
   cur = PieceCursor{p.qo_indptr, p.kv_indptr, p.batch, x0, x1, loc.seg, loc.seg_vs, c};
+  cur.group = p.group;
   return true;
 }
 
@@ -621,6 +638,10 @@ __device__ __forceinline__ void cta_end(const Stage1Params& p, const Ctx<LL>& cx
   }
   if (!*cx.abort_word) merge_listed(p, cx);
 }
+
+// Host: the tensor map of a KV cache of `rows` rows of 576 bytes, boxes of
+// 128 bytes x box_rows rows, 128B swizzle (defined in mla_stage1_tc.cu).
+cudaError_t make_kv_map(CUtensorMap* map, const void* kv, int64_t rows, uint32_t box_rows);
 
 }  // namespace tc
 }  // namespace mla
