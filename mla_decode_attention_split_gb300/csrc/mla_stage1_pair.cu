@@ -17,7 +17,12 @@
 //    which hides the TMA latency with one stage in flight), a 40 KB Q buffer,
 //    the 8 KB rope slot and an 8 KB P buffer;
 //  * a segment with an odd token count ends with a one-token group, which
-//    loads that token into both halves and writes only the first.
+//    loads that token into both halves and writes only the first;
+//  * with fp8 q (a8w8, or q quantised in the call) q has no lo rows, so the
+//    two tokens' codes fill one 32-row Q buffer (Q.K^T at N = 32) and the
+//    rope operand moves into tensor memory (A read from TMEM): that frees
+//    room for a third 64 KB stage, which the two-stage ring lacks (its MMA
+//    waits for KV at every tile).
 // A token's arithmetic (tiles, maxima, weights, accumulation) is the same as
 // in the single-token kernel, so with one partition per segment both give the
 // same bits.
@@ -31,20 +36,25 @@ namespace tc {
 namespace pair {
 
 constexpr int kThreads = 256;  // warp 0 TMA, warp 1 MMA, warps 2-5 softmax, 6-7 only in the merge
-constexpr int kStages = 2;
 constexpr int kStageBytes = kVBytes;
-constexpr int kQChunk = 64 * 128;   // 64 B-operand rows x 128 B
-constexpr int kQBytes2 = 5 * kQChunk;
 constexpr int kPBytes2 = kTileRows * 64;  // [row group][A hi | A lo | B hi | B lo][8 rows][16 heads]
-constexpr uint32_t kTmemS2 = 0;     // 2 buffers x 64 columns
-constexpr uint32_t kTmemO2 = 128;   // 4 blocks x 64 columns
 
-struct L {
+// kQ8 false: bf16 q, Q = 64 rows (both tokens hi + lo), two stages, rope in
+// the shared-memory slot. kQ8 true: fp8 q, Q = 32 rows (both tokens' codes),
+// three stages, rope in tensor memory.
+template <bool kQ8>
+struct LT {
   static constexpr int kThreads = pair::kThreads;
+  static constexpr int kStages = kQ8 ? 3 : 2;
+  static constexpr int kQRows = kQ8 ? 32 : 64;
+  static constexpr int kQChunk = kQRows * 128;
+  static constexpr uint32_t kSCols = kQRows;           // S columns per buffer (Q.K^T N)
+  static constexpr uint32_t kTmemO = 2 * kSCols;       // O: 4 blocks x 64 columns
+  static constexpr uint32_t kTmemRope = kTmemO + 256;  // rope operand, 16 columns (kQ8)
   static constexpr int kOffKv = 0;
   static constexpr int kOffQ = kOffKv + kStages * kStageBytes;
-  static constexpr int kOffRope = kOffQ + kQBytes2;
-  static constexpr int kOffP = kOffRope + kRopeBytes;
+  static constexpr int kOffRope = kOffQ + 5 * kQChunk;
+  static constexpr int kOffP = kOffRope + (kQ8 ? 0 : kRopeBytes);
   static constexpr int kOffRedMax = kOffP + kPBytes2;                // [2 buffers][2 tokens][4 warps][16] f32
   static constexpr int kOffRedL = kOffRedMax + 2 * 2 * 4 * 16 * 4;   // [2 tokens][4][16] f32
   static constexpr int kOffAmax = kOffRedL + 2 * 4 * 16 * 4;         // [2 tokens][4 warps] u32
@@ -52,8 +62,8 @@ struct L {
   static constexpr int kOffScan = kOffMList + 64;                    // 16 x i64
   static constexpr int kOffBars = kOffScan + 16 * 8;
   enum {
-    kKvFull = 0, kKvEmpty = 2, kSFull = 4, kSEmpty = 6, kRopeFull = 8, kPFull = 9, kPEmpty = 10, kQFull = 11,
-    kQEmpty = 12, kOFull = 13, kOEmpty = 14, kGrp = 15, kDrain = 17, kMerge = 18, kNumBars = 19
+    kKvFull = 0, kKvEmpty = 3, kSFull = 6, kSEmpty = 8, kRopeFull = 10, kPFull = 11, kPEmpty = 12, kQFull = 13,
+    kQEmpty = 14, kOFull = 15, kOEmpty = 16, kGrp = 17, kDrain = 19, kMerge = 20, kNumBars = 21
   };
   static constexpr int kMergeBytes = kStages * kStageBytes;  // the stages hold partials for the end-of-CTA merge
   static constexpr int kOffSlot = kOffBars + kNumBars * 8;
@@ -81,11 +91,14 @@ struct L {
     mbar_init(cx.bar(kDrain), 1);
   }
 };
-static_assert(L::kAlloc <= 227 * 1024, "shared memory budget");
-static_assert(L::kOffQ % 1024 == 0 && L::kOffRope % 1024 == 0 && L::kOffP % 1024 == 0, "operand alignment");
-static_assert(L::kOffRedMax % 16 == 0 && L::kOffRedL % 16 == 0 && L::kOffScan % 8 == 0, "scratch alignment");
-static_assert(kTmemO2 + 4 * 64 <= kTmemCols, "tensor memory");
-using Cx = Ctx<L>;
+template <bool kQ8>
+using CxT = Ctx<LT<kQ8>>;
+static_assert(LT<false>::kAlloc <= 227 * 1024 && LT<true>::kAlloc <= 227 * 1024, "shared memory budget");
+static_assert(LT<false>::kOffQ % 1024 == 0 && LT<false>::kOffRope % 1024 == 0 && LT<false>::kOffP % 1024 == 0 &&
+                  LT<true>::kOffQ % 1024 == 0 && LT<true>::kOffP % 1024 == 0,
+              "operand alignment");
+static_assert(LT<false>::kOffScan % 8 == 0 && LT<true>::kOffScan % 8 == 0, "scratch alignment");
+static_assert(LT<false>::kTmemO + 256 <= kTmemCols && LT<true>::kTmemRope + 16 <= kTmemCols, "tensor memory");
 
 // Optional phase timers (build with -DMLA_PHASE_TIMING): cycles per CTA, warp
 // and phase, summed over the launch. Off by default.
@@ -108,10 +121,11 @@ __device__ unsigned long long g_pair_phase[kPhaseCtas * 8 * 8];
   } while (0)
 #endif
 
-// B operands with N = 64.
-//   Q.K^T k-step ks: the 64 Q rows of chunk ks / 4 (K-major, 128B swizzle).
+// B operands.
+//   Q.K^T k-step ks: the Q rows of chunk ks / 4 (K-major, 128B swizzle).
+template <bool kQ8>
 __device__ __forceinline__ uint64_t qk_desc_b2(uint32_t qbuf, int ks) {
-  return smem_desc(qbuf + (ks >> 2) * kQChunk + (ks & 3) * 32, 16, 1024, kLayoutSw128);
+  return smem_desc(qbuf + (ks >> 2) * LT<kQ8>::kQChunk + (ks & 3) * 32, 16, 1024, kLayoutSw128);
 }
 //   P.V k-step ks (32 rows): P^T, 4 N-blocks of 16 columns 128 B apart, 8-row
 //   groups 512 B apart.
@@ -120,8 +134,11 @@ __device__ __forceinline__ uint64_t pv_desc_b2(uint32_t pbuf, int ks) {
 }
 
 // Warp 0: the V dims of each tile, four 128-row x 128-byte boxes, into stage
-// (tile % 2) once the tile two back has been released by its P.V.
-__device__ void producer(const Cx& cx, const CUtensorMap* map, PieceCursor cur, int lane) {
+// (tile % stages) once the tile that used it last has been released by its P.V.
+template <bool kQ8>
+__device__ void producer(const CxT<kQ8>& cx, const CUtensorMap* map, PieceCursor cur, int lane) {
+  using L = LT<kQ8>;
+  constexpr int kStages = L::kStages;
   const uint64_t pol = policy_evict_first();
   Piece pc;
   uint32_t n = 0;
@@ -161,7 +178,10 @@ struct PendingPV {
   bool first, last, valid;
 };
 
-__device__ bool issue_pv(const Cx& cx, const PendingPV& t) {
+template <bool kQ8>
+__device__ bool issue_pv(const CxT<kQ8>& cx, const PendingPV& t) {
+  using L = LT<kQ8>;
+  constexpr int kStages = L::kStages;
   constexpr uint32_t id_pv = umma_idesc(128, 64, 0, 0, true, true);
   PR_PT_INIT
   if (!cx.wait(L::kPFull, t.n & 1u)) return false;
@@ -174,7 +194,7 @@ __device__ bool issue_pv(const Cx& cx, const PendingPV& t) {
   for (int mb = 0; mb < 4; ++mb)
 #pragma unroll
     for (int ks = 0; ks < 4; ++ks)
-      umma_e4m3(cx.tmem + kTmemO2 + 64 * mb, pv_desc_a(stage, mb, ks), pv_desc_b2(pbuf, ks), id_pv,
+      umma_e4m3(cx.tmem + L::kTmemO + 64 * mb, pv_desc_a(stage, mb, ks), pv_desc_b2(pbuf, ks), id_pv,
                 (ks > 0 || !t.first) ? 1u : 0u);
   umma_commit(cx.bar(L::kKvEmpty + (t.n % kStages)));
   umma_commit(cx.bar(L::kPEmpty));
@@ -183,8 +203,11 @@ __device__ bool issue_pv(const Cx& cx, const PendingPV& t) {
   return true;
 }
 
-__device__ void mma_issuer(const Cx& cx, PieceCursor cur) {
-  constexpr uint32_t id_qk = umma_idesc(128, 64, 0, 0, false, false);
+template <bool kQ8>
+__device__ void mma_issuer(const CxT<kQ8>& cx, PieceCursor cur) {
+  using L = LT<kQ8>;
+  constexpr int kStages = L::kStages;
+  constexpr uint32_t id_qk = umma_idesc(128, L::kSCols, 0, 0, false, false);
   Piece pc;
   uint32_t n = 0, k = 0;
   PendingPV pend{0, 0, false, false, false};
@@ -207,18 +230,22 @@ __device__ void mma_issuer(const Cx& cx, PieceCursor cur) {
       PR_PT(2);
       tc_fence_after();
       const uint32_t stage = cx.s + L::kOffKv + st * kStageBytes;
+      const uint32_t sbuf = cx.tmem + L::kSCols * s;
 #pragma unroll
       for (int ks = 0; ks < 16; ++ks)  // the 512 V dims, from the stage
-        umma_e4m3(cx.tmem + kTmemS2 + 64 * s, qk_desc_a(stage, ks), qk_desc_b2(qbuf, ks), id_qk, ks > 0 ? 1u : 0u);
+        umma_e4m3(sbuf, qk_desc_a(stage, ks), qk_desc_b2<kQ8>(qbuf, ks), id_qk, ks > 0 ? 1u : 0u);
 #pragma unroll
-      for (int ks = 0; ks < 2; ++ks)  // the 64 rope dims, from the rope slot
-        umma_e4m3(cx.tmem + kTmemS2 + 64 * s, rope_desc_a(cx.s + L::kOffRope, ks), qk_desc_b2(qbuf, 16 + ks), id_qk,
-                  1u);
+      for (int ks = 0; ks < 2; ++ks) {  // the 64 rope dims, from tensor memory or the rope slot
+        if constexpr (kQ8)
+          umma_e4m3_ta(sbuf, cx.tmem + L::kTmemRope + 8 * ks, qk_desc_b2<kQ8>(qbuf, 16 + ks), id_qk, 1u);
+        else
+          umma_e4m3(sbuf, rope_desc_a(cx.s + L::kOffRope, ks), qk_desc_b2<kQ8>(qbuf, 16 + ks), id_qk, 1u);
+      }
       umma_commit(cx.bar(L::kSFull + s));
       const bool last = r0 + kTileRows >= pc.nrows;
       if (last) umma_commit(cx.bar(L::kQEmpty));
       PR_PT(3);
-      if (pend.valid && !issue_pv(cx, pend)) {
+      if (pend.valid && !issue_pv<kQ8>(cx, pend)) {
         ok = false;
         break;
       }
@@ -227,7 +254,7 @@ __device__ void mma_issuer(const Cx& cx, PieceCursor cur) {
     }
     ++k;
   }
-  if (ok && pend.valid) issue_pv(cx, pend);
+  if (ok && pend.valid) issue_pv<kQ8>(cx, pend);
   // every issued tcgen05 operation completes before tensor memory is freed
   umma_commit(cx.bar(L::kDrain));
   mbar_wait_drain_tc(cx.bar(L::kDrain), 0);
@@ -252,22 +279,36 @@ __device__ __forceinline__ void load_rope(const Stage1Params& p, TileWalker& rw,
   }
 }
 
-__device__ __forceinline__ void store_rope(const Cx& cx, const SoftmaxCtx& sx, const uint4 (&r)[4]) {
-  put_rope_row(cx.g + L::kOffRope, sx.row, r);
-  fence_async_smem();
+// One row's rope bytes into the rope operand (the shared-memory slot, or this
+// row's 16 tensor-memory columns) and the hand-off to the MMA warp.
+template <bool kQ8>
+__device__ __forceinline__ void store_rope(const CxT<kQ8>& cx, const SoftmaxCtx& sx, const uint4 (&r)[4]) {
+  using L = LT<kQ8>;
+  if constexpr (kQ8) {
+    const uint32_t w[16] = {r[0].x, r[0].y, r[0].z, r[0].w, r[1].x, r[1].y, r[1].z, r[1].w,
+                            r[2].x, r[2].y, r[2].z, r[2].w, r[3].x, r[3].y, r[3].z, r[3].w};
+    tmem_st16(cx.tmem + sx.lane_base + L::kTmemRope, w);
+    tmem_wait_st();
+    tc_fence_before();
+  } else {
+    put_rope_row(cx.g + L::kOffRope, sx.row, r);
+    fence_async_smem();
+  }
   __syncwarp();
   if (sx.lane == 0) mbar_arrive(cx.bar(L::kRopeFull));
 }
 
-// The q of a piece's tokens: token A into Q rows 0-31, token B into rows
-// 32-63 (a one-token group loads its token twice). Returns false on abort.
-template <int QF>
-__device__ bool setup_q2(const Stage1Params& p, const Cx& cx, SoftmaxCtx& sx, const Piece& pc, uint32_t kk,
+// The q of a piece's tokens: token A into Q rows 0-31 (fp8 q: 0-15), token B
+// into rows 32-63 (fp8 q: 16-31); a one-token group loads its token twice.
+// Returns false on abort.
+template <bool kQ8, int QF>
+__device__ bool setup_q2(const Stage1Params& p, const CxT<kQ8>& cx, SoftmaxCtx& sx, const Piece& pc, uint32_t kk,
                          float kvsc, float& ca, float& cb) {
+  using L = LT<kQ8>;
   if (kk >= 1 && !cx.wait(L::kQEmpty, (kk - 1) & 1u)) return false;
-  ca = fill_q<L, QF, kQChunk>(p, cx, sx, pc.token, 0, kk, kvsc);
+  ca = fill_q<L, QF, L::kQChunk, !kQ8>(p, cx, sx, pc.token, 0, kk, kvsc);
   if (ca < 0.f) return false;
-  cb = fill_q<L, QF, kQChunk>(p, cx, sx, pc.token + (pc.ntok > 1 ? 1 : 0), 32, kk, kvsc);
+  cb = fill_q<L, QF, L::kQChunk, !kQ8>(p, cx, sx, pc.token + (pc.ntok > 1 ? 1 : 0), L::kQRows / 2, kk, kvsc);
   if (cb < 0.f) return false;
   fence_async_smem();
   __syncwarp();
@@ -358,8 +399,10 @@ __device__ __forceinline__ bool softmax_tok(const float* rm, const float (&x)[16
   return grew;
 }
 
-template <int QF>
-__device__ void softmax_role(const Stage1Params& p, const Cx& cx, PieceCursor cur, int warp, int lane) {
+template <int QF, bool kQ8>
+__device__ void softmax_role(const Stage1Params& p, const CxT<kQ8>& cx, PieceCursor cur, int warp, int lane) {
+  using L = LT<kQ8>;
+  constexpr int kStages = L::kStages;
   SoftmaxCtx sx;
   sx.lane = lane;
   sx.wi = warp - 2;
@@ -369,7 +412,7 @@ __device__ void softmax_role(const Stage1Params& p, const Cx& cx, PieceCursor cu
   const float kvsc = __ldg(static_cast<const float*>(p.kv_scale));
   float* red_max = reinterpret_cast<float*>(cx.g + L::kOffRedMax);
   float* red_l = reinterpret_cast<float*>(cx.g + L::kOffRedL);
-  const uint32_t obase = cx.tmem + sx.lane_base + kTmemO2;
+  const uint32_t obase = cx.tmem + sx.lane_base + L::kTmemO;
 
   PieceCursor ahead = cur;
   Piece pc, nxt;
@@ -381,10 +424,10 @@ __device__ void softmax_role(const Stage1Params& p, const Cx& cx, PieceCursor cu
   uint4 rb0[4], rb1[4];  // rope of the even / odd tile in flight
   load_rope(p, rw, sx.row, rb0);
   load_rope(p, rw, sx.row, rb1);
-  store_rope(cx, sx, rb0);
+  store_rope<kQ8>(cx, sx, rb0);
   load_rope(p, rw, sx.row, rb0);
   float ca, cb;
-  if (!setup_q2<QF>(p, cx, sx, pc, 0, kvsc, ca, cb)) return;
+  if (!setup_q2<kQ8, QF>(p, cx, sx, pc, 0, kvsc, ca, cb)) return;
   uint32_t n = 0, k = 0;
   int tiles_left = count_tiles(cur) - 1;  // tiles of the CTA after the current one (for the rope slot)
   PR_PT_INIT
@@ -405,10 +448,10 @@ __device__ void softmax_role(const Stage1Params& p, const Cx& cx, PieceCursor cu
       // Q.K^T(n) is done: the rope slot takes tile n+1, its registers tile n+3
       if (tiles_left > 0) {
         if (n & 1u) {
-          store_rope(cx, sx, rb0);
+          store_rope<kQ8>(cx, sx, rb0);
           load_rope(p, rw, sx.row, rb0);
         } else {
-          store_rope(cx, sx, rb1);
+          store_rope<kQ8>(cx, sx, rb1);
           load_rope(p, rw, sx.row, rb1);
         }
       }
@@ -418,19 +461,27 @@ __device__ void softmax_role(const Stage1Params& p, const Cx& cx, PieceCursor cu
       tc_fence_after();
       {
         uint32_t sr[32];
-        tmem_ld32(cx.tmem + sx.lane_base + kTmemS2 + 64 * s, sr);
+        tmem_ld32(cx.tmem + sx.lane_base + L::kSCols * s, sr);
         tmem_wait_ld();
+        if constexpr (kQ8) {  // columns 0-15: token A, 16-31: token B (codes, no lo part)
 #pragma unroll
-        for (int h = 0; h < 16; ++h) {
-          const float v = (__uint_as_float(sr[h]) + __uint_as_float(sr[16 + h]) * (1.0f / kLoScale)) * ca;
-          xa[h] = valid ? v : -INFINITY;
-        }
-        tmem_ld32(cx.tmem + sx.lane_base + kTmemS2 + 64 * s + 32, sr);
-        tmem_wait_ld();
+          for (int h = 0; h < 16; ++h) {
+            xa[h] = valid ? __uint_as_float(sr[h]) * ca : -INFINITY;
+            xb[h] = valid ? __uint_as_float(sr[16 + h]) * cb : -INFINITY;
+          }
+        } else {  // columns 0-31: token A hi, lo; 32-63: token B hi, lo
 #pragma unroll
-        for (int h = 0; h < 16; ++h) {
-          const float v = (__uint_as_float(sr[h]) + __uint_as_float(sr[16 + h]) * (1.0f / kLoScale)) * cb;
-          xb[h] = valid ? v : -INFINITY;
+          for (int h = 0; h < 16; ++h) {
+            const float v = (__uint_as_float(sr[h]) + __uint_as_float(sr[16 + h]) * (1.0f / kLoScale)) * ca;
+            xa[h] = valid ? v : -INFINITY;
+          }
+          tmem_ld32(cx.tmem + sx.lane_base + L::kSCols * s + 32, sr);
+          tmem_wait_ld();
+#pragma unroll
+          for (int h = 0; h < 16; ++h) {
+            const float v = (__uint_as_float(sr[h]) + __uint_as_float(sr[16 + h]) * (1.0f / kLoScale)) * cb;
+            xb[h] = valid ? v : -INFINITY;
+          }
         }
       }
       tc_fence_before();
@@ -479,7 +530,7 @@ __device__ void softmax_role(const Stage1Params& p, const Cx& cx, PieceCursor cu
 
     // the next piece's q goes in while this piece's last PV runs
     float ca_next = ca, cb_next = cb;
-    if (have_next && !setup_q2<QF>(p, cx, sx, nxt, k + 1, kvsc, ca_next, cb_next)) return;
+    if (have_next && !setup_q2<kQ8, QF>(p, cx, sx, nxt, k + 1, kvsc, ca_next, cb_next)) return;
     // l over the 128 rows, per head and token
     {
       const float wa = warp_reduce16<false>(la, lane);
@@ -517,22 +568,22 @@ __device__ void softmax_role(const Stage1Params& p, const Cx& cx, PieceCursor cu
   }
 }
 
-template <int QF>
+template <int QF, bool kQ8>
 __global__ void __launch_bounds__(kThreads, 1) stage1_pair_kernel(const Stage1Params p,
                                                                   const __grid_constant__ CUtensorMap kvmap) {
   extern __shared__ uint8_t smem_raw[];
-  Cx cx;
+  CxT<kQ8> cx;
   PieceCursor cur;
   if (!cta_begin(p, cx, smem_raw, 1, cur)) return;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   cur.align8 = 1;  // the tiles of the single-token kernel
   if (warp == 0) {
-    producer(cx, &kvmap, cur, lane);
+    producer<kQ8>(cx, &kvmap, cur, lane);
   } else if (warp == 1) {
-    if (lane == 0) mma_issuer(cx, cur);
+    if (lane == 0) mma_issuer<kQ8>(cx, cur);
     __syncwarp();
   } else if (warp < 6) {
-    softmax_role<QF>(p, cx, cur, warp, lane);
+    softmax_role<QF, kQ8>(p, cx, cur, warp, lane);
   }
   cta_end(p, cx, 1);
 }
@@ -550,29 +601,31 @@ extern "C" int mla_debug_phase_cycles_pair(unsigned long long* host, int n, int 
 }
 #endif
 
-template <int QF>
+template <int QF, bool kQ8>
 static cudaError_t launch_q(const Stage1Params& p, cudaStream_t stream) {
+  constexpr int kAlloc = LT<kQ8>::kAlloc;
   static int configured_device = -1;
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (configured_device != dev) {
-    e = cudaFuncSetAttribute(stage1_pair_kernel<QF>, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kAlloc);
+    e = cudaFuncSetAttribute(stage1_pair_kernel<QF, kQ8>, cudaFuncAttributeMaxDynamicSharedMemorySize, kAlloc);
     if (e != cudaSuccess) return e;
     configured_device = dev;
   }
   CUtensorMap map;
   e = make_kv_map(&map, p.kv, p.total_kv, kTileRows);
   if (e != cudaSuccess) return e;
-  return launch_dependent(stage1_pair_kernel<QF>, p.num_splits, kThreads, L::kAlloc, stream, p, map);
+  return launch_dependent(stage1_pair_kernel<QF, kQ8>, p.num_splits, kThreads, kAlloc, stream, p, map);
 }
 
 }  // namespace pair
 }  // namespace tc
 
 cudaError_t launch_stage1_pair(int q_fmt, const Stage1Params& p, cudaStream_t stream) {
-  if (q_fmt == kQBf16Quant) return tc::pair::launch_q<kQBf16Quant>(p, stream);
-  return q_fmt == kQBf16 ? tc::pair::launch_q<kQBf16>(p, stream) : tc::pair::launch_q<kQFp8>(p, stream);
+  // fp8 q (given, or quantised in the call) takes the three-stage layout
+  if (q_fmt == kQBf16Quant) return tc::pair::launch_q<kQBf16Quant, true>(p, stream);
+  return q_fmt == kQBf16 ? tc::pair::launch_q<kQBf16, false>(p, stream) : tc::pair::launch_q<kQFp8, true>(p, stream);
 }
 
 }  // namespace mla

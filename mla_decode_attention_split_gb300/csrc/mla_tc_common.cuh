@@ -275,8 +275,9 @@ __device__ __forceinline__ float quotient_rn(float x, float s, float inv) {
 }
 
 // q of one token into rows row0..row0+31 of the Q buffer (chunks of
-// kChunk bytes); returns the score scale or a negative value on abort.
-template <class LL, int QF, int kChunk>
+// kChunk bytes); returns the score scale or a negative value on abort. With
+// fp8 codes and kLo false only rows row0..row0+15 are written (no lo rows).
+template <class LL, int QF, int kChunk, bool kLo = true>
 __device__ float fill_q(const Stage1Params& p, const Ctx<LL>& cx, SoftmaxCtx& sx, int token, int row0, uint32_t kk,
                         float kvsc) {
   const int t = 32 * sx.wi + sx.lane;  // 0..127
@@ -313,8 +314,10 @@ __device__ float fill_q(const Stage1Params& p, const Ctx<LL>& cx, SoftmaxCtx& sx
       }
       *qaddr(h, d0 + 8 * i) = code[0];
       *qaddr(h, d0 + 8 * i + 4) = code[1];
-      *qaddr(16 + h, d0 + 8 * i) = 0u;
-      *qaddr(16 + h, d0 + 8 * i + 4) = 0u;
+      if (kLo) {
+        *qaddr(16 + h, d0 + 8 * i) = 0u;
+        *qaddr(16 + h, d0 + 8 * i + 4) = 0u;
+      }
     }
     c = p.sm_scale * kLog2e * kvsc * qs;
   } else if (QF == kQBf16) {
@@ -360,8 +363,10 @@ __device__ float fill_q(const Stage1Params& p, const Ctx<LL>& cx, SoftmaxCtx& sx
       const uint2 v = __ldg(reinterpret_cast<const uint2*>(src) + i);
       *qaddr(h, d0 + 8 * i) = v.x;
       *qaddr(h, d0 + 8 * i + 4) = v.y;
-      *qaddr(16 + h, d0 + 8 * i) = 0u;
-      *qaddr(16 + h, d0 + 8 * i + 4) = 0u;
+      if (kLo) {
+        *qaddr(16 + h, d0 + 8 * i) = 0u;
+        *qaddr(16 + h, d0 + 8 * i + 4) = 0u;
+      }
     }
     c = p.sm_scale * kLog2e * kvsc * __ldg(p.q_scale);
   }
