@@ -158,15 +158,18 @@ def workload_by_name(synth, name):
     return synth.Workload(name, int(bs[2:]), 1, int(kvl[2:]), synth.BF16, kv_dtype)
 
 
-def time_workload(m, synth, torch, name, steps, warmup, flush_l2: bool, quantize_q: bool = False):
+def time_workload(m, synth, torch, name, steps, warmup, flush_l2: bool, quantize_q: bool = False, w=None,
+                  token_pairs: bool = False):
     """Per-call device time of one workload (stage-1 and total), median over steps.
-    quantize_q: pass bf16 q and let the call quantise it (the pages' a8w8 flow)."""
-    w = synth.WORKLOADS[name]
+    quantize_q: pass bf16 q and let the call quantise it (the pages' a8w8 flow).
+    w: a Workload instead of a named one; token_pairs: a segment's tokens share KV tiles in pairs."""
+    w = synth.WORKLOADS[name] if w is None else w
     if quantize_q:
         w = synth.Workload(w.name, w.batch, w.q_len, w.kv_len, synth.BF16, w.kv_dtype, w.ragged_max, w.seed)
     inp = synth.make_inputs(w, "cuda")
     out = torch.empty((inp.total_q, 16, 512), dtype=torch.bfloat16, device="cuda")
-    ws = m.alloc_workspace(inp.batch, inp.total_q, inp.total_kv, inp.kv_dtype)
+    ws = (m.alloc_pairs_workspace if token_pairs else m.alloc_workspace)(inp.batch, inp.total_q, inp.total_kv,
+                                                                         inp.kv_dtype)
     flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device="cuda") if flush_l2 else None
     ev = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
     tot, st1 = [], []
@@ -174,7 +177,7 @@ def time_workload(m, synth, torch, name, steps, warmup, flush_l2: bool, quantize
         if flush is not None:
             flush.fill_(i & 0xFF)
         m.decode(inp.q, inp.kv, inp.kv_scale, inp.qo_indptr, inp.kv_indptr, out, inp.kv_dtype, workspace=ws,
-                 q_dtype=inp.q_dtype, q_scale=inp.q_scale, events=ev, quantize_q=quantize_q)
+                 q_dtype=inp.q_dtype, q_scale=inp.q_scale, events=ev, quantize_q=quantize_q, token_pairs=token_pairs)
         torch.cuda.synchronize()
         if i >= warmup:
             tot.append(m.elapsed_ms(ev[0], ev[2]) * 1e3)
@@ -457,6 +460,14 @@ def finish(args, line, rank, world, w, m, synth, torch, inp):
             qq = "a8w8_bs64_kv1024+in_call_q_quantisation"
             table[qq] = {"cold": time_workload(m, synth, torch, "a8w8_bs64_kv1024", 30, 5, True, quantize_q=True),
                          "warm": time_workload(m, synth, torch, "a8w8_bs64_kv1024", 30, 5, False, quantize_q=True)}
+            # two query tokens per segment (multi-token decode), with and without token pairs
+            for qd, qn in ((synth.BF16, "bf16q"), (synth.FP8_E4M3, "fp8q")):
+                wq = synth.Workload(f"fp8kv_bs128_q2_kv8192_{qn}", 128, 2, 8192, qd, synth.FP8_E4M3)
+                for pairs in (False, True):
+                    key = wq.name + ("+token_pairs" if pairs else "")
+                    table[key] = {"cold": time_workload(m, synth, torch, None, 30, 5, True, w=wq, token_pairs=pairs),
+                                  "warm": time_workload(m, synth, torch, None, 30, 5, False, w=wq,
+                                                        token_pairs=pairs)}
             # the headline shape with the cache in pages scattered over a pool
             for ps, in_order in ((1, True), (1, False), (16, False), (64, False)):
                 key = f"fp8kv_bs256_kv8192+paged_ps{ps}_{'in_order' if in_order else 'random'}"
