@@ -147,3 +147,13 @@ def test_paged_workspace_size_and_argument_checks(lib):
     n = m.workspace_size(1, 1, 10, m.FP8_E4M3, num_splits=1)
     opts.workspace, opts.workspace_bytes = 256, n
     assert L.mla_decode_paged(*args(m.FP8_E4M3)) == m.MLA_ERR_WORKSPACE
+
+
+def test_pairs_workspace_size(lib):
+    # token pairs: 2 num_splits + total_q partial slots
+    n = m.pairs_workspace_size(4, 8, 4096, m.FP8_E4M3, num_splits=32)
+    slots = 2 * 32 + 8
+    assert n == 256 + 256 + slots * 16 * 512 * 4 + slots * 16 * 4
+    assert n == m.workspace_size(4, 8, 4096, m.FP8_E4M3, num_splits=64)
+    with pytest.raises(m.MlaError):
+        m.pairs_workspace_size(4, 8, 4096, m.FP8_E4M3, num_splits=-1)

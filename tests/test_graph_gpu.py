@@ -4,8 +4,9 @@ A serving engine captures its decode step once and replays it. Every entry
 point used here makes no allocation and no synchronisation inside the call,
 so it can be captured; the replays must give the same bits as eager calls
 (with the same inputs and partition count). Covered: the contiguous fp8 path
-(programmatic dependent launch), in-call q quantisation (two kernels), the
-paged path (two kernels), mxfp4 and bf16 KV, and the allocation-free variant.
+(programmatic dependent launch), in-call q quantisation (two kernels), token
+pairs, the paged path (two kernels), mxfp4 and bf16 KV, and the
+allocation-free variant.
 """
 import ctypes
 
@@ -63,6 +64,23 @@ def test_decode_replays_bitwise(kv_dtype, q_dtype, quantize):
     def call():
         m.decode(inp.q, inp.kv, inp.kv_scale, inp.qo_indptr, inp.kv_indptr, out, inp.kv_dtype, workspace=ws,
                  q_dtype=inp.q_dtype, q_scale=inp.q_scale, num_splits=11, quantize_q=quantize)
+
+    eager, replays = _captured(call, out)
+    assert m.device_error(ws)[0] == m.MLA_OK
+    for r in replays:
+        assert torch.equal(r, eager)
+
+
+@pytest.mark.parametrize("q_dtype", [synth.BF16, synth.FP8_E4M3])
+def test_token_pairs_decode_replays_bitwise(q_dtype):
+    w = synth.Workload("graphpairs", 4, 1, 0, q_dtype, synth.FP8_E4M3, seed=54)
+    inp = synth.make_inputs(w, "cuda", kv_lens=[700, 64, 1301, 3], q_lens=[2, 3, 1, 2])
+    out = torch.empty((inp.total_q, 16, 512), dtype=torch.bfloat16, device="cuda")
+    ws = m.alloc_pairs_workspace(inp.batch, inp.total_q, inp.total_kv, inp.kv_dtype, num_splits=11)
+
+    def call():
+        m.decode(inp.q, inp.kv, inp.kv_scale, inp.qo_indptr, inp.kv_indptr, out, inp.kv_dtype, workspace=ws,
+                 q_dtype=inp.q_dtype, q_scale=inp.q_scale, num_splits=11, token_pairs=True)
 
     eager, replays = _captured(call, out)
     assert m.device_error(ws)[0] == m.MLA_OK
