@@ -152,10 +152,14 @@ def kv_bytes(inp) -> int:
 def workload_by_name(synth, name):
     if name in synth.WORKLOADS:
         return synth.WORKLOADS[name]
-    # profiling shapes: kvfp8_bs64_kv8192, kvbf16_bs8_kv4096, kvmx_bs64_kv8192 (bf16 q, one token per segment)
-    fmt, bs, kvl = name.split("_")
-    kv_dtype = {"kvfp8": synth.FP8_E4M3, "kvbf16": synth.BF16, "kvmx": synth.MXFP4}[fmt]
-    return synth.Workload(name, int(bs[2:]), 1, int(kvl[2:]), synth.BF16, kv_dtype)
+    # profiling shapes: kvfp8_bs64_kv8192, kvbf16_bs8_kv4096, kvmx_bs64_kv8192 (bf16 q, one token per
+    # segment); kvfp8a8_...: fp8 q; an optional q<N> field sets the tokens per segment (kvfp8_bs64_q2_kv8192)
+    parts = name.split("_")
+    fmt, bs, kvl = parts[0], parts[1], parts[-1]
+    q_len = int(parts[2][1:]) if len(parts) == 4 else 1
+    kv_dtype = {"kvfp8": synth.FP8_E4M3, "kvfp8a8": synth.FP8_E4M3, "kvbf16": synth.BF16, "kvmx": synth.MXFP4}[fmt]
+    q_dtype = synth.FP8_E4M3 if fmt == "kvfp8a8" else synth.BF16
+    return synth.Workload(name, int(bs[2:]), q_len, int(kvl[2:]), q_dtype, kv_dtype)
 
 
 def time_workload(m, synth, torch, name, steps, warmup, flush_l2: bool, quantize_q: bool = False, w=None,
@@ -292,7 +296,10 @@ def main():
     ap.add_argument("--no-workloads", action="store_true", help="skip the per-workload table")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end measurement")
     ap.add_argument("--workload", default=HEADLINE,
-                    help="workload name (the five benchmark workloads, or kv{fp8,bf16}_bs<B>_kv<L> for profiling)")
+                    help="workload name (the five benchmark workloads, or kv{fp8,fp8a8,bf16,mx}_bs<B>[_q<N>]_kv<L> "
+                         "for profiling)")
+    ap.add_argument("--token-pairs", action="store_true",
+                    help="the tokens of a segment share each KV tile in pairs (fp8 KV, q_len > 1)")
     args = ap.parse_args()
     if args.impl == "reference":
         return run_reference(args)
@@ -315,7 +322,8 @@ def main():
     kvb = kv_bytes(inp)
     out = torch.empty((inp.total_q, 16, 512), dtype=torch.bfloat16, device=device)
     splits = m.plan(inp.batch, inp.total_q, inp.total_kv, inp.kv_dtype)
-    ws = m.alloc_workspace(inp.batch, inp.total_q, inp.total_kv, inp.kv_dtype, num_splits=splits)
+    alloc = m.alloc_pairs_workspace if args.token_pairs else m.alloc_workspace
+    ws = alloc(inp.batch, inp.total_q, inp.total_kv, inp.kv_dtype, num_splits=splits)
     stream = torch.cuda.current_stream()
     K, W = args.steps, args.warmup
     # the per-launch profile events run in a second, shorter pass: an event
@@ -327,7 +335,8 @@ def main():
 
     def step(events=None):
         m.decode(inp.q, inp.kv, inp.kv_scale, inp.qo_indptr, inp.kv_indptr, out, inp.kv_dtype, workspace=ws,
-                 q_dtype=inp.q_dtype, q_scale=inp.q_scale, num_splits=splits, events=events, stream=stream)
+                 q_dtype=inp.q_dtype, q_scale=inp.q_scale, num_splits=splits, events=events, stream=stream,
+                 token_pairs=args.token_pairs)
 
     for _ in range(W):
         step()
@@ -366,7 +375,8 @@ def main():
 
     # end to end through the host-buffer entry point: every input H2D from
     # pinned memory and the output D2H inside the timed region, every step
-    e2e = None if args.no_e2e else measure_e2e(m, torch, inp, out, ws, splits, stream, K, world, device, kvb)
+    e2e = None if (args.no_e2e or args.token_pairs) else measure_e2e(m, torch, inp, out, ws, splits, stream, K,
+                                                                       world, device, kvb)
     line = build_line(args, w, inp, kvb, splits, world, K, W, value, ms_step, achieved, peak, peak_kind, s1_avg_s,
                       stage2_ms, clocks, e2e)
     finish(args, line, rank, world, w, m, synth, torch, inp)
@@ -432,7 +442,8 @@ def build_line(args, w, inp, kvb, splits, world, K, W, value, ms_step, achieved,
                        "parallelism": f"{world} independent replicas (weak scaling)"},
             "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                          "frac": round(achieved / peak, 4), "traffic": _ncu_traffic(w.name),
-                         "kernel": _kernel_name(synth, w),
+                         "kernel": ("stage1_pair_kernel (tcgen05, token pairs) " if args.token_pairs else "")
+                                   + _kernel_name(synth, w),
                          "algorithmic_bytes": f"{kvb} per launch = {kvb // inp.total_kv} B x {inp.total_kv} KV rows",
                          "peak_kind": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)",
                          "stage1_us": round(s1_avg_s * 1e6, 2),
