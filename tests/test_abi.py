@@ -143,6 +143,10 @@ def test_paged_workspace_size_and_argument_checks(lib):
     pg.num_pages = 3
     for dt in (m.BF16, m.MXFP4):  # the paged path is the fp8 tensor-core kernel
         assert L.mla_decode_paged(*args(dt)) == m.MLA_ERR_UNSUPPORTED
+    # token pairs are not combined with a page table
+    opts.token_pairs = 1
+    assert L.mla_decode_paged(*args(m.FP8_E4M3)) == m.MLA_ERR_UNSUPPORTED
+    opts.token_pairs = 0
     # a workspace sized for the contiguous call is too small for the paged one
     n = m.workspace_size(1, 1, 10, m.FP8_E4M3, num_splits=1)
     opts.workspace, opts.workspace_bytes = 256, n
