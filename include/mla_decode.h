@@ -21,7 +21,8 @@
  * with LSE weights (the pages' stage 2), as in kernelbot-amd-mixed-mla-753817
  * (module docstring, `mla_flash_decode_stage1`, `mla_flash_decode_stage2`).
  * The merge runs inside the same launch: the CTA that finishes a token's last
- * partial merges it, so one decode call is one kernel launch.
+ * partial merges it, so one decode call is one kernel launch (two with
+ * in-call q quantisation or a page table: a small kernel runs first).
  *
  * Conventions for every entry point:
  *   - Pointers named d_* or documented "device" are CUDA device pointers that
