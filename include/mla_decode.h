@@ -246,10 +246,18 @@ mla_status_t mla_decode_from_host(const void* h_q, const void* h_kv, const void*
                                   void* stream);
 
 /* Dequantisation through the decode kernels' own operand path: KV rows
- * [row0, row0+nrows) are loaded and converted exactly as stage 1 does, pushed
- * through the same tensor-core instruction against an identity operand, and
- * written as fp32 to d_out [nrows][576]. The result equals the format's
- * definition (code * scale) bit for bit wherever that value is representable.
+ * [row0, row0+nrows) are loaded and converted exactly as stage 1 does and
+ * written as fp32 to d_out [nrows][576] (device, 4-byte aligned).
+ *  - bf16, fp8: the rows are pushed through the same tensor-core instruction
+ *    against an identity operand; kv_scale is not read (fp8: value = code,
+ *    the per-tensor scale is the caller's).
+ *  - mxfp4: kv_scale = the e8m0 block scales [total_kv][18] (required). The
+ *    rows go through stage 1's conversion to rebased e5m2 operand bytes and
+ *    the row exponent R; value = byte * 2^(R - 127). Blocks more than 15
+ *    binades below the row's largest block are 0, as in the decode; a NaN
+ *    scale (0xFF) is outside the domain.
+ * The result equals the format's definition bit for bit wherever that value
+ * is representable in fp32 (and, for mxfp4, the block is not flushed).
  * Asynchronous. Errors: MLA_ERR_INVALID_ARG.                                  */
 mla_status_t mla_dequant_rows(const void* kv, const void* kv_scale, mla_dtype_t kv_dtype,
                               int32_t total_kv, int32_t row0, int32_t nrows, float* d_out,

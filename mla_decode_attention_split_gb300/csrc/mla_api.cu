@@ -274,8 +274,9 @@ mla_status_t mla_dequant_rows(const void* kv, const void* kv_scale, mla_dtype_t 
   if (!kv || !d_out || !aligned16(kv) || total_kv < 0 || row0 < 0 || nrows < 0 ||
       static_cast<int64_t>(row0) + nrows > total_kv)
     return MLA_ERR_INVALID_ARG;
-  if (kv_dtype == MLA_DTYPE_MXFP4) return MLA_ERR_UNSUPPORTED;
-  if (kv_dtype != MLA_DTYPE_BF16 && kv_dtype != MLA_DTYPE_FP8_E4M3) return MLA_ERR_INVALID_ARG;
+  if (kv_dtype == MLA_DTYPE_MXFP4 && !kv_scale) return MLA_ERR_INVALID_ARG;
+  if (kv_dtype != MLA_DTYPE_BF16 && kv_dtype != MLA_DTYPE_FP8_E4M3 && kv_dtype != MLA_DTYPE_MXFP4)
+    return MLA_ERR_INVALID_ARG;
   if (mla::launch_dequant(kv, kv_scale, kv_dtype, total_kv, row0, nrows, d_out, static_cast<cudaStream_t>(stream)) !=
       cudaSuccess)
     return MLA_ERR_CUDA;

@@ -1,8 +1,11 @@
-// The dequantisation check kernel: it pushes KV rows through stage 1's
-// operand path (same byte layout, same MMA) against an identity operand, so
-// the decode of the stored codes can be compared bit for bit.
+// The dequantisation check kernels. bf16 and fp8: KV rows go through stage
+// 1's operand path (same byte layout, same MMA) against an identity operand.
+// mxfp4: rows go through the mxfp4 stage-1 conversion (the same device code)
+// to its rebased e5m2 operand bytes and row exponent. Either way the decode
+// of the stored codes can be compared bit for bit.
 #include "mla_device.cuh"
 #include "mla_internal.h"
+#include "mla_mx_convert.cuh"
 #include "mla_partition.cuh"
 
 namespace mla {
@@ -104,15 +107,42 @@ __global__ void mla_dequant_kernel(const uint8_t* __restrict__ kv, int32_t total
   }
 }
 
+// mxfp4: one warp per row, lane b < 18 takes block b (32 dims). The value of
+// dim d is operand byte d times the row factor 2^(R - 127), R = the row's
+// largest block exponent: exactly code * 2^(s - 127) unless the block is
+// flushed (more than 15 binades below R, then 0).
+__global__ void mla_dequant_mx_kernel(const uint8_t* __restrict__ kv, const uint8_t* __restrict__ kv_scale,
+                                      int32_t row0, int32_t nrows, float* __restrict__ out) {
+  const int lane = threadIdx.x & 31;
+  const int i = 4 * blockIdx.x + (threadIdx.x >> 5);
+  if (i >= nrows) return;
+  const int64_t row = static_cast<int64_t>(row0) + i;
+  const uint32_t s = lane < 18 ? kv_scale[row * 18 + lane] : 0u;
+  uint32_t R = s;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) R = max(R, __shfl_xor_sync(0xffffffffu, R, o));
+  if (lane >= 18) return;
+  const uint4 v = __ldg(reinterpret_cast<const uint4*>(kv + row * 288 + 16 * lane));
+  uint4 lo, hi;
+  mxcvt::convert_block(v, mxcvt::rebase_scale2(R - s), lo, hi);
+  const float f = mxcvt::exp2i(static_cast<int>(R) - 127);
+  const uint32_t w[8] = {lo.x, lo.y, lo.z, lo.w, hi.x, hi.y, hi.z, hi.w};
+  float* o = out + static_cast<int64_t>(i) * 576 + 32 * lane;
+#pragma unroll
+  for (int k = 0; k < 32; ++k) o[k] = mxcvt::e5m2_value(w[k >> 2] >> (8 * (k & 3))) * f;
+}
+
 cudaError_t launch_dequant(const void* kv, const void* kv_scale, int kv_fmt, int32_t total_kv, int32_t row0,
                            int32_t nrows, float* out, cudaStream_t stream) {
-  (void)kv_scale;
   if (nrows <= 0) return cudaSuccess;
   const int blocks = (nrows + 7) / 8;
   if (kv_fmt == kKvFp8) {
     mla_dequant_kernel<kKvFp8><<<blocks, 32, 0, stream>>>(static_cast<const uint8_t*>(kv), total_kv, row0, nrows, out);
   } else if (kv_fmt == kKvBf16) {
     mla_dequant_kernel<kKvBf16><<<blocks, 32, 0, stream>>>(static_cast<const uint8_t*>(kv), total_kv, row0, nrows, out);
+  } else if (kv_fmt == kKvMxfp4) {
+    mla_dequant_mx_kernel<<<(nrows + 3) / 4, 128, 0, stream>>>(static_cast<const uint8_t*>(kv),
+                                                               static_cast<const uint8_t*>(kv_scale), row0, nrows, out);
   } else {
     return cudaErrorInvalidValue;
   }

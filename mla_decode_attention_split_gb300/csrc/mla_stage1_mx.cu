@@ -31,11 +31,16 @@
 //  * Warps 0-3 convert (warp 0, lane 0 also issues the UMMAs and owns tensor
 //    memory), warps 4-7 run the online softmax (thread = row = TMEM lane).
 //    Every mbarrier wait is bounded.
+#include "mla_mx_convert.cuh"
 #include "mla_tc_common.cuh"
 
 namespace mla {
 namespace tc {
 namespace mx {
+
+using mxcvt::convert_block;
+using mxcvt::exp2i;
+using mxcvt::rebase_scale2;
 
 constexpr int kThreads = 384;  // warpgroup 0 converts, 1 runs the softmax, 2 issues the UMMAs (warp 8)
 // Registers per thread: launched at 168 (384 threads), then the issuing
@@ -45,7 +50,6 @@ constexpr uint32_t kLaunchRegs = 168, kWorkRegs = 224, kIssueRegs = 56;
 static_assert(kWorkRegs * 2 + kIssueRegs == 3 * kLaunchRegs, "register split must equal the launch budget");
 constexpr int kStages = 2;
 constexpr int kStageBytes = kVBytes + kRopeBytes;  // 72 KB: V dims + rope dims (e5m2)
-constexpr int kMaxRebase = 15;  // e5m2 holds e2m1 * 2^-down exactly for down <= 15
 
 struct L {
   static constexpr int kThreads = mx::kThreads;
@@ -179,41 +183,6 @@ __device__ __forceinline__ void dump_raw(uint8_t* raw_w, uint8_t* sc_w, int lane
   for (int j = 0; j < 18; ++j) *reinterpret_cast<uint4*>(raw_w + 16 * (32 * j + lane)) = r.nib[j];
 #pragma unroll
   for (int k = 0; k < 9; ++k) *reinterpret_cast<uint16_t*>(sc_w + 2 * (32 * k + lane)) = static_cast<uint16_t>(r.sc[k]);
-}
-
-// e2m1 -> rebased e5m2, through f16: the hardware conversion turns each byte
-// (two e2m1 codes) into two exact f16 values, an f16 multiply by 2^-down
-// rebases them (exact: every e2m1 value times 2^-down, down <= 15, is an f16
-// number with at most 2 significant bits below the leading one), and e5m2 is
-// the high byte of f16 (same exponent bias, 2 mantissa bits), so the bytes are
-// exact. A block more than 15 binades below the row's largest is multiplied by
-// zero (flushed).
-__device__ __forceinline__ uint32_t rebase_scale2(uint32_t down) {
-  const uint32_t s = down <= static_cast<uint32_t>(kMaxRebase) ? ((15u - down) << 10) : 0u;  // f16 2^-down
-  return s | (s << 16);
-}
-
-// Eight e2m1 codes (one 32-bit word, element 0 in the lowest nibble) -> eight
-// e5m2 bytes: byte i of out_lo is element i, of out_hi element 4 + i.
-__device__ __forceinline__ void e2m1x8_to_e5m2x8(uint32_t w, uint32_t s2, uint32_t& out_lo, uint32_t& out_hi) {
-  uint32_t h0, h1, h2, h3;
-  asm("{\n .reg .b8 b0, b1, b2, b3;\n mov.b32 {b0, b1, b2, b3}, %4;\n"
-      " cvt.rn.f16x2.e2m1x2 %0, b0;\n cvt.rn.f16x2.e2m1x2 %1, b1;\n"
-      " cvt.rn.f16x2.e2m1x2 %2, b2;\n cvt.rn.f16x2.e2m1x2 %3, b3;\n"
-      " mul.rn.f16x2 %0, %0, %5;\n mul.rn.f16x2 %1, %1, %5;\n"
-      " mul.rn.f16x2 %2, %2, %5;\n mul.rn.f16x2 %3, %3, %5;\n}"
-      : "=r"(h0), "=r"(h1), "=r"(h2), "=r"(h3)
-      : "r"(w), "r"(s2));
-  out_lo = prmt(h0, h1, 0x7531u);  // high bytes of the four f16 values
-  out_hi = prmt(h2, h3, 0x7531u);
-}
-
-// 32 e2m1 codes (16 bytes) -> 32 e5m2 bytes as two 16-byte units.
-__device__ __forceinline__ void convert_block(const uint4& v, uint32_t s2, uint4& lo, uint4& hi) {
-  e2m1x8_to_e5m2x8(v.x, s2, lo.x, lo.y);
-  e2m1x8_to_e5m2x8(v.y, s2, lo.z, lo.w);
-  e2m1x8_to_e5m2x8(v.z, s2, hi.x, hi.y);
-  e2m1x8_to_e5m2x8(v.w, s2, hi.z, hi.w);
 }
 
 // Converts this thread's row (tile row tr, staged at srow / ssc) into the
@@ -392,11 +361,6 @@ __device__ void issuer_role(const Cx& cx, PieceCursor cur) {
   // every issued tcgen05 operation completes before tensor memory is freed
   umma_commit(cx.bar(L::kDrain));
   mbar_wait_drain_tc(cx.bar(L::kDrain), 0);
-}
-
-// 2^e for an integer e in [-127, 127] (exact).
-__device__ __forceinline__ float exp2i(int e) {
-  return e >= -126 ? __uint_as_float(static_cast<uint32_t>(e + 127) << 23) : __uint_as_float(0x00400000u);
 }
 
 // ---------------------------------------------------------------------------

@@ -115,6 +115,9 @@ def test_argument_checks_fail_before_any_device_work(lib):
     # dequant entry: row range beyond the cache
     st = L.mla_dequant_rows(ctypes.c_void_p(aligned), None, m.FP8_E4M3, 10, 5, 6, ctypes.c_void_p(aligned), None)
     assert st == m.MLA_ERR_INVALID_ARG
+    # mxfp4 rows need their block scales
+    st = L.mla_dequant_rows(ctypes.c_void_p(aligned), None, m.MXFP4, 10, 0, 6, ctypes.c_void_p(aligned), None)
+    assert st == m.MLA_ERR_INVALID_ARG
     assert L.mla_get_device_error(None, None, None) == m.MLA_ERR_INVALID_ARG
 
 

@@ -315,6 +315,45 @@ def test_dequant_bf16_bit_exact_with_offset_rows():
     assert np.array_equal(got[normal], ref[normal])
 
 
+def test_dequant_mxfp4_bit_exact_through_the_stage1_conversion():
+    # Every byte (two e2m1 codes) meets block exponents 0..20 binades below its
+    # row's largest: within 15 the value is code * 2^(s - 127) exactly (that
+    # covers the e5m2 subnormals at 14 and 15 below), beyond it the block is
+    # flushed to zero as in the decode. Two more rows: every scale 254 (values
+    # from 2^128 up overflow fp32 on both sides) and every scale 0 (fp32
+    # subnormals).
+    rows, nb = 66, 18
+    r = np.arange(rows)[:, None]
+    codes = ((r * 7 + np.arange(288)[None, :] * 13) % 256).astype(np.uint8)
+    base = 120 + (np.arange(rows) % 9)
+    down = (np.arange(rows)[:, None] * 5 + np.arange(nb)[None, :] * 3) % 21
+    down[:, 0] = 0  # block 0 holds the row's largest exponent
+    scales = (base[:, None] - down).astype(np.uint8)
+    scales[64], scales[65] = 254, 0
+    kv = torch.from_numpy(codes).cuda()
+    sc = torch.from_numpy(scales).cuda()
+    out = torch.empty((rows - 2, 576), dtype=torch.float32, device="cuda")
+    m.dequant_rows(kv, sc, m.MXFP4, 2, rows - 2, out)
+    torch.cuda.synchronize()
+    got = out.cpu().numpy()
+    nib = np.stack([codes & 0xF, codes >> 4], axis=-1).reshape(rows, 576)
+    elem = oracle.decode_array("e2m1", nib)
+    scale = oracle.decode_array("e8m0", scales)
+    with np.errstate(over="ignore"):
+        ref = (elem * np.repeat(scale, 32, axis=1)).astype(np.float32)[2:]
+    flushed = np.repeat((scales.max(axis=1, keepdims=True) - scales.astype(np.int32)) > 15, 32, axis=1)[2:]
+    assert flushed.any() and (~flushed).any()
+    bad = np.argwhere((got != ref) & ~flushed & ~(np.isnan(got) & np.isnan(ref)))
+    rs, ds = bad[:, 0] + 2, bad[:, 1]
+    assert len(bad) == 0, (len(bad), [(int(a), int(d), int(nib[a, d]), int(scales[a, d // 32]),
+                                        int(scales[a].max()), float(got[a - 2, d]), float(ref[a - 2, d]))
+                                       for a, d in zip(rs[:12], ds[:12])])
+    assert np.all(got[flushed] == 0)
+    assert np.isinf(got[62]).any() and np.isfinite(got[62]).any()
+    assert ((np.abs(got[63]) < 2.0 ** -126) & (got[63] != 0)).any()
+    assert len(np.unique(codes[2:])) == 256
+
+
 def test_host_buffer_entry_matches_device_entry():
     w = synth.Workload("host", 3, 1, 0, synth.FP8_E4M3, synth.FP8_E4M3, seed=6)
     inp = synth.make_inputs(w, "cuda", kv_lens=[500, 64, 1500])
