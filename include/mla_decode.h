@@ -130,9 +130,12 @@ typedef struct {
  * length: kernelbot-amd-mixed-mla-586148 "Adaptive split-K", -753817
  * `_choose_kv_splits`, -739756 `_get_config`). Here the KV rows of all
  * segments are divided evenly over the CTAs, so the planner picks only how
- * many partitions to use: enough to fill the GPU (`sm_count` SMs, one CTA
- * each), but no partition smaller than a few tiles. Host only; no device
- * access. sm_count <= 0 queries the current device.
+ * many partitions P <= sm_count to use (one CTA per SM). It minimises a cost
+ * model of the slowest CTA: the tiles it streams, a fixed cost per token run
+ * it holds (so P a multiple or a divisor of the token count, where no CTA
+ * straddles a segment boundary, is preferred), and the merge of the splits
+ * of a token. Segment lengths are taken as equal (total_kv / batch). Host
+ * only; no device access. sm_count <= 0 queries the current device.
  * Writes the partition count to *num_splits. Errors: MLA_ERR_INVALID_ARG for
  * negative sizes or a NULL output.                                           */
 mla_status_t mla_plan(int32_t batch, int32_t total_q, int32_t total_kv, mla_dtype_t kv_dtype,

@@ -1,5 +1,6 @@
 // C-ABI entry points of the MLA decode library (declared in mla_decode.h):
 // argument checks, the split planner, workspace carving and kernel launches.
+#include <algorithm>
 #include <cmath>
 #include <cstdint>
 #include <cstring>
@@ -25,21 +26,59 @@ int sm_count_of_current_device() {
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
-// Fewest KV rows a partition should get: below this, the per-partition fixed
-// cost (query load, partial write and merge) outweighs the parallelism.
-constexpr int64_t kMinRowsPerSplit = 128;
 constexpr int32_t kMaxSplits = 4096;
+
+// Split planner: a cost model of the slowest CTA, in units of one 128-row
+// tile of streaming. A "piece" is one token's run of rows inside one CTA.
+//  * Every piece a CTA holds costs kPieceCost more (query setup, epilogue,
+//    partial write and count), and a piece that does not start on an 8-row
+//    boundary of its segment may take one more tile.
+//  * The CTA that merges a token reads one partial per split of it
+//    (kMergeCost each).
+//  * P a multiple of the token count gives every CTA one piece of one
+//    segment; P a divisor of it gives every CTA whole segments. Otherwise the
+//    worst CTA straddles a boundary and holds one piece more.
+// Segments are taken as equally long (the planner sees only the totals).
+// Constants from decode timings on the fp8 tensor-core kernel over split
+// counts: one piece costs about 4 tiles, one merged partial a quarter tile.
+constexpr double kPieceCost = 4.0, kMergeCost = 0.25;
+
+double split_cost(int64_t p, int64_t nseg, int64_t lv) {
+  if (p % nseg == 0) {  // k CTAs per segment, one piece each
+    const int64_t k = p / nseg;
+    const int64_t rows = (lv + k - 1) / k;
+    const int64_t lead = (lv % k == 0 && (lv / k) % 8 == 0) ? 0 : 7;
+    return kPieceCost + static_cast<double>((rows + lead + 127) / 128) + (k > 1 ? kMergeCost * k : 0.0);
+  }
+  if (nseg % p == 0) {  // whole segments per CTA, no merges
+    const int64_t j = nseg / p;
+    return static_cast<double>(j) * (kPieceCost + static_cast<double>((lv + 127) / 128));
+  }
+  const double r = static_cast<double>(nseg) * static_cast<double>(lv) / static_cast<double>(p);
+  const double lvd = static_cast<double>(lv);
+  const double pieces = std::min(static_cast<double>(nseg), std::ceil(r / lvd) + 1.0);
+  const double tiles = std::ceil(r / 128.0) + pieces;
+  const double k = r < lvd ? std::ceil(lvd / r) + 1.0 : 2.0;
+  return kPieceCost * pieces + tiles + kMergeCost * k;
+}
 
 int32_t plan_splits(int64_t total_q, int64_t batch, int64_t total_kv, int sm_count) {
   if (sm_count <= 0) sm_count = 1;
-  // Work estimate: every query token streams its segment's rows; with one
-  // token per segment this is exactly total_kv.
-  int64_t work = total_kv;
-  if (batch > 0 && total_q > batch) work = (total_kv * total_q + batch - 1) / batch;
-  int64_t p = (work + kMinRowsPerSplit - 1) / kMinRowsPerSplit;
-  if (p > sm_count) p = sm_count;
-  if (p < 1) p = 1;
-  return static_cast<int32_t>(p);
+  if (total_q <= 0 || batch <= 0 || total_kv <= 0) return 1;
+  // one unit of work per query token: its segment's rows (average length)
+  const int64_t nseg = total_q;
+  const int64_t lv = std::max<int64_t>(1, total_kv / batch);
+  const int64_t maxp = std::min<int64_t>(sm_count, nseg * lv);  // at least one row per CTA
+  int64_t best = 1;
+  double best_cost = split_cost(1, nseg, lv);
+  for (int64_t p = 2; p <= maxp; ++p) {
+    const double c = split_cost(p, nseg, lv);
+    if (c <= best_cost + 1e-9) {  // ties go to more CTAs
+      best = p;
+      best_cost = std::min(best_cost, c);
+    }
+  }
+  return static_cast<int32_t>(best);
 }
 
 size_t kv_bytes(mla_dtype_t dt, int64_t total_kv) {

@@ -49,13 +49,27 @@ def test_status_strings(lib):
 
 
 def test_planner_host_logic(lib):
-    # one partition per 128 KV rows of work, capped at the SM count
+    # more segments than SMs: one CTA per SM (straddling beats idle SMs)
     assert m.plan(256, 256, 256 * 8192, m.FP8_E4M3, sm_count=152) == 152
+    assert m.plan(128, 128, 128 * 8192, m.MXFP4, sm_count=152) == 152
+    # fewer segments: a multiple of the segment count, so each CTA holds one
+    # piece of one segment (measured 44 us at 128 splits against 53 at 152 for
+    # 32 x 8192 rows; 20 against 29 for 64 x 1024)
+    assert m.plan(32, 32, 32 * 8192, m.FP8_E4M3, sm_count=152) == 128
+    assert m.plan(64, 64, 64 * 1024, m.FP8_E4M3, sm_count=152) == 128
+    # short segments: splitting them further costs merges; one CTA per segment
+    assert m.plan(64, 64, 64 * 8, m.FP8_E4M3, sm_count=152) == 64
+    assert m.plan(4, 4, 4 * 64, m.FP8_E4M3, sm_count=152) == 4
+    # 4 x 1024 rows: 8 splits per segment, each one full tile
     assert m.plan(4, 4, 4096, m.BF16, sm_count=152) == 32
     assert m.plan(1, 1, 1, m.FP8_E4M3, sm_count=152) == 1
     assert m.plan(1, 1, 0, m.FP8_E4M3, sm_count=152) == 1
-    # q_len > 1: work scales with tokens per segment
+    # q_len > 1: one unit of work per query token
     assert m.plan(2, 8, 256, m.BF16, sm_count=152) == 8
+    assert m.plan(32, 64, 32 * 8192, m.FP8_E4M3, sm_count=152) == 128
+    # never more CTAs than SMs
+    for b, kv in ((1, 10 ** 6), (7, 7 * 3000), (300, 300 * 50)):
+        assert 1 <= m.plan(b, b, kv, m.FP8_E4M3, sm_count=152) <= 152
     with pytest.raises(m.MlaError):
         m.plan(-1, 1, 1, m.BF16, sm_count=152)
 
