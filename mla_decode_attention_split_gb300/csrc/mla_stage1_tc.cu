@@ -44,7 +44,8 @@
 namespace mla {
 namespace tc {
 
-constexpr int kThreads = 256;  // warp 0 TMA, warp 1 MMA, warps 2-5 softmax, 6-7 only in the merge
+constexpr int kThreads = 256;  // warp 0 TMA, warp 1 MMA, warps 2-5 softmax, 6-7 the Q operand of pieces >= 1
+constexpr uint32_t kBarQprep = 2;  // named barrier of the two q-prep warps (0 is __syncthreads)
 constexpr int kStages = 3;
 constexpr int kStageBytes = kVBytes;  // 64 KB: the 512 V dims of a tile
 
@@ -59,7 +60,9 @@ struct L {
   static constexpr int kOffAmax = kOffRedL + 4 * 16 * 4;          // [4] u32
   static constexpr int kOffMList = kOffAmax + 16;                 // MergeList (64 B)
   static constexpr int kOffScan = kOffMList + 64;                 // 16 x i64
-  static constexpr int kOffBars = kOffScan + 16 * 8;
+  static constexpr int kOffCRing = kOffScan + 16 * 8;             // score scale of piece k: f32 [4] + tag u32 [4]
+  static constexpr int kOffQpAmax = kOffCRing + 32;               // [2] u32: the q-prep warps' maxima
+  static constexpr int kOffBars = kOffQpAmax + 16;
   enum {
     kKvFull = 0, kKvEmpty = 3, kSFull = 6, kSEmpty = 8, kRopeFull = 10, kPFull = 11, kPEmpty = 12, kQFull = 13,
     kQEmpty = 14, kOFull = 15, kOEmpty = 17, kGrp = 19, kDrain = 21, kMerge = 22, kNumBars = 23
@@ -85,9 +88,10 @@ struct L {
     mbar_init(cx.bar(kRopeFull), 4);
     mbar_init(cx.bar(kPFull), 4);
     mbar_init(cx.bar(kPEmpty), 1);
-    mbar_init(cx.bar(kQFull), 4);
+    mbar_init(cx.bar(kQFull), 4);  // piece 0: the 4 softmax warps; later pieces: the 2 q-prep warps, 2 each
     mbar_init(cx.bar(kQEmpty), 1);
     mbar_init(cx.bar(kDrain), 1);
+    for (int i = 0; i < 4; ++i) reinterpret_cast<volatile uint32_t*>(cx.g + kOffCRing + 16)[i] = 0u;
   }
 };
 static_assert(L::kAlloc <= 227 * 1024, "shared memory budget");
@@ -428,6 +432,145 @@ __device__ __forceinline__ void store_rope(const Cx& cx, const SoftmaxCtx& sx, c
   if (sx.lane == 0) mbar_arrive(cx.bar(L::kRopeFull));
 }
 
+// Warps 6-7: the Q operand (B of Q.K^T, the layout fill_q writes) of every
+// piece after the first, prepared while the piece before it streams, so that
+// at a piece boundary the tensor pipe waits only for the copy into the Q
+// buffer. Thread t (0..63) takes head t / 4, dims 144 (t % 4) .. +143; the
+// codes and the score scale are those fill_q computes (the same per-token
+// amax, here over two warps). The scale of piece k goes to ring slot k % 4,
+// tagged k + 1, for the softmax warps. The ring cannot be overwritten early:
+// piece k + 4's operand waits for the last Q.K^T of piece k + 3, which needs
+// a score buffer that the softmax warps freed after they started piece k.
+__device__ __forceinline__ bool qprep_all(bool v) {  // both q-prep warps agree
+  uint32_t r;
+  asm volatile("{\n .reg .pred p, q;\n setp.ne.u32 p, %1, 0;\n bar.red.and.pred q, %2, 64, p;\n selp.u32 %0, 1, 0, q;\n}"
+               : "=r"(r)
+               : "r"(static_cast<uint32_t>(v)), "r"(kBarQprep)
+               : "memory");
+  return r != 0u;
+}
+
+template <int QF>
+__device__ void qprep_role(const Stage1Params& p, const Cx& cx, PieceCursor cur, int warp, int lane) {
+  Piece pc;
+  if (!cur.next(pc)) return;  // piece 0 is set up by the softmax warps
+  const int t = 32 * (warp - 6) + lane;  // 0..63
+  const int h = t >> 2, d0 = 144 * (t & 3);
+  const float kvsc = __ldg(static_cast<const float*>(p.kv_scale));
+  uint8_t* qb = cx.g + L::kOffQ;
+  auto qaddr = [&](int row, int d) -> uint32_t* {
+    const int unit = (d & 127) >> 4;
+    return reinterpret_cast<uint32_t*>(qb + (d >> 7) * kQChunkBytes + (row >> 3) * 1024 + (row & 7) * 128 +
+                                       ((unit ^ (row & 7)) << 4) + (d & 15));
+  };
+  volatile float* ring_c = reinterpret_cast<volatile float*>(cx.g + L::kOffCRing);
+  volatile uint32_t* ring_tag = reinterpret_cast<volatile uint32_t*>(cx.g + L::kOffCRing + 16);
+  uint32_t* am = reinterpret_cast<uint32_t*>(cx.g + L::kOffQpAmax);
+  if (QF == kQBf16Quant && p.wait_late) griddep_wait();  // the scale comes from this call's amax kernel
+  for (uint32_t k = 1; cur.next(pc); ++k) {
+    uint32_t hi[36], lo[36];
+    float c;
+    if (QF == kQFp8) {
+      const uint8_t* src = static_cast<const uint8_t*>(p.q) + (static_cast<int64_t>(pc.token) * kHeads + h) * kDqk + d0;
+#pragma unroll
+      for (int i = 0; i < 9; ++i) {
+        const uint4 v = __ldg(reinterpret_cast<const uint4*>(src) + i);
+        hi[4 * i] = v.x; hi[4 * i + 1] = v.y; hi[4 * i + 2] = v.z; hi[4 * i + 3] = v.w;
+      }
+#pragma unroll
+      for (int i = 0; i < 36; ++i) lo[i] = 0u;
+      c = p.sm_scale * kLog2e * kvsc * __ldg(p.q_scale);
+    } else {
+      const uint16_t* src =
+          static_cast<const uint16_t*>(p.q) + (static_cast<int64_t>(pc.token) * kHeads + h) * kDqk + d0;
+      uint32_t w[72];
+#pragma unroll
+      for (int i = 0; i < 18; ++i) {
+        const uint4 v = __ldg(reinterpret_cast<const uint4*>(src) + i);
+        w[4 * i] = v.x; w[4 * i + 1] = v.y; w[4 * i + 2] = v.z; w[4 * i + 3] = v.w;
+      }
+      if (QF == kQBf16Quant) {
+        const float qs = *static_cast<const volatile float*>(p.q_scale);
+        const float inv = 1.0f / qs;  // correctly rounded, once
+#pragma unroll
+        for (int i = 0; i < 36; ++i) {  // dims d0 + 4i .. +3
+          const float a = quotient_rn(bf16_bits_to_f32(w[2 * i] & 0xFFFFu), qs, inv);
+          const float b = quotient_rn(bf16_bits_to_f32(w[2 * i] >> 16), qs, inv);
+          const float e = quotient_rn(bf16_bits_to_f32(w[2 * i + 1] & 0xFFFFu), qs, inv);
+          const float f = quotient_rn(bf16_bits_to_f32(w[2 * i + 1] >> 16), qs, inv);
+          hi[i] = f32x2_to_e4m3x2(a, b) | (f32x2_to_e4m3x2(e, f) << 16);
+          lo[i] = 0u;
+        }
+        c = p.sm_scale * kLog2e * kvsc * qs;
+      } else {
+        uint32_t mx = 0;
+#pragma unroll
+        for (int i = 0; i < 72; ++i) mx = __vmaxu2(mx, w[i] & 0x7FFF7FFFu);
+        mx = max(mx & 0xFFFFu, mx >> 16);
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+        if (lane == 0) am[warp - 6] = mx;
+        named_bar_sync(kBarQprep, 64);
+        mx = max(am[0], am[1]);
+        named_bar_sync(kBarQprep, 64);  // both have read am before the next piece writes it
+        const int e = static_cast<int>((mx >> 7) & 0xFF);  // biased exponent of max |q|
+        int shift = (mx == 0) ? 0 : 134 - e;               // max |q| 2^shift in [128, 256)
+        shift = max(-126, min(126, shift));
+        const float up = __uint_as_float(static_cast<uint32_t>(shift + 127) << 23);
+        const float down = __uint_as_float(static_cast<uint32_t>(127 - shift) << 23);
+#pragma unroll
+        for (int g = 0; g < 36; ++g) {  // dims d0 + 4g .. +3
+          const float x0 = bf16_bits_to_f32(w[2 * g] & 0xFFFFu) * up, x1 = bf16_bits_to_f32(w[2 * g] >> 16) * up;
+          const float x2 = bf16_bits_to_f32(w[2 * g + 1] & 0xFFFFu) * up,
+                      x3 = bf16_bits_to_f32(w[2 * g + 1] >> 16) * up;
+          const uint32_t h01 = f32x2_to_e4m3x2(x0, x1), h23 = f32x2_to_e4m3x2(x2, x3);
+          const float2 d01 = e4m3x2_to_f32x2(h01), d23 = e4m3x2_to_f32x2(h23);
+          const uint32_t l01 = f32x2_to_e4m3x2(kLoScale * (x0 - d01.x), kLoScale * (x1 - d01.y));
+          const uint32_t l23 = f32x2_to_e4m3x2(kLoScale * (x2 - d23.x), kLoScale * (x3 - d23.y));
+          hi[g] = h01 | (h23 << 16);
+          lo[g] = l01 | (l23 << 16);
+        }
+        c = p.sm_scale * kLog2e * kvsc * down;
+      }
+    }
+    // the previous piece's last Q.K^T has read the Q buffer
+    if (!qprep_all(cx.wait(L::kQEmpty, (k - 1) & 1u))) return;
+#pragma unroll
+    for (int g = 0; g < 36; ++g) {
+      *qaddr(h, d0 + 4 * g) = hi[g];
+      *qaddr(16 + h, d0 + 4 * g) = lo[g];
+    }
+    if (t == 0) {
+      ring_c[k & 3u] = c;
+      __threadfence_block();
+      ring_tag[k & 3u] = k + 1u;
+    }
+    fence_async_smem();
+    __syncwarp();
+    if (lane == 0) mbar_arrive_cnt(cx.bar(L::kQFull), 2);
+  }
+}
+
+// The score scale of piece k >= 1 from the q-prep ring (bounded wait); a
+// negative value on abort.
+__device__ __forceinline__ float ring_scale(const Cx& cx, uint32_t k) {
+  const volatile float* ring_c = reinterpret_cast<const volatile float*>(cx.g + L::kOffCRing);
+  const volatile uint32_t* ring_tag = reinterpret_cast<const volatile uint32_t*>(cx.g + L::kOffCRing + 16);
+  if (ring_tag[k & 3u] != k + 1u) {
+    const long long t0 = clock64();
+    while (ring_tag[k & 3u] != k + 1u) {
+      if (*cx.abort_word) return -1.f;
+      if (clock64() - t0 > kWaitLimitCycles) {
+        *cx.abort_word = 1u;
+        atomicOr(cx.flags, kFlagTimeout);
+        return -1.f;
+      }
+    }
+  }
+  __threadfence_block();
+  return ring_c[k & 3u];
+}
+
 template <int QF, bool kPaged>
 __device__ void softmax_role(const Stage1Params& p, const Cx& cx, PieceCursor cur, int warp, int lane) {
   SoftmaxCtx sx;
@@ -478,6 +621,10 @@ __device__ void softmax_role(const Stage1Params& p, const Cx& cx, PieceCursor cu
   TC_PT_INIT
   while (have) {
     const bool have_next = ahead.next(nxt);
+    if (k > 0) {
+      c = ring_scale(cx, k);
+      if (c < 0.f) return;
+    }
     float m[16], l[16];
 #pragma unroll
     for (int h = 0; h < 16; ++h) {
@@ -579,12 +726,7 @@ __device__ void softmax_role(const Stage1Params& p, const Cx& cx, PieceCursor cu
       ++n;
     }
 
-    // the next piece's q goes in while this piece's last PV runs
-    float c_next = c;
-    if (have_next) {
-      c_next = setup_q<L, QF>(p, cx, sx, nxt.token, k + 1, kvsc);
-      if (c_next < 0.f) return;
-    }
+    // (the next piece's Q operand comes from warps 6-7, qprep_role)
     // l over the 128 rows, per head
     const float wl = warp_reduce16<false>(l, lane);
     if ((lane & 1) == 0) red_l[sx.wi * 16 + (lane >> 1)] = wl;
@@ -606,7 +748,6 @@ __device__ void softmax_role(const Stage1Params& p, const Cx& cx, PieceCursor cu
     TC_PT(6);
     pc = nxt;
     have = have_next;
-    c = c_next;
     ++k;
   }
 }
@@ -638,8 +779,11 @@ __global__ void __launch_bounds__(kThreads, 1) stage1_tc_kernel(const Stage1Para
     __syncwarp();
   } else if (warp < 6) {
     softmax_role<QF, kPaged>(p, cx, cur, warp, lane);
-  } else if (warp == 6) {
-    if constexpr (kPaged) prefetch_page_ids(p, cur, lane);
+  } else {
+    if constexpr (kPaged) {
+      if (warp == 6) prefetch_page_ids(p, cur, lane);
+    }
+    qprep_role<QF>(p, cx, cur, warp, lane);
   }
   if constexpr (kPaged) {
     __syncthreads();
