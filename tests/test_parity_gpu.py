@@ -207,6 +207,43 @@ def test_in_call_q_quantisation_equals_caller_quantised_a8w8():
     check(ref.float().cpu().numpy(), oracle_ref(dataclasses.replace(inp, q=codes, q_scale=scale, q_dtype=synth.FP8_E4M3)))
 
 
+@pytest.mark.parametrize("q_mode", ["bf16", "fp8", "quantize"])
+def test_later_token_runs_of_a_cta_equal_first_runs(q_mode):
+    # 12 equal segments: with one CTA each, every token is its CTA's first run
+    # (its Q operand set up by the softmax warps); with one CTA for all, runs
+    # 1..11 get theirs from the Q-prep warps through the 4-slot scale ring
+    # (wrapping twice). Each token's run lies inside one CTA either way, with
+    # the same tiles, so the outputs must agree bit for bit.
+    nseg = 12
+    q_dtype = synth.FP8_E4M3 if q_mode == "fp8" else synth.BF16
+    w = synth.Workload("qprep", nseg, 1, 0, q_dtype, synth.FP8_E4M3, seed=47)
+    inp = synth.make_inputs(w, "cuda", kv_lens=[200] * nseg)
+    outs = []
+    for ns in (nseg, 1):
+        out = torch.empty((inp.total_q, 16, 512), dtype=torch.bfloat16, device="cuda")
+        ws = m.alloc_workspace(inp.batch, inp.total_q, inp.total_kv, inp.kv_dtype, num_splits=ns)
+        m.decode(inp.q, inp.kv, inp.kv_scale, inp.qo_indptr, inp.kv_indptr, out, inp.kv_dtype, workspace=ws,
+                 q_dtype=inp.q_dtype, q_scale=inp.q_scale, num_splits=ns, quantize_q=q_mode == "quantize")
+        torch.cuda.synchronize()
+        assert m.device_error(ws)[0] == m.MLA_OK
+        outs.append(out)
+    assert torch.equal(outs[0], outs[1])
+    if q_mode != "quantize":
+        check(outs[1].float().cpu().numpy(), oracle_ref(inp))
+
+
+def test_many_token_runs_per_cta_ragged():
+    # 21 short ragged segments (one empty) over 1, 2 and 5 CTAs: up to 20 runs
+    # per CTA, split and whole, for bf16 and fp8 q
+    lens = [1, 7, 130, 0, 64, 65, 3, 300, 8, 9, 127, 128, 129, 2, 40, 17, 256, 5, 90, 11, 200]
+    for q_dtype in (synth.BF16, synth.FP8_E4M3):
+        w = synth.Workload("manyruns", len(lens), 1, 0, q_dtype, synth.FP8_E4M3, seed=48)
+        inp = synth.make_inputs(w, "cuda", kv_lens=lens)
+        ref = oracle_ref(inp)
+        for ns in (1, 2, 5):
+            check(run_decode(inp, num_splits=ns).float().cpu().numpy(), ref)
+
+
 @pytest.mark.parametrize("amax_bits", [0x3F80, 0x3FFF, 0x42C9, 0x3B01])
 def test_in_call_q_quantisation_codes_over_every_mantissa(amax_bits):
     # Every bf16 value within 13 binades below the tensor maximum (both signs) is
