@@ -145,6 +145,12 @@ def _barrier(world: int):
         dist.barrier()
 
 
+def aggregate_gbs(kv_bytes_per_step: int, steps: int, world: int, ms_total: float) -> float:
+    """Whole-job KV-read GB/s: every rank streams kv_bytes_per_step per step
+    (weak scaling), over the slowest rank's time for all steps."""
+    return kv_bytes_per_step * steps * world / (ms_total * 1e-3) / 1e9
+
+
 def kv_bytes(inp) -> int:
     return inp.kv_bytes()
 
@@ -417,7 +423,7 @@ def main():
     stage2_ms = [m.elapsed_ms(e[1], e[2]) for e in ev]
     s1_avg_s = sum(stage1_ms) / KP * 1e-3
     ms_step = ms_total / K
-    value = kvb * K * world / (ms_total * 1e-3) / 1e9
+    value = aggregate_gbs(kvb, K, world, ms_total)
     peak, peak_kind = _measured_peaks()
     achieved = kvb / s1_avg_s / 1e9
     clocks = sampler.summary(t_wall0, t_wall1)
