@@ -119,6 +119,16 @@ __device__ __forceinline__ void cp_async16(uint32_t dst_smem, const void* src, u
 
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
 
+// The mbarrier gets an arrival once all of this thread's earlier cp.async
+// copies have completed; its pending count is raised by one first, so the
+// current phase waits for that arrival without a change of its count.
+__device__ __forceinline__ void cp_async_mbar_arrive(uint32_t bar) {
+  asm volatile("cp.async.mbarrier.arrive.shared::cta.b64 [%0];" ::"r"(bar) : "memory");
+}
+
+// Waits for all of this thread's cp.async copies.
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
+
 // Waits until at most N of this thread's committed copy groups are pending.
 template <int N>
 __device__ __forceinline__ void cp_async_wait() {

@@ -249,25 +249,21 @@ __device__ PagedDrain producer_paged(const Stage1Params& p, const Cx& cx, const 
                        pol);
         }
       }
-      cp_async_commit();
-    } else {  // all by TMA: the barrier completes when the boxes land
-      __syncwarp();
-      if (lane == 0) mbar_arrive(bar);
+      // each lane's copies complete its own (pending-count neutral) arrival
+      // on the barrier; the producer does not wait for them
+      cp_async_mbar_arrive(bar);
     }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(bar);
 #pragma unroll
     for (int j = 0; j < 4; ++j) id[j] = id_next[j];
     have = have_next;
     have_next = have && paged_tile_ids(p, tw, lane, id_next);  // two tiles ahead
-    if (contig != 0xFFFFu) {
-      cp_async_wait<0>();
-      fence_async_smem();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(bar);
-    }
     d.tma_hist = (d.tma_hist << 1) | (contig ? 1u : 0u);
     ++d.issued;
     d.n_last = n;
   }
+  cp_async_wait_all();  // none of this warp's copies may land after the CTA exits
   return d;
 }
 
@@ -328,6 +324,7 @@ __device__ bool issue_pv(const Cx& cx, const PendingPV& t) {
   return true;
 }
 
+template <bool kPaged>
 __device__ void mma_issuer(const Cx& cx, PieceCursor cur) {
   constexpr uint32_t id_qk = umma_idesc(128, 32, 0, 0, false, false);
   Piece pc;
@@ -347,6 +344,8 @@ __device__ void mma_issuer(const Cx& cx, PieceCursor cur) {
         ok = false;
         break;
       }
+      // paged: rows gathered by cp.async were written through the generic proxy
+      if constexpr (kPaged) fence_async_smem();
       TC_PT(1);
       if (n >= 2 && !cx.wait(L::kSEmpty + s, ((n >> 1) - 1) & 1u)) {
         ok = false;
@@ -775,7 +774,7 @@ __global__ void __launch_bounds__(kThreads, 1) stage1_tc_kernel(const Stage1Para
     else
       producer(cx, &kvmap, cur, lane);
   } else if (warp == 1) {
-    if (lane == 0) mma_issuer(cx, cur);
+    if (lane == 0) mma_issuer<kPaged>(cx, cur);
     __syncwarp();
   } else if (warp < 6) {
     softmax_role<QF, kPaged>(p, cx, cur, warp, lane);
