@@ -471,7 +471,8 @@ def _kernel_name(synth, w) -> str:
 
 
 def _dtype_desc(synth, w) -> str:
-    q = "bf16 q as exact hi+lo e4m3" if w.q_dtype == synth.BF16 else "e4m3 q codes"
+    q = ("bf16 q as a hi+lo e4m3 pair per element (exact for elements within about 2^-13 of the token's "
+         "max |q|; smaller ones rounded to the e4m3 subnormal step)" if w.q_dtype == synth.BF16 else "e4m3 q codes")
     return {synth.FP8_E4M3: f"e4m3 x e4m3 -> f32 (fp8 KV codes; {q})",
             synth.MXFP4: f"e5m2 x e4m3 -> f32 (mxfp4 KV rebased to e5m2 per row; {q})",
             synth.BF16: "bf16 x bf16 -> f32"}[w.kv_dtype]

@@ -266,6 +266,22 @@ mla_status_t mla_dequant_rows(const void* kv, const void* kv_scale, mla_dtype_t 
                               int32_t total_kv, int32_t row0, int32_t nrows, float* d_out,
                               void* stream);
 
+/* Host-side input check, for callers that do not trust their indptr arrays
+ * (the pages' interface trusts them: kernelbot-amd-mixed-mla-675627, module
+ * docstring, where qo_indptr and kv_indptr are built by the harness). Copies
+ * qo_indptr and kv_indptr (device, int32 [batch+1]) to the host and checks
+ * what mla_decode() assumes: [0] = 0, monotone non-decreasing,
+ * qo_indptr[batch] = total_q and kv_indptr[batch] = total_kv. For an mxfp4
+ * cache it also scans kv_scale (device, [total_kv][18] e8m0) for the NaN
+ * code 0xFF. Synchronises `stream`; allocates host memory only.
+ * Returns MLA_OK, or MLA_ERR_DEVICE_CHECK with *bad_index (may be NULL) set to
+ * the first offending element: i for qo_indptr[i], batch + 1 + i for
+ * kv_indptr[i], 2 (batch + 1) + j for byte j of kv_scale. MLA_ERR_INVALID_ARG
+ * for NULL arrays or negative sizes, MLA_ERR_CUDA if a copy fails.          */
+mla_status_t mla_validate_inputs(const int32_t* qo_indptr, const int32_t* kv_indptr, int32_t batch,
+                                 int32_t total_q, int32_t total_kv, mla_dtype_t kv_dtype,
+                                 const void* kv_scale, void* stream, int64_t* bad_index);
+
 /* Reads the device error flags that kernels set in `workspace` (OR of
  * MLA_DEVFLAG_*). Synchronises `stream`. Returns MLA_OK, MLA_ERR_TIMEOUT or
  * MLA_ERR_DEVICE_CHECK (timeout wins); *flags may be NULL.                    */
@@ -302,13 +318,22 @@ mla_status_t mla_event_elapsed_ms(void* ev_start, void* ev_end, float* ms);
  *   - Every call shares the one array and clears its error flags at the start;
  *     two calls that overlap on the GPU (different streams, no ordering) race
  *     on it and produce undefined results. Calls on one stream are ordered.
- *   - The device error flags of this entry point are not readable by the
- *     caller; argument errors are returned as for mla_decode().              */
+ *   - Argument errors are returned as for mla_decode(); the device error
+ *     flags (bounded-wait timeouts, indptr checks) are read with
+ *     mla_static_workspace_device_error().                                   */
 #define MLA_STATIC_WORKSPACE_BYTES (16u * 1024u * 1024u)
 mla_status_t mla_decode_static_workspace(const void* q, const void* kv, const void* kv_scale,
                                          const int32_t* qo_indptr, const int32_t* kv_indptr,
                                          void* out, mla_dtype_t kv_dtype,
                                          const mla_decode_opts* opts, void* stream);
+
+/* The device error flags of mla_decode_static_workspace() on the current
+ * device (the flags live in the library's fixed array, which the caller cannot
+ * address): MLA_OK, MLA_ERR_TIMEOUT or MLA_ERR_DEVICE_CHECK as
+ * mla_get_device_error(), and the OR of MLA_DEVFLAG_* in *flags (may be NULL).
+ * Flags are those of the last call on this device (each call clears them when
+ * it starts). Synchronises `stream`; allocates nothing.                      */
+mla_status_t mla_static_workspace_device_error(void* stream, uint32_t* flags);
 
 /* Static description of a status code.                                        */
 const char* mla_status_string(mla_status_t status);

@@ -11,7 +11,10 @@ import ctypes
 import os
 import threading
 
-from .synth import BF16, D_QK, D_V, FP8_E4M3, HEADS, MXFP4  # noqa: F401  (dtype codes / sizes)
+# Sizes and storage-format codes of mla_decode.h (MLA_NUM_HEADS, MLA_D_QK,
+# MLA_D_V, MLA_MX_BLOCK; mla_dtype_t).
+HEADS, D_QK, D_V, MX_BLOCK = 16, 576, 512, 32
+BF16, FP8_E4M3, MXFP4 = 0, 1, 2
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_PKG, "libmla_decode.so")
@@ -23,7 +26,7 @@ DEVFLAG_TIMEOUT, DEVFLAG_BAD_INDPTR = 0x1, 0x2
 EXPORTED = ("mla_plan", "mla_decode_workspace_size", "mla_decode", "mla_decode_from_host", "mla_dequant_rows",
             "mla_get_device_error", "mla_reset_device_error", "mla_event_elapsed_ms", "mla_decode_static_workspace",
             "mla_decode_paged_workspace_size", "mla_decode_paged", "mla_decode_pairs_workspace_size",
-            "mla_status_string")
+            "mla_validate_inputs", "mla_static_workspace_device_error", "mla_status_string")
 DEVFLAG_BAD_PAGE = 0x4
 MLA_ERR_TOO_LARGE = 7
 STATIC_WORKSPACE_BYTES = 16 * 1024 * 1024
@@ -85,6 +88,8 @@ def lib():
             L.mla_decode_paged_workspace_size.argtypes = [i32, i32, i32, st, i32, ctypes.POINTER(ctypes.c_size_t)]
             L.mla_decode_pairs_workspace_size.argtypes = [i32, i32, i32, st, i32, ctypes.POINTER(ctypes.c_size_t)]
             L.mla_decode_paged.argtypes = [P, P, P, P, ctypes.POINTER(PagedKV), P, st, ctypes.POINTER(DecodeOpts), P]
+            L.mla_validate_inputs.argtypes = [P, P, i32, i32, i32, st, P, P, ctypes.POINTER(ctypes.c_int64)]
+            L.mla_static_workspace_device_error.argtypes = [P, ctypes.POINTER(ctypes.c_uint32)]
             L.mla_status_string.argtypes = [st]
             L.mla_status_string.restype = ctypes.c_char_p
             for name in EXPORTED[:-1]:
@@ -235,6 +240,22 @@ def device_error(workspace, stream=None) -> tuple[int, int]:
     """(status, flags) from the workspace header. Synchronises the stream."""
     flags = ctypes.c_uint32(0)
     st = lib().mla_get_device_error(_ptr(workspace), _stream_handle(stream), ctypes.byref(flags))
+    return st, flags.value
+
+
+def validate_inputs(qo_indptr, kv_indptr, total_q: int, total_kv: int, kv_dtype: int, kv_scale=None,
+                    stream=None) -> tuple[int, int]:
+    """mla_validate_inputs(): (status, first bad index or -1). Synchronises the stream."""
+    bad = ctypes.c_int64(-1)
+    st = lib().mla_validate_inputs(_ptr(qo_indptr), _ptr(kv_indptr), qo_indptr.numel() - 1, total_q, total_kv,
+                                   kv_dtype, _ptr(kv_scale), _stream_handle(stream), ctypes.byref(bad))
+    return st, bad.value
+
+
+def static_workspace_device_error(stream=None) -> tuple[int, int]:
+    """(status, flags) of the last mla_decode_static_workspace() call on the current device."""
+    flags = ctypes.c_uint32(0)
+    st = lib().mla_static_workspace_device_error(_stream_handle(stream), ctypes.byref(flags))
     return st, flags.value
 
 

@@ -23,8 +23,6 @@ LIB = os.path.join(PKG, "libmla_decode.so")
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xptxas", "-v", "-I", INCLUDE, "-I", CSRC]
-# Extra nvcc flags for instrumented builds (e.g. MLA_NVCC_EXTRA=-DMLA_PHASE_TIMING); empty by default.
-EXTRA = os.environ.get("MLA_NVCC_EXTRA", "").split()
 
 
 def _nvcc() -> str:
@@ -59,7 +57,7 @@ def build(force: bool = False, verbose: bool = False) -> str:
 
     def compile_one(src):
         obj = os.path.join(BUILD_DIR, os.path.basename(src) + ".o")
-        cmd = [nvcc, *ARCH, *NVCC_FLAGS, *EXTRA, "-c", src, "-o", obj]
+        cmd = [nvcc, *ARCH, *NVCC_FLAGS, "-c", src, "-o", obj]
         r = subprocess.run(cmd, capture_output=True, text=True)
         logs[src] = r.stdout + r.stderr
         if r.returncode != 0:

@@ -4,6 +4,7 @@
 #include <cmath>
 #include <cstdint>
 #include <cstring>
+#include <vector>
 
 #include "mla_decode.h"
 #include "mla_internal.h"
@@ -347,6 +348,59 @@ mla_status_t mla_reset_device_error(void* workspace, void* stream) {
   return MLA_OK;
 }
 
+mla_status_t mla_validate_inputs(const int32_t* qo_indptr, const int32_t* kv_indptr, int32_t batch,
+                                 int32_t total_q, int32_t total_kv, mla_dtype_t kv_dtype, const void* kv_scale,
+                                 void* stream, int64_t* bad_index) {
+  if (bad_index) *bad_index = -1;
+  if (!qo_indptr || !kv_indptr || batch < 1 || total_q < 0 || total_kv < 0) return MLA_ERR_INVALID_ARG;
+  if (kv_dtype != MLA_DTYPE_BF16 && kv_dtype != MLA_DTYPE_FP8_E4M3 && kv_dtype != MLA_DTYPE_MXFP4)
+    return MLA_ERR_INVALID_ARG;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const size_t n = static_cast<size_t>(batch) + 1;
+  std::vector<int32_t> qo(n), kvp(n);
+  if (cudaMemcpyAsync(qo.data(), qo_indptr, n * sizeof(int32_t), cudaMemcpyDeviceToHost, st) != cudaSuccess ||
+      cudaMemcpyAsync(kvp.data(), kv_indptr, n * sizeof(int32_t), cudaMemcpyDeviceToHost, st) != cudaSuccess ||
+      cudaStreamSynchronize(st) != cudaSuccess)
+    return MLA_ERR_CUDA;
+  // the first offending entry of qo_indptr, then of kv_indptr (index batch + 1 + i)
+  auto first_bad = [&](const std::vector<int32_t>& a, int32_t total) -> int64_t {
+    if (a[0] != 0) return 0;
+    for (size_t i = 1; i < n; ++i)
+      if (a[i] < a[i - 1]) return static_cast<int64_t>(i);
+    if (a[n - 1] != total) return static_cast<int64_t>(n - 1);
+    return -1;
+  };
+  int64_t bad = first_bad(qo, total_q);
+  if (bad < 0) {
+    bad = first_bad(kvp, total_kv);
+    if (bad >= 0) bad += static_cast<int64_t>(n);
+  }
+  if (bad >= 0) {
+    if (bad_index) *bad_index = bad;
+    return MLA_ERR_DEVICE_CHECK;
+  }
+  if (kv_dtype == MLA_DTYPE_MXFP4 && total_kv > 0) {
+    // e8m0 0xFF is NaN: the decode's output for such a row is unspecified
+    if (!kv_scale) return MLA_ERR_INVALID_ARG;
+    const size_t nb = static_cast<size_t>(total_kv) * (MLA_D_QK / MLA_MX_BLOCK);
+    constexpr size_t kChunk = size_t{1} << 20;
+    std::vector<uint8_t> buf(std::min(nb, kChunk));
+    for (size_t off = 0; off < nb; off += kChunk) {
+      const size_t len = std::min(kChunk, nb - off);
+      if (cudaMemcpyAsync(buf.data(), static_cast<const uint8_t*>(kv_scale) + off, len, cudaMemcpyDeviceToHost,
+                          st) != cudaSuccess ||
+          cudaStreamSynchronize(st) != cudaSuccess)
+        return MLA_ERR_CUDA;
+      for (size_t i = 0; i < len; ++i)
+        if (buf[i] == 0xFFu) {
+          if (bad_index) *bad_index = static_cast<int64_t>(2 * n + off + i);
+          return MLA_ERR_DEVICE_CHECK;
+        }
+    }
+  }
+  return MLA_OK;
+}
+
 mla_status_t mla_event_elapsed_ms(void* ev_start, void* ev_end, float* ms) {
   if (!ev_start || !ev_end || !ms) return MLA_ERR_INVALID_ARG;
   if (cudaEventSynchronize(static_cast<cudaEvent_t>(ev_end)) != cudaSuccess) return MLA_ERR_CUDA;
@@ -394,4 +448,13 @@ extern "C" mla_status_t mla_decode_static_workspace(const void* q, const void* k
   o.workspace = g_static_ws_ptr[dev];
   o.workspace_bytes = MLA_STATIC_WORKSPACE_BYTES;
   return mla_decode(q, kv, kv_scale, qo_indptr, kv_indptr, out, kv_dtype, &o, stream);
+}
+
+extern "C" mla_status_t mla_static_workspace_device_error(void* stream, uint32_t* flags) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return MLA_ERR_CUDA;
+  if (flags) *flags = 0;
+  // no call on this device yet: nothing can have set a flag
+  if (!g_static_ws_ptr[dev]) return MLA_OK;
+  return mla_get_device_error(g_static_ws_ptr[dev], stream, flags);
 }

@@ -37,27 +37,6 @@ constexpr int kThreads1 = 256;
 constexpr int kTile = 64;
 constexpr float kLog2e = 1.4426950408889634f;
 
-// Optional phase timers (build with -DMLA_PHASE_TIMING): per CTA, warp and
-// phase, the SM clock cycles spent, summed over the launch. Off by default.
-#ifdef MLA_PHASE_TIMING
-constexpr int kPhaseCtas = 1024;
-__device__ unsigned long long g_phase_cycles[kPhaseCtas * 8 * 8];
-#define MLA_PT_INIT long long pt_last_ = clock64();
-#define MLA_PT(ph)                                                                                    \
-  do {                                                                                                \
-    const long long now_ = clock64();                                                                 \
-    if ((threadIdx.x & 31) == 0 && blockIdx.x < kPhaseCtas)                                           \
-      atomicAdd(&g_phase_cycles[(blockIdx.x * 8 + (threadIdx.x >> 5)) * 8 + (ph)],                    \
-                static_cast<unsigned long long>(now_ - pt_last_));                                    \
-    pt_last_ = now_;                                                                                  \
-  } while (0)
-#else
-#define MLA_PT_INIT
-#define MLA_PT(ph) \
-  do {             \
-  } while (0)
-#endif
-
 template <int KV>
 struct KvTraits;
 template <>
@@ -327,7 +306,6 @@ __device__ void score_role(const Stage1Params& p, const Ctx& cx, PieceCursor cur
   QFragsFp8 qf8;
   QFragsBf16 qfb;
   Piece pc;
-  MLA_PT_INIT
   while (cur.next(pc)) {
     float c;  // score scale (exp2 domain)
     if constexpr (KV == kKvFp8) {
@@ -350,9 +328,7 @@ __device__ void score_role(const Stage1Params& p, const Ctx& cx, PieceCursor cur
     for (int r0 = 0; r0 < pc.nrows; r0 += kTile) {
       const int nr = min(kTile, pc.nrows - r0);
       const uint32_t s = n % S::kStages, rnd = n / S::kStages;
-      MLA_PT(5);
       if (!mbar_wait(cx.bar(S::kOffBars, S::full(s)), rnd & 1u, cx.abort_word, cx.flags)) return;
-      MLA_PT(0);
       const uint32_t sb = cx.sbase + s * S::kStageBytes;
       float s0[2][4], s1[2][4];
 #pragma unroll
@@ -407,7 +383,6 @@ __device__ void score_role(const Stage1Params& p, const Ctx& cx, PieceCursor cur
       __syncwarp();
       if (lane == 0) mbar_arrive(cx.bar(S::kOffBars, S::empty(s)));
 
-      MLA_PT(1);
       // scale, mask, tile max over the 64 rows (this warp's 16, then across warps)
       float sc[2][4];
       float mx_g = -INFINITY, mx_g8 = -INFINITY;
@@ -457,10 +432,8 @@ __device__ void score_role(const Stage1Params& p, const Ctx& cx, PieceCursor cur
 
       // hand P to the output warps through slot n & 1
       const uint32_t slot = n & 1u;
-      MLA_PT(2);
       if (n >= 2 && !mbar_wait(cx.bar(S::kOffBars, S::pempty(slot)), ((n >> 1) - 1) & 1u, cx.abort_word, cx.flags))
         return;
-      MLA_PT(3);
       uint8_t* pbuf = cx.smem + S::kOffP + slot * S::kPBytes;
       if constexpr (KV == kKvFp8) {
         // P' = 256 P as hi + lo e4m3; byte layout [ks][hl][khalf][head][16]
@@ -499,7 +472,6 @@ __device__ void score_role(const Stage1Params& p, const Ctx& cx, PieceCursor cur
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(cx.bar(S::kOffBars, S::pfull(slot)));
-      MLA_PT(4);
       ++n;
     }
 
@@ -562,7 +534,6 @@ __device__ void output_role(const Stage1Params& p, const Ctx& cx, PieceCursor cu
   uint32_t n = 0, pm = 0;
   Piece pc;
   bool ok = true;
-  MLA_PT_INIT
   while (ok && cur.next(pc)) {
     float acc[16][4];
 #pragma unroll
@@ -573,12 +544,10 @@ __device__ void output_role(const Stage1Params& p, const Ctx& cx, PieceCursor cu
     for (int r0 = 0; r0 < pc.nrows; r0 += kTile) {
       const int nr = min(kTile, pc.nrows - r0);
       const uint32_t slot = n & 1u;
-      MLA_PT(5);
       if (!mbar_wait(cx.bar(S::kOffBars, S::pfull(slot)), (n >> 1) & 1u, cx.abort_word, cx.flags)) {
         ok = false;
         break;
       }
-      MLA_PT(0);
       const float al_g = alpha_sm[slot * 16 + g], al_g8 = alpha_sm[slot * 16 + g + 8];
       const uint32_t pb = cx.sbase + S::kOffP + slot * S::kPBytes;
       uint32_t pa[4][4];  // fp8: [ks*2 + hl]; bf16: [ks]
@@ -600,12 +569,10 @@ __device__ void output_role(const Stage1Params& p, const Ctx& cx, PieceCursor cu
         acc[j][3] *= al_g8;
       }
       const uint32_t s = n % S::kStages, rnd = n / S::kStages;
-      MLA_PT(1);
       if (!mbar_wait(cx.bar(S::kOffBars, S::full(s)), rnd & 1u, cx.abort_word, cx.flags)) {
         ok = false;
         break;
       }
-      MLA_PT(2);
       const uint32_t sb = cx.sbase + s * S::kStageBytes;
 
       if constexpr (KV == kKvFp8) {
@@ -658,7 +625,6 @@ __device__ void output_role(const Stage1Params& p, const Ctx& cx, PieceCursor cu
           }
         }
       }
-      MLA_PT(3);
       __syncwarp();
       if (lane == 0) mbar_arrive(cx.bar(S::kOffBars, S::empty(s)));
       if (v == 0 && !prod.done()) {
@@ -669,7 +635,6 @@ __device__ void output_role(const Stage1Params& p, const Ctx& cx, PieceCursor cu
         }
         prod.issue(p, cx, lane);
       }
-      MLA_PT(4);
       ++n;
     }
     if (!ok) break;
@@ -783,19 +748,6 @@ static cudaError_t launch_t(const Stage1Params& p, cudaStream_t stream) {
   }
   return launch_dependent(mla_stage1_kernel<KV, QF>, p.num_splits, kThreads1, bytes, stream, p);
 }
-
-#ifdef MLA_PHASE_TIMING
-extern "C" int mla_debug_phase_cycles(unsigned long long* host, int n, int reset) {
-  if (n > kPhaseCtas * 64) n = kPhaseCtas * 64;
-  if (cudaMemcpyFromSymbol(host, g_phase_cycles, sizeof(unsigned long long) * n) != cudaSuccess) return -1;
-  if (reset) {
-    void* p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_phase_cycles) != cudaSuccess) return -1;
-    if (cudaMemset(p, 0, sizeof(g_phase_cycles)) != cudaSuccess) return -1;
-  }
-  return n;
-}
-#endif
 
 bool stage1_supported(int kv_fmt, int q_fmt) {
   if (q_fmt == kQBf16Quant) return kv_fmt == kKvFp8;  // the in-call a8w8 mode

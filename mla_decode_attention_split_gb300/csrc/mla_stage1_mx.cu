@@ -98,28 +98,6 @@ static_assert(kStageBytes % 1024 == 0 && L::kOffQ % 1024 == 0 && L::kOffP % 1024
 static_assert(L::kOffRaw % 16 == 0 && L::kOffBars % 8 == 0, "staging alignment");
 using Cx = Ctx<L>;
 
-// Optional phase timers (build with -DMLA_PHASE_TIMING): cycles per CTA, warp
-// and phase, summed over the launch. Off by default.
-#ifdef MLA_PHASE_TIMING
-constexpr int kPhaseCtas = 1024;
-constexpr int kPhaseWarps = kThreads / 32;
-__device__ unsigned long long g_mx_phase[kPhaseCtas * kPhaseWarps * 8];
-#define MX_PT_INIT long long mx_pt_ = clock64();
-#define MX_PT(ph)                                                                                          \
-  do {                                                                                                     \
-    const long long now_ = clock64();                                                                      \
-    if ((threadIdx.x & 31) == 0 && blockIdx.x < kPhaseCtas)                                                \
-      atomicAdd(&g_mx_phase[(blockIdx.x * kPhaseWarps + (threadIdx.x >> 5)) * 8 + (ph)],                   \
-                static_cast<unsigned long long>(now_ - mx_pt_));                                           \
-    mx_pt_ = now_;                                                                                         \
-  } while (0)
-#else
-#define MX_PT_INIT
-#define MX_PT(ph) \
-  do {            \
-  } while (0)
-#endif
-
 // ---------------------------------------------------------------------------
 // Converters (warps 0-3; thread = tile row).
 
@@ -292,33 +270,23 @@ __device__ void converter_role(const Stage1Params& p, const Cx& cx, PieceCursor 
   MxRaw ra;
   uint32_t ma;
   load_mx_raw(p, rw, warp, lane, ra, ma);
-  MX_PT_INIT
   for (uint32_t i = 0; i < ntiles; i += 2) {
     const bool two = i + 1 < ntiles;
-    MX_PT(7);
     if (!wait_stage(cx, i)) break;
-    MX_PT(3);
     dump_raw(raw_w, sc_w, lane, ra);
     __syncwarp();
     const uint32_t m0 = ma;
     load_mx_raw(p, rw, warp, lane, ra, ma);  // tile i + 1
-    MX_PT(5);
     convert_tile(cx, i, warp, lane, raw_w, sc_w);
-    MX_PT(0);
     publish_tile(cx, i, warp, lane, m0);
-    MX_PT(6);
     if (!two) break;
     if (!wait_stage(cx, i + 1)) break;
-    MX_PT(3);
     dump_raw(raw_w, sc_w, lane, ra);
     __syncwarp();
     const uint32_t m1 = ma;
     load_mx_raw(p, rw, warp, lane, ra, ma);  // tile i + 2
-    MX_PT(5);
     convert_tile(cx, i + 1, warp, lane, raw_w, sc_w);
-    MX_PT(0);
     publish_tile(cx, i + 1, warp, lane, m1);
-    MX_PT(6);
   }
 }
 
@@ -383,7 +351,6 @@ __device__ void softmax_role(const Stage1Params& p, const Cx& cx, PieceCursor cu
   float c = setup_q<L, QF>(p, cx, sx, pc.token, 0, 1.0f);
   if (c < 0.f) return;
   uint32_t i = 0, k = 0;
-  MX_PT_INIT
   while (have) {
     const bool have_next = ahead.next(nxt);
     float m[16], mu[16], l[16];
@@ -397,11 +364,9 @@ __device__ void softmax_role(const Stage1Params& p, const Cx& cx, PieceCursor cu
       const int nr = min(kTileRows, pc.nrows - r0);
       const uint32_t b = i & 1u;
       const bool valid = sx.row < nr;
-      MX_PT(7);
       if (!cx.wait(L::kSFull + b, (i >> 1) & 1u)) return;
       // the converters' row exponents of this stage (already complete: Q.K^T read the stage)
       if (!cx.wait(L::kKvFull + b, (i >> 1) & 1u)) return;
-      MX_PT(0);
       const int r = static_cast<int>(cx.g[L::kOffRexp + b * kTileRows + sx.row]) - 127;
       tc_fence_after();
       uint32_t sr[32];
@@ -427,9 +392,7 @@ __device__ void softmax_role(const Stage1Params& p, const Cx& cx, PieceCursor cu
         store16(rm + sx.wi * 16, wm, lane);
         store16(rz + sx.wi * 16, wz, lane);
       }
-      MX_PT(1);
       if (!group_sync(cx, sx)) return;
-      MX_PT(2);
       bool grew = false;
       float alpha[16], alpha_o[16], tm[16], tz[16];
       {
@@ -462,7 +425,6 @@ __device__ void softmax_role(const Stage1Params& p, const Cx& cx, PieceCursor cu
       float pv[16];
 #pragma unroll
       for (int h = 0; h < 16; ++h) pv[h] = fast_exp2(z[h] - mu[h]) * kPScale;
-      MX_PT(3);
       // P buffer b is free once the P.V of tile i - 2 is done
       if (i >= 2 && !cx.wait(L::kPvDone + b, ((i - 2) >> 1) & 1u)) return;
       put_p_row(cx.g + L::kOffP + b * kPBytes, sx.row, pv);
@@ -472,7 +434,6 @@ __device__ void softmax_role(const Stage1Params& p, const Cx& cx, PieceCursor cu
         tc_fence_after();
         rescale_o(cx.tmem + sx.lane_base + kTmemO + (k & 1u) * 128, alpha_o);
       }
-      MX_PT(4);
       fence_async_smem();
       tc_fence_before();
       __syncwarp();
@@ -480,7 +441,6 @@ __device__ void softmax_role(const Stage1Params& p, const Cx& cx, PieceCursor cu
       // the row sums, off the P handoff
 #pragma unroll
       for (int h = 0; h < 16; ++h) l[h] = l[h] * alpha[h] + fast_exp2(x[h] - m[h]);
-      MX_PT(5);
       ++i;
     }
     // the next piece's q goes in while this piece's last P.V runs
@@ -506,7 +466,6 @@ __device__ void softmax_role(const Stage1Params& p, const Cx& cx, PieceCursor cu
     __syncwarp();
     if (lane == 0) mbar_arrive(cx.bar(L::kOEmpty + (k & 1u)));
     if (!pc.direct && !finish_partial(p, cx, sx, pc)) return;
-    MX_PT(6);
     pc = nxt;
     have = have_next;
     c = c_next;
@@ -533,23 +492,16 @@ __global__ void __launch_bounds__(kThreads, 1) stage1_mx_kernel(const Stage1Para
     setmaxnreg_dec<kIssueRegs>();
     if (warp == 8 && lane == 0) issuer_role(cx, cur);
     __syncwarp();
-    setmaxnreg_inc<kLaunchRegs>();  // back to the launch budget for the common tail
   }
+  // The issuing warpgroup takes its registers back only after warpgroups 0
+  // and 1 have returned theirs (their dec comes before this barrier), so the
+  // inc below can always be granted at once. Asking for them earlier could
+  // leave warpgroups 0-1 waiting in their own inc for registers that the
+  // issuing warpgroup holds while it waits at a barrier for them.
+  __syncthreads();
+  if (warp >= 8) setmaxnreg_inc<kLaunchRegs>();  // back to the launch budget for the common tail
   cta_end(p, cx, 8);
 }
-
-#ifdef MLA_PHASE_TIMING
-extern "C" int mla_debug_phase_cycles_mx(unsigned long long* host, int n, int reset) {
-  if (n > kPhaseCtas * kPhaseWarps * 8) n = kPhaseCtas * kPhaseWarps * 8;
-  if (cudaMemcpyFromSymbol(host, g_mx_phase, sizeof(unsigned long long) * n) != cudaSuccess) return -1;
-  if (reset) {
-    void* q = nullptr;
-    if (cudaGetSymbolAddress(&q, g_mx_phase) != cudaSuccess) return -1;
-    if (cudaMemset(q, 0, sizeof(g_mx_phase)) != cudaSuccess) return -1;
-  }
-  return n;
-}
-#endif
 
 template <int QF>
 static cudaError_t launch_q(const Stage1Params& p, cudaStream_t stream) {

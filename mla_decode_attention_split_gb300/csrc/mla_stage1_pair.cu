@@ -100,27 +100,6 @@ static_assert(LT<false>::kOffQ % 1024 == 0 && LT<false>::kOffRope % 1024 == 0 &&
 static_assert(LT<false>::kOffScan % 8 == 0 && LT<true>::kOffScan % 8 == 0, "scratch alignment");
 static_assert(LT<false>::kTmemO + 256 <= kTmemCols && LT<true>::kTmemRope + 16 <= kTmemCols, "tensor memory");
 
-// Optional phase timers (build with -DMLA_PHASE_TIMING): cycles per CTA, warp
-// and phase, summed over the launch. Off by default.
-#ifdef MLA_PHASE_TIMING
-constexpr int kPhaseCtas = 1024;
-__device__ unsigned long long g_pair_phase[kPhaseCtas * 8 * 8];
-#define PR_PT_INIT long long pr_pt_ = clock64();
-#define PR_PT(ph)                                                                                          \
-  do {                                                                                                     \
-    const long long now_ = clock64();                                                                      \
-    if ((threadIdx.x & 31) == 0 && blockIdx.x < kPhaseCtas)                                                \
-      atomicAdd(&g_pair_phase[(blockIdx.x * 8 + (threadIdx.x >> 5)) * 8 + (ph)],                           \
-                static_cast<unsigned long long>(now_ - pr_pt_));                                           \
-    pr_pt_ = now_;                                                                                         \
-  } while (0)
-#else
-#define PR_PT_INIT
-#define PR_PT(ph) \
-  do {            \
-  } while (0)
-#endif
-
 // B operands.
 //   Q.K^T k-step ks: the Q rows of chunk ks / 4 (K-major, 128B swizzle).
 template <bool kQ8>
@@ -143,16 +122,13 @@ __device__ void producer(const CxT<kQ8>& cx, const CUtensorMap* map, PieceCursor
   Piece pc;
   uint32_t n = 0;
   bool ok = true;
-  PR_PT_INIT
   while (ok && cur.next(pc)) {
     for (int r0 = 0; r0 < pc.nrows; r0 += kTileRows) {
       const uint32_t s = n % kStages, rnd = n / kStages;
-      PR_PT(1);
       if (rnd >= 1 && !cx.wait(L::kKvEmpty + s, (rnd - 1) & 1u)) {
         ok = false;
         break;
       }
-      PR_PT(0);
       if (lane == 0) {
         mbar_arrive_expect_tx(cx.bar(L::kKvFull + s), kStageBytes);
         const uint32_t dst = cx.s + L::kOffKv + s * kStageBytes;
@@ -183,10 +159,8 @@ __device__ bool issue_pv(const CxT<kQ8>& cx, const PendingPV& t) {
   using L = LT<kQ8>;
   constexpr int kStages = L::kStages;
   constexpr uint32_t id_pv = umma_idesc(128, 64, 0, 0, true, true);
-  PR_PT_INIT
   if (!cx.wait(L::kPFull, t.n & 1u)) return false;
   if (t.first && t.k >= 1 && !cx.wait(L::kOEmpty, (t.k - 1) & 1u)) return false;
-  PR_PT(4);
   tc_fence_after();
   const uint32_t stage = cx.s + L::kOffKv + (t.n % kStages) * kStageBytes;
   const uint32_t pbuf = cx.s + L::kOffP;
@@ -199,7 +173,6 @@ __device__ bool issue_pv(const CxT<kQ8>& cx, const PendingPV& t) {
   umma_commit(cx.bar(L::kKvEmpty + (t.n % kStages)));
   umma_commit(cx.bar(L::kPEmpty));
   if (t.last) umma_commit(cx.bar(L::kOFull));
-  PR_PT(5);
   return true;
 }
 
@@ -217,17 +190,14 @@ __device__ void mma_issuer(const CxT<kQ8>& cx, PieceCursor cur) {
     const uint32_t qbuf = cx.s + L::kOffQ;
     for (int r0 = 0; r0 < pc.nrows; r0 += kTileRows) {
       const uint32_t s = n & 1u, st = n % kStages;
-      PR_PT_INIT
       if (!cx.wait(L::kKvFull + st, (n / kStages) & 1u)) {
         ok = false;
         break;
       }
-      PR_PT(1);
       if (!cx.wait(L::kRopeFull, n & 1u) || (n >= 2 && !cx.wait(L::kSEmpty + s, ((n >> 1) - 1) & 1u))) {
         ok = false;
         break;
       }
-      PR_PT(2);
       tc_fence_after();
       const uint32_t stage = cx.s + L::kOffKv + st * kStageBytes;
       const uint32_t sbuf = cx.tmem + L::kSCols * s;
@@ -244,7 +214,6 @@ __device__ void mma_issuer(const CxT<kQ8>& cx, PieceCursor cur) {
       umma_commit(cx.bar(L::kSFull + s));
       const bool last = r0 + kTileRows >= pc.nrows;
       if (last) umma_commit(cx.bar(L::kQEmpty));
-      PR_PT(3);
       if (pend.valid && !issue_pv<kQ8>(cx, pend)) {
         ok = false;
         break;
@@ -430,7 +399,6 @@ __device__ void softmax_role(const Stage1Params& p, const CxT<kQ8>& cx, PieceCur
   if (!setup_q2<kQ8, QF>(p, cx, sx, pc, 0, kvsc, ca, cb)) return;
   uint32_t n = 0, k = 0;
   int tiles_left = count_tiles(cur) - 1;  // tiles of the CTA after the current one (for the rope slot)
-  PR_PT_INIT
   while (have) {
     const bool have_next = ahead.next(nxt);
     float ma[16], la[16], mb[16], lb[16];
@@ -442,9 +410,7 @@ __device__ void softmax_role(const Stage1Params& p, const CxT<kQ8>& cx, PieceCur
     for (int r0 = 0; r0 < pc.nrows; r0 += kTileRows) {
       const int nr = min(kTileRows, pc.nrows - r0);
       const uint32_t s = n & 1u;
-      PR_PT(7);
       if (!cx.wait(L::kSFull + s, (n >> 1) & 1u)) return;
-      PR_PT(0);
       // Q.K^T(n) is done: the rope slot takes tile n+1, its registers tile n+3
       if (tiles_left > 0) {
         if (n & 1u) {
@@ -495,16 +461,12 @@ __device__ void softmax_role(const Stage1Params& p, const CxT<kQ8>& cx, PieceCur
         warp_max16(xb, wm);
         store16(rm + 64 + sx.wi * 16, wm, lane);
       }
-      PR_PT(1);
       if (!group_sync(cx, sx)) return;
-      PR_PT(2);
       float alpha_a[16], pa[16], alpha_b[16], pb[16];
       const bool grew_a = softmax_tok(rm, xa, ma, la, alpha_a, pa);
       const bool grew_b = softmax_tok(rm + 64, xb, mb, lb, alpha_b, pb);
-      PR_PT(3);
       // single P buffer: P.V(n-1) must be done
       if (n >= 1 && !cx.wait(L::kPEmpty, (n - 1) & 1u)) return;
-      PR_PT(4);
       put_p_row2(cx.g + L::kOffP, sx.row, pa, pb);
       if (!valid) {
         // rows outside the piece: zero their V bytes so P = 0 meets finite values
@@ -524,7 +486,6 @@ __device__ void softmax_role(const Stage1Params& p, const CxT<kQ8>& cx, PieceCur
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(cx.bar(L::kPFull));
-      PR_PT(5);
       ++n;
     }
 
@@ -559,7 +520,6 @@ __device__ void softmax_role(const Stage1Params& p, const CxT<kQ8>& cx, PieceCur
     __syncwarp();
     if (lane == 0) mbar_arrive(cx.bar(L::kOEmpty));
     if (!pc.direct && !finish_partial(p, cx, sx, pc)) return;
-    PR_PT(6);
     pc = nxt;
     have = have_next;
     ca = ca_next;
@@ -587,19 +547,6 @@ __global__ void __launch_bounds__(kThreads, 1) stage1_pair_kernel(const Stage1Pa
   }
   cta_end(p, cx, 1);
 }
-
-#ifdef MLA_PHASE_TIMING
-extern "C" int mla_debug_phase_cycles_pair(unsigned long long* host, int n, int reset) {
-  if (n > kPhaseCtas * 64) n = kPhaseCtas * 64;
-  if (cudaMemcpyFromSymbol(host, g_pair_phase, sizeof(unsigned long long) * n) != cudaSuccess) return -1;
-  if (reset) {
-    void* q = nullptr;
-    if (cudaGetSymbolAddress(&q, g_pair_phase) != cudaSuccess) return -1;
-    if (cudaMemset(q, 0, sizeof(g_pair_phase)) != cudaSuccess) return -1;
-  }
-  return n;
-}
-#endif
 
 template <int QF, bool kQ8>
 static cudaError_t launch_q(const Stage1Params& p, cudaStream_t stream) {

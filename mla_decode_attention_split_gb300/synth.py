@@ -24,13 +24,9 @@ import math
 import numpy as np
 import torch
 
-HEADS = 16
-D_QK = 576
-D_V = 512
-MX_BLOCK = 32
-FP8_MAX = 448.0
+from . import BF16, D_QK, D_V, FP8_E4M3, HEADS, MX_BLOCK, MXFP4  # noqa: F401  (sizes and format codes)
 
-BF16, FP8_E4M3, MXFP4 = 0, 1, 2
+FP8_MAX = 448.0
 DTYPE_NAMES = {BF16: "bf16", FP8_E4M3: "fp8_e4m3", MXFP4: "mxfp4"}
 
 

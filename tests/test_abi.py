@@ -178,3 +178,15 @@ def test_pairs_workspace_size(lib):
     assert n == m.workspace_size(4, 8, 4096, m.FP8_E4M3, num_splits=64)
     with pytest.raises(m.MlaError):
         m.pairs_workspace_size(4, 8, 4096, m.FP8_E4M3, num_splits=-1)
+
+
+def test_validate_inputs_argument_errors(lib):
+    bad = ctypes.c_int64(0)
+    # NULL arrays and negative sizes are rejected before any device access
+    assert lib.mla_validate_inputs(None, None, 1, 1, 1, m.FP8_E4M3, None, None, ctypes.byref(bad)) == \
+        m.MLA_ERR_INVALID_ARG
+    assert bad.value == -1
+    p = ctypes.c_void_p(16)
+    assert lib.mla_validate_inputs(p, p, 0, 1, 1, m.FP8_E4M3, None, None, None) == m.MLA_ERR_INVALID_ARG
+    assert lib.mla_validate_inputs(p, p, 1, -1, 1, m.FP8_E4M3, None, None, None) == m.MLA_ERR_INVALID_ARG
+    assert lib.mla_validate_inputs(p, p, 1, 1, 1, 7, None, None, None) == m.MLA_ERR_INVALID_ARG

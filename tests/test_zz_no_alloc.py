@@ -6,11 +6,13 @@ memory at start-up and forbid allocations afterwards. They cannot hand
 mla_decode() a workspace, so the library offers this variant whose scratch is
 a fixed array inside the library. These checks call it through the C ABI
 twice in a row, with different inputs, and compare each result with
-mla_decode() on a caller-provided workspace (same tolerance as the parity
-tests). This file sorts last so that a run stopping at the first failure has
+mla_decode() on a caller-provided workspace: within the parity tests'
+tolerance and, since both run the same kernel over the same partition, bit
+for bit. This file sorts last so that a run stopping at the first failure has
 already run every other test.
 """
 import ctypes
+import dataclasses
 
 import numpy as np
 import pytest
@@ -66,11 +68,34 @@ def test_static_workspace_two_calls_match_mla_decode():
     w2 = synth.Workload("b", 3, 1, 0, synth.FP8_E4M3, synth.FP8_E4M3, seed=32)
     in2 = synth.make_inputs(w2, "cuda", kv_lens=[500, 2048, 129])
     st1, o1 = _static(in1, 0)
+    f1 = m.static_workspace_device_error()
     st2, o2 = _static(in2, 7)  # second call reuses the same scratch with other sizes
+    f2 = m.static_workspace_device_error()
     torch.cuda.synchronize()
     assert st1 == m.MLA_OK and st2 == m.MLA_OK, (m.status_string(st1), m.status_string(st2))
-    _close(o1, _ref(in1, 0))
-    _close(o2, _ref(in2, 7))
+    assert f1 == (m.MLA_OK, 0) and f2 == (m.MLA_OK, 0), (f1, f2)
+    r1, r2 = _ref(in1, 0), _ref(in2, 7)
+    _close(o1, r1)
+    _close(o2, r2)
+    assert torch.equal(o1, r1) and torch.equal(o2, r2)
+
+
+def test_static_workspace_flags_are_readable():
+    # a decreasing kv_indptr: the kernels skip the work and flag it in the fixed array
+    w = synth.Workload("bad", 2, 1, 0, synth.BF16, synth.FP8_E4M3, seed=34)
+    inp = synth.make_inputs(w, "cuda", kv_lens=[300, 200])
+    bad = inp.kv_indptr.clone()
+    bad[1] = 501  # kv_indptr = [0, 501, 500]: not monotone
+    inp_bad = dataclasses.replace(inp, kv_indptr=bad)
+    st, _ = _static(inp_bad, 3)
+    assert st == m.MLA_OK
+    status, flags = m.static_workspace_device_error()
+    assert status == m.MLA_ERR_DEVICE_CHECK and flags & m.DEVFLAG_BAD_INDPTR, (status, flags)
+    # the next good call clears them
+    st, out = _static(inp, 3)
+    assert st == m.MLA_OK
+    assert m.static_workspace_device_error() == (m.MLA_OK, 0)
+    assert torch.equal(out, _ref(inp, 3))
 
 
 def test_static_workspace_with_token_pairs():
