@@ -159,10 +159,11 @@ mla_status_t mla_decode_workspace_size(int32_t batch, int32_t total_q, int32_t t
  *             fp4x2 bytes for mxfp4; 16-byte aligned
  *   kv_scale  device: NULL (bf16), one float (fp8), or [total_kv][18] e8m0
  *             bytes (mxfp4; 2-byte aligned). mxfp4 rows are used as e2m1
- *             values rebased to the row's largest block scale R: blocks whose
- *             scale is more than 15 below R count as zero (their elements are
- *             at most 6 * 2^(R - 143)); a NaN scale code (0xFF) gives
- *             unspecified output values.
+ *             values rebased to the row's largest block scale R: every block
+ *             whose scale is within 28 of R is used exactly; blocks further
+ *             below count as zero (their elements are under 2^-28 of the
+ *             row's largest block); a NaN scale code (0xFF) gives unspecified
+ *             output values.
  *   qo_indptr, kv_indptr  device int32 [batch+1]: monotone, [0] = 0,
  *             qo_indptr[batch] = total_q, kv_indptr[batch] = total_kv. The
  *             kernels check this and, on a violation, skip the work and set
@@ -256,7 +257,7 @@ mla_status_t mla_decode_from_host(const void* h_q, const void* h_kv, const void*
  *    the per-tensor scale is the caller's).
  *  - mxfp4: kv_scale = the e8m0 block scales [total_kv][18] (required). The
  *    rows go through stage 1's conversion to rebased e5m2 operand bytes and
- *    the row exponent R; value = byte * 2^(R - 127). Blocks more than 15
+ *    the row exponent R; value = byte * 2^(R - 140). Blocks more than 28
  *    binades below the row's largest block are 0, as in the decode; a NaN
  *    scale (0xFF) is outside the domain.
  * The result equals the format's definition bit for bit wherever that value

@@ -108,9 +108,9 @@ __global__ void mla_dequant_kernel(const uint8_t* __restrict__ kv, int32_t total
 }
 
 // mxfp4: one warp per row, lane b < 18 takes block b (32 dims). The value of
-// dim d is operand byte d times the row factor 2^(R - 127), R = the row's
+// dim d is operand byte d times the row factor 2^(R - 140), R = the row's
 // largest block exponent: exactly code * 2^(s - 127) unless the block is
-// flushed (more than 15 binades below R, then 0).
+// flushed (more than 28 binades below R, then 0).
 __global__ void mla_dequant_mx_kernel(const uint8_t* __restrict__ kv, const uint8_t* __restrict__ kv_scale,
                                       int32_t row0, int32_t nrows, float* __restrict__ out) {
   const int lane = threadIdx.x & 31;
@@ -125,7 +125,7 @@ __global__ void mla_dequant_mx_kernel(const uint8_t* __restrict__ kv, const uint
   const uint4 v = __ldg(reinterpret_cast<const uint4*>(kv + row * 288 + 16 * lane));
   uint4 lo, hi;
   mxcvt::convert_block(v, mxcvt::rebase_scale2(R - s), lo, hi);
-  const float f = mxcvt::exp2i(static_cast<int>(R) - 127);
+  const float f = mxcvt::exp2i(mxcvt::row_exp(R));
   const uint32_t w[8] = {lo.x, lo.y, lo.z, lo.w, hi.x, hi.y, hi.z, hi.w};
   float* o = out + static_cast<int64_t>(i) * 576 + 32 * lane;
 #pragma unroll

@@ -7,15 +7,21 @@
 // head dimension shares one e8m0 scale 2^(s - 127).
 //
 // Conversion: every e2m1 element becomes an e5m2 byte rebased to the row's
-// largest block exponent R, e5m2 = e2m1 * 2^(s - R). The row factor
-// 2^(R - 127) is applied separately (stage 1 adds it to the row's scores).
-//  * Exact while s >= R - 15: e2m1 values have at most 2 significant bits and
-//    e5m2 reaches down to 2^-16 with subnormals.
-//  * Blocks more than 15 binades below R are flushed to (signed) zero.
+// largest block exponent R with kHeadroom binades to spare:
+// e5m2 = e2m1 * 2^(s - R + kHeadroom). The row factor 2^(R - 127 - kHeadroom)
+// is applied separately (stage 1 puts it into the row's scores and softmax
+// weights).
+//  * The largest element, 6 * 2^13 = 49152, stays below the e5m2 maximum
+//    (57344), so no block overflows.
+//  * A block d = R - s binades below the largest is exact while
+//    0.5 * 2^(13 - d) >= 2^-16 (the e5m2 subnormal step), i.e. d <= 28: e2m1
+//    values have at most 2 significant bits.
+//  * Blocks more than 28 binades below R are flushed to (signed) zero. Their
+//    elements are below 2^-28 of the row's largest block.
 //  * Route: the hardware conversion turns each byte (two e2m1 codes) into two
-//    exact f16 values, an f16 multiply by 2^-down rebases them (exact, by the
-//    first point), and e5m2 is the high byte of f16 (same exponent bias, two
-//    mantissa bits), so the bytes are exact.
+//    exact f16 values, an f16 multiply by 2^(13 - d) rebases them (exact, by
+//    the points above, f16 reaching 2^-24), and e5m2 is the high byte of f16
+//    (same exponent bias, two mantissa bits), so the bytes are exact.
 #pragma once
 
 #include <cuda_fp16.h>
@@ -27,14 +33,22 @@
 namespace mla {
 namespace mxcvt {
 
-constexpr int kMaxRebase = 15;  // e5m2 holds e2m1 * 2^-down exactly for down <= 15
+constexpr int kHeadroom = 13;  // binades between the row's largest block and the e5m2 top
+constexpr int kMaxDepth = 28;  // e5m2 holds e2m1 * 2^(kHeadroom - d) exactly for d <= 28
 
-// f16x2 2^-down in both halves (0 for a flushed block). 2^-15 is the f16
-// subnormal 0x0200; 2^-down for down < 15 is normal, exponent field 15 - down.
-__device__ __forceinline__ uint32_t rebase_scale2(uint32_t down) {
-  const uint32_t s = down < 15u ? ((15u - down) << 10) : (down == static_cast<uint32_t>(kMaxRebase) ? 0x0200u : 0u);
+// f16x2 2^(kHeadroom - d) in both halves for a block d = R - s binades below
+// the row's largest (0 for a flushed block). 2^-15 is the f16 subnormal
+// 0x0200; 2^e for -14 <= e <= 13 is normal, exponent field e + 15.
+__device__ __forceinline__ uint32_t rebase_scale2(uint32_t d) {
+  const int e = kHeadroom - static_cast<int>(d);
+  const uint32_t s = d <= static_cast<uint32_t>(kMaxDepth)
+                         ? (e >= -14 ? static_cast<uint32_t>(e + 15) << 10 : 0x0200u)
+                         : 0u;
   return s | (s << 16);
 }
+
+// The exponent of the row factor: K = e5m2 * 2^(R - 127 - kHeadroom).
+__device__ __forceinline__ int row_exp(uint32_t R) { return static_cast<int>(R) - 127 - kHeadroom; }
 
 // Eight e2m1 codes (one 32-bit word, element 0 in the lowest nibble) -> eight
 // e5m2 bytes: byte i of out_lo is element i, of out_hi element 4 + i.
@@ -60,9 +74,10 @@ __device__ __forceinline__ void convert_block(const uint4& v, uint32_t s2, uint4
   e2m1x8_to_e5m2x8(v.w, s2, hi.z, hi.w);
 }
 
-// 2^e for an integer e in [-127, 127] (exact).
+// 2^e for an integer e in [-149, 127] (exact; fp32 subnormals below -126).
 __device__ __forceinline__ float exp2i(int e) {
-  return e >= -126 ? __uint_as_float(static_cast<uint32_t>(e + 127) << 23) : __uint_as_float(0x00400000u);
+  return e >= -126 ? __uint_as_float(static_cast<uint32_t>(e + 127) << 23)
+                   : __uint_as_float(1u << static_cast<uint32_t>(max(e + 149, 0)));
 }
 
 // The value of an e5m2 byte (exact: it is the high byte of an f16).

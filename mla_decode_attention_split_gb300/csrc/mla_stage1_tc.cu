@@ -98,27 +98,6 @@ static_assert(L::kAlloc <= 227 * 1024, "shared memory budget");
 static_assert(L::kOffQ % 1024 == 0 && L::kOffRope % 1024 == 0, "operands need 1024-byte alignment");
 using Cx = Ctx<L>;
 
-// Optional phase timers (build with -DMLA_PHASE_TIMING): cycles per CTA, warp
-// and phase, summed over the launch. Off by default.
-#ifdef MLA_PHASE_TIMING
-constexpr int kPhaseCtas = 1024;
-__device__ unsigned long long g_tc_phase[kPhaseCtas * 8 * 8];
-#define TC_PT_INIT long long tc_pt_ = clock64();
-#define TC_PT(ph)                                                                                          \
-  do {                                                                                                     \
-    const long long now_ = clock64();                                                                      \
-    if ((threadIdx.x & 31) == 0 && blockIdx.x < kPhaseCtas)                                                \
-      atomicAdd(&g_tc_phase[(blockIdx.x * 8 + (threadIdx.x >> 5)) * 8 + (ph)],                             \
-                static_cast<unsigned long long>(now_ - tc_pt_));                                           \
-    tc_pt_ = now_;                                                                                         \
-  } while (0)
-#else
-#define TC_PT_INIT
-#define TC_PT(ph) \
-  do {            \
-  } while (0)
-#endif
-
 // Warp 0: the V dims of each tile, four 128-row x 128-byte boxes, into stage
 // (tile % 3) once the tile three back has been released by its P.V.
 __device__ void producer(const Cx& cx, const CUtensorMap* map, PieceCursor cur, int lane) {
@@ -126,16 +105,13 @@ __device__ void producer(const Cx& cx, const CUtensorMap* map, PieceCursor cur, 
   Piece pc;
   uint32_t n = 0;
   bool ok = true;
-  TC_PT_INIT
   while (ok && cur.next(pc)) {
     for (int r0 = 0; r0 < pc.nrows; r0 += kTileRows) {
       const uint32_t s = n % kStages, rnd = n / kStages;
-      TC_PT(1);
       if (rnd >= 1 && !cx.wait(L::kKvEmpty + s, (rnd - 1) & 1u)) {
         ok = false;
         break;
       }
-      TC_PT(0);
       if (lane == 0) {
         mbar_arrive_expect_tx(cx.bar(L::kKvFull + s), kStageBytes);
         const uint32_t dst = cx.s + L::kOffKv + s * kStageBytes;
@@ -303,10 +279,8 @@ struct PendingPV {
 
 __device__ bool issue_pv(const Cx& cx, const PendingPV& t) {
   constexpr uint32_t id_pv = umma_idesc(128, 32, 0, 0, true, true);
-  TC_PT_INIT
   if (!cx.wait(L::kPFull, t.n & 1u)) return false;
   if (t.first && t.k >= 2 && !cx.wait(L::kOEmpty + (t.k & 1u), ((t.k >> 1) - 1) & 1u)) return false;
-  TC_PT(4);
   tc_fence_after();
   const uint32_t stage = cx.s + L::kOffKv + (t.n % kStages) * kStageBytes;
   const uint32_t pbuf = cx.s + L::kOffP;
@@ -320,7 +294,6 @@ __device__ bool issue_pv(const Cx& cx, const PendingPV& t) {
   umma_commit(cx.bar(L::kKvEmpty + (t.n % kStages)));
   umma_commit(cx.bar(L::kPEmpty));
   if (t.last) umma_commit(cx.bar(L::kOFull + (t.k & 1u)));
-  TC_PT(5);
   return true;
 }
 
@@ -331,27 +304,21 @@ __device__ void mma_issuer(const Cx& cx, PieceCursor cur) {
   uint32_t n = 0, k = 0;
   PendingPV pend{0, 0, false, false, false};
   bool ok = true;
-  TC_PT_INIT
   while (ok && cur.next(pc)) {
-    TC_PT(7);
     if (!cx.wait(L::kQFull, k & 1u)) break;
-    TC_PT(0);
     const uint32_t qbuf = cx.s + L::kOffQ;
     for (int r0 = 0; r0 < pc.nrows; r0 += kTileRows) {
       const uint32_t s = n & 1u, st = n % kStages;
-      TC_PT(7);
       if (!cx.wait(L::kKvFull + st, (n / kStages) & 1u) || !cx.wait(L::kRopeFull, n & 1u)) {
         ok = false;
         break;
       }
       // paged: rows gathered by cp.async were written through the generic proxy
       if constexpr (kPaged) fence_async_smem();
-      TC_PT(1);
       if (n >= 2 && !cx.wait(L::kSEmpty + s, ((n >> 1) - 1) & 1u)) {
         ok = false;
         break;
       }
-      TC_PT(2);
       tc_fence_after();
       const uint32_t stage = cx.s + L::kOffKv + st * kStageBytes;
 #pragma unroll
@@ -365,15 +332,11 @@ __device__ void mma_issuer(const Cx& cx, PieceCursor cur) {
       umma_commit(cx.bar(L::kSFull + s));
       const bool last = r0 + kTileRows >= pc.nrows;
       if (last) umma_commit(cx.bar(L::kQEmpty));
-      TC_PT(3);
       if (pend.valid && !issue_pv(cx, pend)) {
         ok = false;
         break;
       }
       pend = PendingPV{n, k, r0 == 0, last, true};
-#ifdef MLA_PHASE_TIMING
-      tc_pt_ = clock64();
-#endif
       ++n;
     }
     ++k;
@@ -617,7 +580,6 @@ __device__ void softmax_role(const Stage1Params& p, const Cx& cx, PieceCursor cu
     while (cnt.next(t)) tiles_left += (t.nrows + kTileRows - 1) / kTileRows;
     tiles_left -= 1;
   }
-  TC_PT_INIT
   while (have) {
     const bool have_next = ahead.next(nxt);
     if (k > 0) {
@@ -633,9 +595,7 @@ __device__ void softmax_role(const Stage1Params& p, const Cx& cx, PieceCursor cu
     for (int r0 = 0; r0 < pc.nrows; r0 += kTileRows) {
       const int nr = min(kTileRows, pc.nrows - r0);
       const uint32_t s = n & 1u;
-      TC_PT(7);
       if (!cx.wait(L::kSFull + s, (n >> 1) & 1u)) return;
-      TC_PT(0);
       // Q.K^T(n) is done: the rope slot takes tile n+1, its registers tile n+3
       if (tiles_left > 0) {
         if constexpr (kPaged) {  // the page id was loaded one tile earlier
@@ -678,9 +638,7 @@ __device__ void softmax_role(const Stage1Params& p, const Cx& cx, PieceCursor cu
         warp_max16(x, wm);
         store16(rm + sx.wi * 16, wm, lane);
       }
-      TC_PT(1);
       if (!group_sync(cx, sx)) return;
-      TC_PT(2);
       bool grew = false;
       float alpha[16];
 #pragma unroll
@@ -699,10 +657,8 @@ __device__ void softmax_role(const Stage1Params& p, const Cx& cx, PieceCursor cu
         l[h] = l[h] * alpha[h] + pv[h];
         pv[h] *= kPScale;
       }
-      TC_PT(3);
       // single P buffer: P.V(n-1) must be done
       if (n >= 1 && !cx.wait(L::kPEmpty, (n - 1) & 1u)) return;
-      TC_PT(4);
       put_p_row(cx.g + L::kOffP, sx.row, pv);
       if (!valid) {
         // rows past the piece: zero their V bytes so P = 0 meets finite values
@@ -721,7 +677,6 @@ __device__ void softmax_role(const Stage1Params& p, const Cx& cx, PieceCursor cu
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(cx.bar(L::kPFull));
-      TC_PT(5);
       ++n;
     }
 
@@ -744,7 +699,6 @@ __device__ void softmax_role(const Stage1Params& p, const Cx& cx, PieceCursor cu
     __syncwarp();
     if (lane == 0) mbar_arrive(cx.bar(L::kOEmpty + (k & 1u)));
     if (!pc.direct && !finish_partial(p, cx, sx, pc)) return;
-    TC_PT(6);
     pc = nxt;
     have = have_next;
     ++k;
@@ -807,33 +761,25 @@ static EncodeFn encode_fn() {
   return fn;
 }
 
-// box_rows = 128 (a whole tile) for a contiguous cache; 8, 16, .., 128 for the
-// pool of a paged one.
-cudaError_t make_kv_map(CUtensorMap* map, const void* kv, int64_t total_kv, uint32_t box_rows) {
+cudaError_t make_u8_map(CUtensorMap* map, const void* base, int64_t inner, int64_t rows, int64_t pitch,
+                        uint32_t box_inner, uint32_t box_rows, CUtensorMapSwizzle swizzle) {
   EncodeFn fn = encode_fn();
   if (!fn) return cudaErrorNotSupported;
-  const cuuint64_t dims[2] = {static_cast<cuuint64_t>(kDqk), static_cast<cuuint64_t>(total_kv)};
-  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(kDqk)};
-  const cuuint32_t box[2] = {128, box_rows};
+  const cuuint64_t dims[2] = {static_cast<cuuint64_t>(inner), static_cast<cuuint64_t>(rows)};
+  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(pitch)};
+  const cuuint32_t box[2] = {box_inner, box_rows};
   const cuuint32_t es[2] = {1, 1};
-  const CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(kv), dims, strides, box, es,
-                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+  const CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, es,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
-#ifdef MLA_PHASE_TIMING
-extern "C" int mla_debug_phase_cycles_tc(unsigned long long* host, int n, int reset) {
-  if (n > kPhaseCtas * 64) n = kPhaseCtas * 64;
-  if (cudaMemcpyFromSymbol(host, g_tc_phase, sizeof(unsigned long long) * n) != cudaSuccess) return -1;
-  if (reset) {
-    void* q = nullptr;
-    if (cudaGetSymbolAddress(&q, g_tc_phase) != cudaSuccess) return -1;
-    if (cudaMemset(q, 0, sizeof(g_tc_phase)) != cudaSuccess) return -1;
-  }
-  return n;
+// box_rows = 128 (a whole tile) for a contiguous cache; 8, 16, .., 128 for the
+// pool of a paged one.
+cudaError_t make_kv_map(CUtensorMap* map, const void* kv, int64_t total_kv, uint32_t box_rows) {
+  return make_u8_map(map, kv, kDqk, total_kv, kDqk, 128, box_rows, CU_TENSOR_MAP_SWIZZLE_128B);
 }
-#endif
 
 // The launch: a programmatic dependent of the kernel before it in the stream
 // (with in-call q quantisation that kernel is the amax: the CTAs stream KV

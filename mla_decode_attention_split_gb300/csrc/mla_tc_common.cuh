@@ -648,5 +648,11 @@ __device__ __forceinline__ void cta_end(const Stage1Params& p, const Ctx<LL>& cx
 // 128 bytes x box_rows rows, 128B swizzle (defined in mla_stage1_tc.cu).
 cudaError_t make_kv_map(CUtensorMap* map, const void* kv, int64_t rows, uint32_t box_rows);
 
+// Host: a 2-D byte tensor map, `rows` rows of `inner` bytes `pitch` bytes
+// apart (pitch a multiple of 16), boxes of box_inner bytes x box_rows rows;
+// rows past the end read as zero (defined in mla_stage1_tc.cu).
+cudaError_t make_u8_map(CUtensorMap* map, const void* base, int64_t inner, int64_t rows, int64_t pitch,
+                        uint32_t box_inner, uint32_t box_rows, CUtensorMapSwizzle swizzle);
+
 }  // namespace tc
 }  // namespace mla

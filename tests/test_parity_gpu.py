@@ -119,19 +119,46 @@ def test_mxfp4_rows_of_very_different_magnitude():
 
 
 def test_mxfp4_blocks_far_below_the_row_maximum():
-    # block magnitudes 2^0 .. 2^-20 inside each row: blocks more than 15 binades
+    # block magnitudes 2^0 .. 2^-40 inside each row: blocks more than 28 binades
     # below the row's largest scale are flushed by the kernel (elements under
-    # 2^-15 of the row's largest block range), which the oracle keeps exactly
+    # 2^-28 of the row's largest block), which the oracle keeps exactly
     lens = [513, 77, 1000]
     w = synth.Workload("mxblocks", len(lens), 1, 0, synth.BF16, synth.MXFP4, seed=32)
     inp = synth.make_inputs(w, "cuda", kv_lens=lens)
     g = torch.Generator(device="cuda").manual_seed(78)
     kvf = torch.randn((inp.total_kv, synth.D_QK), generator=g, device="cuda")
-    e = torch.randint(-20, 1, (inp.total_kv, synth.D_QK // 32, 1), generator=g, device="cuda").float()
+    e = torch.randint(-40, 1, (inp.total_kv, synth.D_QK // 32, 1), generator=g, device="cuda").float()
     kvf = (kvf.view(inp.total_kv, -1, 32) * torch.pow(2.0, e)).view(inp.total_kv, synth.D_QK)
     inp = _with_mxfp4_rows(inp, kvf)
-    assert int((inp.kv_scale.max(dim=1).values.int()[:, None] - inp.kv_scale.int() > 15).sum()) > 0
+    assert int((inp.kv_scale.max(dim=1).values.int()[:, None] - inp.kv_scale.int() > 28).sum()) > 0
     check(run_decode(inp, num_splits=5).float().cpu().numpy(), oracle_ref(inp))
+
+
+def test_mxfp4_deep_blocks_are_exact_within_28_binades():
+    # V block 5 (dims 160..191) of every row 2^-16 .. 2^-22 below the rest, rope
+    # block 17 2^-22 below: every block sits 13..28 binades under its row's
+    # largest, where the old 15-binade operand flushed most of them. The output
+    # dims 160..191 are that small too (a flushed block would leave them 0), so
+    # they are also compared on their own scale.
+    lens = [700, 129, 1301]
+    w = synth.Workload("mxdeep", len(lens), 1, 0, synth.BF16, synth.MXFP4, seed=33)
+    inp = synth.make_inputs(w, "cuda", kv_lens=lens)
+    g = torch.Generator(device="cuda").manual_seed(79)
+    kvf = torch.randn((inp.total_kv, synth.D_QK), generator=g, device="cuda")
+    deep = torch.randint(16, 23, (inp.total_kv, 1), generator=g, device="cuda").float()
+    kvf[:, 160:192] *= torch.pow(2.0, -deep)
+    kvf[:, 544:576] *= 2.0 ** -22
+    inp = _with_mxfp4_rows(inp, kvf)
+    d = inp.kv_scale.max(dim=1).values.int()[:, None] - inp.kv_scale.int()
+    assert int(d[:, 5].min()) >= 13 and int(d.max()) <= 28 and int((d[:, 5] > 15).sum()) > 0
+    ref = oracle_ref(inp)
+    for ns in (1, 7):
+        got = run_decode(inp, num_splits=ns).float().cpu().numpy()
+        check(got, ref)
+        blk = ref[:, :, 160:192]
+        s = np.abs(blk).max()
+        assert s > 0
+        check(got[:, :, 160:192] / s, blk / s)
 
 
 def test_single_row_segments_return_v_rows():
@@ -380,9 +407,9 @@ def test_dequant_bf16_bit_exact_with_offset_rows():
 
 
 def test_dequant_mxfp4_bit_exact_through_the_stage1_conversion():
-    # Every byte (two e2m1 codes) meets block exponents 0..20 binades below its
-    # row's largest: within 15 the value is code * 2^(s - 127) exactly (that
-    # covers the e5m2 subnormals at 14 and 15 below), beyond it the block is
+    # Every byte (two e2m1 codes) meets block exponents 0..40 binades below its
+    # row's largest: within 28 the value is code * 2^(s - 127) exactly (that
+    # covers the e5m2 subnormals at 26..28 below), beyond it the block is
     # flushed to zero as in the decode. Two more rows: every scale 254 (values
     # from 2^128 up overflow fp32 on both sides) and every scale 0 (fp32
     # subnormals).
@@ -390,7 +417,7 @@ def test_dequant_mxfp4_bit_exact_through_the_stage1_conversion():
     r = np.arange(rows)[:, None]
     codes = ((r * 7 + np.arange(288)[None, :] * 13) % 256).astype(np.uint8)
     base = 120 + (np.arange(rows) % 9)
-    down = (np.arange(rows)[:, None] * 5 + np.arange(nb)[None, :] * 3) % 21
+    down = (np.arange(rows)[:, None] * 5 + np.arange(nb)[None, :] * 3) % 41
     down[:, 0] = 0  # block 0 holds the row's largest exponent
     scales = (base[:, None] - down).astype(np.uint8)
     scales[64], scales[65] = 254, 0
@@ -405,8 +432,10 @@ def test_dequant_mxfp4_bit_exact_through_the_stage1_conversion():
     scale = oracle.decode_array("e8m0", scales)
     with np.errstate(over="ignore"):
         ref = (elem * np.repeat(scale, 32, axis=1)).astype(np.float32)[2:]
-    flushed = np.repeat((scales.max(axis=1, keepdims=True) - scales.astype(np.int32)) > 15, 32, axis=1)[2:]
+    depth = scales.max(axis=1, keepdims=True) - scales.astype(np.int32)
+    flushed = np.repeat(depth > 28, 32, axis=1)[2:]
     assert flushed.any() and (~flushed).any()
+    assert set(np.unique(depth[:64])) == set(range(41))  # every block distance 0..40 occurs
     bad = np.argwhere((got != ref) & ~flushed & ~(np.isnan(got) & np.isnan(ref)))
     rs, ds = bad[:, 0] + 2, bad[:, 1]
     assert len(bad) == 0, (len(bad), [(int(a), int(d), int(nib[a, d]), int(scales[a, d // 32]),
