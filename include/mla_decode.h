@@ -158,7 +158,7 @@ mla_status_t mla_decode_workspace_size(int32_t batch, int32_t total_q, int32_t t
  *   kv        device, [total_kv][576] bf16 / e4m3 codes, or [total_kv][288]
  *             fp4x2 bytes for mxfp4; 16-byte aligned
  *   kv_scale  device: NULL (bf16), one float (fp8), or [total_kv][18] e8m0
- *             bytes (mxfp4; 2-byte aligned). mxfp4 rows are used as e2m1
+ *             bytes (mxfp4; 16-byte aligned). mxfp4 rows are used as e2m1
  *             values rebased to the row's largest block scale R: every block
  *             whose scale is within 28 of R is used exactly; blocks further
  *             below count as zero (their elements are under 2^-28 of the

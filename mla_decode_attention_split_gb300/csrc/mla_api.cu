@@ -158,7 +158,7 @@ mla_status_t decode_impl(const void* q, const void* kv, const void* kv_scale, co
   if (total_q > 0 && (!q || !out || !aligned16(q) || !aligned16(out))) return MLA_ERR_INVALID_ARG;
   if (total_kv > 0 && (!kv || !aligned16(kv))) return MLA_ERR_INVALID_ARG;
   if (kv_dtype != MLA_DTYPE_BF16 && !kv_scale) return MLA_ERR_INVALID_ARG;
-  if (kv_dtype == MLA_DTYPE_MXFP4 && (reinterpret_cast<uintptr_t>(kv_scale) & 1u) != 0) return MLA_ERR_INVALID_ARG;
+  if (kv_dtype == MLA_DTYPE_MXFP4 && !aligned16(kv_scale)) return MLA_ERR_INVALID_ARG;
   if (opts->q_dtype == MLA_DTYPE_FP8_E4M3 && !opts->q_scale) return MLA_ERR_INVALID_ARG;
   if (opts->quantize_q && opts->q_dtype != MLA_DTYPE_BF16) return MLA_ERR_UNSUPPORTED;
   const bool pairs = opts->token_pairs != 0;

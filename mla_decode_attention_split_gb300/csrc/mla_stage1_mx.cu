@@ -22,24 +22,25 @@
 //      - the raw fp4x2 bytes come in by TMA, in two halves of 64 rows, each
 //        three boxes (bytes 0-127 and 128-255 with 128-byte swizzle, bytes
 //        256-287 with 32-byte swizzle) into a ring of three 20 KB stages; rows
-//        past the end of the cache read as zero. The lanes of the producer
-//        warp load the halves' e8m0 bytes with plain loads into the same stage
-//        (a row's 18 bytes are not 16-byte aligned);
-//      - a converter thread per tile row (= tensor-memory lane) reads its row
-//        from the stage (the swizzle makes the reads conflict-free) and writes
-//        the e5m2 bytes twice: all 576 into tensor memory, where Q.K^T reads
-//        its A operand (144 columns a row), and the 512 V dims into a 64 KB
-//        shared-memory stage in the 128-byte-swizzled layout that P.V reads as
-//        V^T. The K operand therefore never crosses shared memory.
+//        past the end of the cache read as zero. The halves' e8m0 bytes come
+//        along as one bulk copy of the 16-byte units around them (a half's
+//        1152 bytes need not start on a 16-byte boundary);
+//      - two converter threads per tile row (the warps of one tensor-memory
+//        lane quarter, 9 blocks each) read the row from the stage (the
+//        swizzle makes the reads conflict-free) and write the e5m2 bytes
+//        twice: all 576 into tensor memory, where Q.K^T reads its A operand
+//        (144 columns a row), and the 512 V dims into a 64 KB shared-memory
+//        stage in the 128-byte-swizzled layout that P.V reads as V^T. The K
+//        operand therefore never crosses shared memory.
 //  * Buffers: two V stages, two K buffers in tensor memory, two S and two P
 //    buffers, one O accumulator (2 x 144 + 2 x 32 + 128 = 480 of the 512
 //    tensor-memory columns). A tile's stage and K buffer are rewritten once
 //    the P.V of the tile two back is done.
-//  * Roles: warps 0-3 convert, warps 4-7 run the online softmax (thread =
-//    row = tensor-memory lane), warp 8 issues both UMMA kinds from a
+//  * Roles: warps 0-7 convert, warps 8-11 run the online softmax (thread =
+//    row = tensor-memory lane), warp 12 issues both UMMA kinds from a
 //    non-blocking loop (an issue blocks while the tensor pipe's queue is full,
 //    so the issuer is neither a converter nor a softmax warp) and owns tensor
-//    memory, warp 9 loads the raw tiles. Every mbarrier wait is bounded.
+//    memory, warp 13 loads the raw tiles. Every mbarrier wait is bounded.
 //  * Registers: setmaxnreg moves registers from the converting and the
 //    issuing warpgroups to the softmax warpgroup at the start. At the end the
 //    softmax warpgroup gives them back before a CTA barrier, and only after
@@ -57,13 +58,16 @@ using mxcvt::exp2i;
 using mxcvt::rebase_scale2;
 using mxcvt::row_exp;
 
-constexpr int kThreads = 384;                          // three warpgroups
-constexpr int kIssuerWarp = 8;                         // warp 9 loads the raw tiles, warps 10-11 only hold registers
-// Registers per thread: the launch gives 168 to every warpgroup; the softmax
-// warpgroup takes 232 from the converters (160) and the issuing and loading
-// warpgroup (112): 160 + 232 + 112 = 3 x 168, the launch budget exactly.
-constexpr uint32_t kLaunchRegs = 168, kConvRegs = 160, kSoftRegs = 232, kAuxRegs = 112;
-static_assert(kConvRegs + kSoftRegs + kAuxRegs == 3 * kLaunchRegs, "register split must equal the launch budget");
+constexpr int kThreads = 512;                          // four warpgroups
+constexpr int kConvWarps = 8;                          // two per tensor-memory lane quarter, half a row each
+constexpr int kSoftWarp0 = 8;                          // warps 8-11 run the softmax
+constexpr int kIssuerWarp = 12;                        // warp 13 loads the raw tiles, 14-15 only hold registers
+// Registers per thread: the launch gives 128 to every warpgroup; the softmax
+// warpgroup takes 232 from the two converting warpgroups (96 each) and the
+// issuing and loading warpgroup (88): 96 + 96 + 232 + 88 = 4 x 128, the
+// launch budget exactly.
+constexpr uint32_t kLaunchRegs = 128, kConvRegs = 96, kSoftRegs = 232, kAuxRegs = 88;
+static_assert(2 * kConvRegs + kSoftRegs + kAuxRegs == 4 * kLaunchRegs, "register split must equal the launch budget");
 constexpr int kStages = 2;                             // V stages, K buffers, S and P buffers
 constexpr int kHalfRows = 64;                          // raw tiles come in halves of 64 rows
 constexpr int kRawStages = 3;
@@ -72,9 +76,9 @@ constexpr int kRowScales = kDqk / kMxBlock;            // 18 e8m0 bytes a row
 constexpr int kRawBox = kHalfRows * 128;               // one 128-byte-wide box of 64 rows (8 KB)
 constexpr int kRawOffTail = 2 * kRawBox;               // bytes 256-287 of the 64 rows (2 KB)
 constexpr int kRawNibBytes = kHalfRows * kRowBytes;    // 18 KB per half, the TMA transaction
-constexpr int kRawOffSc = kRawNibBytes;                // [64 rows][18] e8m0 bytes
+constexpr int kRawOffSc = kRawNibBytes;                // the 16-byte units holding the 64 rows' e8m0 bytes
 constexpr int kRawStageBytes = 20 * 1024;
-static_assert(kRawOffSc + kHalfRows * kRowScales <= kRawStageBytes, "raw stage");
+static_assert(kRawOffSc + kHalfRows * kRowScales + 30 <= kRawStageBytes && kRawOffSc % 16 == 0, "raw stage");
 // tensor-memory columns
 constexpr uint32_t kTmS = 0;          // S: 2 buffers x 32
 constexpr uint32_t kTmK = 64;         // K operand buffer b at kTmK + kTmKStride b, 144 columns
@@ -88,18 +92,21 @@ struct L {
   static constexpr int kOffRaw = kOffKv + kStages * kVBytes;             // raw halves
   static constexpr int kOffQ = kOffRaw + kRawStages * kRawStageBytes;
   static constexpr int kOffP = kOffQ + kQBytes;                          // 2 x 4 KB
-  static constexpr int kOffRexp = kOffP + kStages * kPBytes;             // [2][128] u8: R of each row
-  static constexpr int kOffRedMax = kOffRexp + kStages * kTileRows;      // [2][4][16] f32
+  static constexpr int kOffRexp = kOffP + kStages * kPBytes;             // [4][128] u8: R of each row
+  static constexpr int kOffRedMax = kOffRexp + 4 * kTileRows;            // [2][4][16] f32
   static constexpr int kOffRedMu = kOffRedMax + 2 * 4 * 16 * 4;          // [2][4][16] f32
   static constexpr int kOffRedL = kOffRedMu + 2 * 4 * 16 * 4;            // [4][16] f32
   static constexpr int kOffAmax = kOffRedL + 4 * 16 * 4;                 // [4] u32
   static constexpr int kOffMList = kOffAmax + 16;                        // MergeList (64 B)
-  static constexpr int kOffScan = kOffMList + 64;                        // 16 x i64
-  static constexpr int kOffMeta = kOffScan + 16 * 8;                     // [4] u32: tile i in slot i % 4
+  static constexpr int kOffScan = kOffMList + 64;                        // 24 x i64
+  static constexpr int kOffMeta = kOffScan + 24 * 8;                     // [4] u32: tile i in slot i % 4
   static constexpr int kOffBars = kOffMeta + 16;
+  // kKvFull and the row exponents have four slots (tile i in slot i % 4): the
+  // converters run up to two tiles ahead of the softmax, which still reads
+  // them, while K buffers and V stages have two (tile i in i % 2)
   enum {
-    kKvFull = 0, kSFull = 2, kSEmpty = 4, kPFull = 6, kPvDone = 8, kQFull = 10, kQEmpty = 11, kOFull = 12,
-    kOEmpty = 13, kGrp = 14, kRawFull = 16, kRawEmpty = 19, kDrain = 22, kMerge = 23, kNumBars = 24
+    kKvFull = 0, kSFull = 4, kSEmpty = 6, kPFull = 8, kPvDone = 10, kQFull = 12, kQEmpty = 13, kOFull = 14,
+    kOEmpty = 15, kGrp = 16, kRawFull = 18, kRawEmpty = 21, kDrain = 24, kMerge = 25, kVFull = 26, kNumBars = 28
   };
   static constexpr int kMergeBytes = kStages * kVBytes;  // the V stages hold partials for the end-of-CTA merge
   static constexpr int kOffSlot = kOffBars + kNumBars * 8;
@@ -108,8 +115,9 @@ struct L {
   static constexpr int kAlloc = kBytes + 1024;
   template <class C>
   __device__ static void init_barriers(const C& cx) {
+    for (int i = 0; i < 4; ++i) mbar_init(cx.bar(kKvFull + i), kConvWarps);  // K operand in tensor memory
     for (int i = 0; i < kStages; ++i) {
-      mbar_init(cx.bar(kKvFull + i), 4);  // the 4 converter warps
+      mbar_init(cx.bar(kVFull + i), kConvWarps);  // V dims of the tile in the V stage
       mbar_init(cx.bar(kSFull + i), 1);
       mbar_init(cx.bar(kSEmpty + i), 4);
       mbar_init(cx.bar(kPFull + i), 4);
@@ -118,7 +126,7 @@ struct L {
     }
     for (int i = 0; i < kRawStages; ++i) {
       mbar_init(cx.bar(kRawFull + i), 1);   // the producer (TMA bytes + scales)
-      mbar_init(cx.bar(kRawEmpty + i), 2);  // the 2 converter warps of that half
+      mbar_init(cx.bar(kRawEmpty + i), 4);  // the 4 converter warps that read that half
     }
     mbar_init(cx.bar(kQFull), 4);
     mbar_init(cx.bar(kQEmpty), 1);
@@ -148,7 +156,7 @@ __device__ __forceinline__ uint32_t ld_nc_u16(const void* p) {
 }
 
 // ---------------------------------------------------------------------------
-// Warp 9: the raw halves of each tile into the ring, half j into stage j % 3
+// Warp 13: the raw halves of each tile into the ring, half j into stage j % 3
 // once the converters of half j - 3 have read it.
 __device__ void producer_role(const Stage1Params& p, const Cx& cx, const RawMaps* maps, PieceCursor cur, int lane) {
   const uint64_t pol = policy_evict_first();
@@ -156,8 +164,9 @@ __device__ void producer_role(const Stage1Params& p, const Cx& cx, const RawMaps
     prefetch_tensormap(&maps->wide);
     prefetch_tensormap(&maps->tail);
   }
-  const uint8_t* scales = static_cast<const uint8_t*>(p.kv_scale);
+  const uint8_t* scales = static_cast<const uint8_t*>(p.kv_scale);  // 16-byte aligned (checked by the host)
   const int64_t sc_end = static_cast<int64_t>(p.total_kv) * kRowScales;
+  const int64_t sc_full = sc_end & ~int64_t{15};  // bytes readable in whole 16-byte units
   TileWalker tw;
   tw.init(cur);
   uint32_t j = 0;
@@ -167,29 +176,28 @@ __device__ void producer_role(const Stage1Params& p, const Cx& cx, const RawMaps
     for (int hh = 0; hh < 2; ++hh) {
       const uint32_t s = j % kRawStages, rnd = j / kRawStages;
       const int32_t r0 = row0 + hh * kHalfRows;
-      // the half's 64 x 18 e8m0 bytes as 16-bit words, 18 per lane (rows past
-      // the end of the cache read as zero), loaded before the stage is free
-      uint32_t w[18];
+      // the half's e8m0 bytes [sb, se) come in as the 16-byte units [a, b)
+      // around them; bytes of the cache's last partial unit by plain loads
       const int64_t sb = static_cast<int64_t>(r0) * kRowScales;
-#pragma unroll
-      for (int k = 0; k < 18; ++k) {
-        const int64_t off = sb + 2 * (32 * k + lane);
-        w[k] = off + 2 <= sc_end ? ld_nc_u16(scales + off) : 0u;
-      }
+      const int64_t se = min(sb + kHalfRows * kRowScales, sc_end);
+      const int64_t a = sb & ~int64_t{15};
+      const int64_t b = min((se + 15) & ~int64_t{15}, sc_full);
+      const uint32_t win = b > a ? static_cast<uint32_t>(b - a) : 0u;
       if (rnd >= 1 && !cx.wait(L::kRawEmpty + s, (rnd - 1) & 1u)) {
         ok = false;
         break;
       }
       const uint32_t dst = cx.s + L::kOffRaw + s * kRawStageBytes;
       if (lane == 0) {
-        mbar_expect_tx(cx.bar(L::kRawFull + s), kRawNibBytes);
+        mbar_expect_tx(cx.bar(L::kRawFull + s), kRawNibBytes + win);
         tma_load_2d(dst, &maps->wide, 0, r0, cx.bar(L::kRawFull + s), pol);
         tma_load_2d(dst + kRawBox, &maps->wide, 128, r0, cx.bar(L::kRawFull + s), pol);
         tma_load_2d(dst + kRawOffTail, &maps->tail, 256, r0, cx.bar(L::kRawFull + s), pol);
+        if (win) bulk_g2s(dst + kRawOffSc, scales + a, win, cx.bar(L::kRawFull + s), pol);
       }
       uint8_t* scd = cx.g + L::kOffRaw + s * kRawStageBytes + kRawOffSc;
-#pragma unroll
-      for (int k = 0; k < 18; ++k) *reinterpret_cast<uint16_t*>(scd + 2 * (32 * k + lane)) = static_cast<uint16_t>(w[k]);
+      for (int64_t off = max(b, sb) + 2 * lane; off < se; off += 64)
+        *reinterpret_cast<uint16_t*>(scd + (off - a)) = static_cast<uint16_t>(ld_nc_u16(scales + off));
       __syncwarp();
       if (lane == 0) mbar_arrive(cx.bar(L::kRawFull + s));
       ++j;
@@ -203,87 +211,107 @@ __device__ void producer_role(const Stage1Params& p, const Cx& cx, const RawMaps
 }
 
 // ---------------------------------------------------------------------------
-// Converters (warps 0-3; thread = tile row = tensor-memory lane).
+// Converters (warps 0-7; two threads per tile row, in its tensor-memory lane).
 
-// Row rr of the raw half at `raw` (tile row `row`): the rebased e5m2 bytes
-// into tensor-memory columns tk.. (all 576) and into the V stage (dims 0-511,
-// 128-byte-swizzled K-major rows); records R.
-__device__ __forceinline__ void convert_row(const uint8_t* raw, int rr, uint8_t* vstage, int row, uint32_t tk,
-                                            uint8_t* rexp) {
-  const uint8_t* sc = raw + kRawOffSc + rr * kRowScales;
-  uint32_t scw[9];
+// Blocks [bl0, bl0 + 9) of row rr of the raw half at `raw` (the row's scale
+// bytes start sc0 bytes into the stage's scale window): the rebased e5m2 bytes
+// into tensor-memory columns tk + 8 bl. Returns R.
+__device__ __forceinline__ uint32_t convert_half_row(const uint8_t* raw, int sc0, int rr, uint32_t tk, int bl0) {
+  const uint8_t* sc = raw + kRawOffSc + sc0 + rr * kRowScales;
   uint32_t R = 0;
 #pragma unroll
   for (int k = 0; k < 9; ++k) {
-    scw[k] = *reinterpret_cast<const uint16_t*>(sc + 2 * k);
-    R = max(R, max(scw[k] & 0xFFu, scw[k] >> 8));
+    const uint32_t h = *reinterpret_cast<const uint16_t*>(sc + 2 * k);
+    R = max(R, max(h & 0xFFu, h >> 8));
   }
-  const int sw = row & 7, swa = rr & 7, swt = (rr >> 2) & 1;
+  const int swa = rr & 7, swt = (rr >> 2) & 1;
 #pragma unroll 1
-  for (int bp = 0; bp < 9; ++bp) {  // blocks 2 bp, 2 bp + 1: bytes 32 bp .. 32 bp + 31
-    uint4 v0, v1;
-    if (bp < 8) {
-      const uint8_t* rb = raw + (bp >> 2) * kRawBox + rr * 128;
-      const int u0 = 2 * (bp & 3);
-      v0 = *reinterpret_cast<const uint4*>(rb + ((u0 ^ swa) << 4));
-      v1 = *reinterpret_cast<const uint4*>(rb + (((u0 + 1) ^ swa) << 4));
-    } else {
-      const uint8_t* rb = raw + kRawOffTail + rr * 32;
-      v0 = *reinterpret_cast<const uint4*>(rb + (swt << 4));
-      v1 = *reinterpret_cast<const uint4*>(rb + ((swt ^ 1) << 4));
-    }
-    const uint32_t s2 = bp < 8 ? scw[bp] : scw[8];
-    uint4 a0, a1, b0, b1;
-    convert_block(v0, rebase_scale2(R - (s2 & 0xFFu)), a0, a1);
-    convert_block(v1, rebase_scale2(R - (s2 >> 8)), b0, b1);
-    if (bp < 8) {  // V dims 64 bp .. 64 bp + 63: chunk bp / 2, 16-byte units 4 (bp % 2) ..
-      uint8_t* vb = vstage + (bp >> 1) * kChunkBytes + row * 128;
-      const int u = 4 * (bp & 1);
-      *reinterpret_cast<uint4*>(vb + ((u ^ sw) << 4)) = a0;
-      *reinterpret_cast<uint4*>(vb + (((u + 1) ^ sw) << 4)) = a1;
-      *reinterpret_cast<uint4*>(vb + (((u + 2) ^ sw) << 4)) = b0;
-      *reinterpret_cast<uint4*>(vb + (((u + 3) ^ sw) << 4)) = b1;
-    }
-    const uint32_t w[16] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w,
-                            b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
-    tmem_st16(tk + 16 * bp, w);
+  for (int bl = bl0; bl < bl0 + 9; ++bl) {  // block bl: fp4x2 bytes 16 bl .. 16 bl + 15
+    const uint8_t* src = bl < 16 ? raw + (bl >> 3) * kRawBox + rr * 128 + (((bl & 7) ^ swa) << 4)
+                                 : raw + kRawOffTail + rr * 32 + (((bl - 16) ^ swt) << 4);
+    const uint4 v = *reinterpret_cast<const uint4*>(src);
+    uint4 lo, hi;
+    convert_block(v, rebase_scale2(R - sc[bl]), lo, hi);
+    const uint32_t w[8] = {lo.x, lo.y, lo.z, lo.w, hi.x, hi.y, hi.z, hi.w};
+    tmem_st8(tk + 8 * bl, w);
   }
-  rexp[row] = static_cast<uint8_t>(R);
+  return R;
 }
 
+// V blocks [bl0, bl1) of tile row `row` (dims 32 bl .. 32 bl + 31), copied from
+// the K operand in tensor memory (columns tk + 8 bl) into the V stage: 128-byte
+// -swizzled K-major rows, 16 KB per 128 dims. Four blocks per tensor-memory
+// wait.
+__device__ __forceinline__ void copy_v_blocks(uint32_t tk, uint8_t* vstage, int row, int bl0, int bl1) {
+  const int sw = row & 7;
+  for (int g = bl0; g < bl1; g += 4) {
+    const int n = min(4, bl1 - g);
+    uint32_t w[4][8];
+#pragma unroll
+    for (int k = 0; k < 4; ++k)
+      if (k < n) tmem_ld8(tk + 8 * (g + k), w[k]);
+    tmem_wait_ld();
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      if (k < n) {
+        const int bl = g + k, u = 2 * (bl & 3);
+        uint8_t* vb = vstage + (bl >> 2) * kChunkBytes + row * 128;
+        *reinterpret_cast<uint4*>(vb + ((u ^ sw) << 4)) = make_uint4(w[k][0], w[k][1], w[k][2], w[k][3]);
+        *reinterpret_cast<uint4*>(vb + (((u + 1) ^ sw) << 4)) = make_uint4(w[k][4], w[k][5], w[k][6], w[k][7]);
+      }
+    }
+  }
+}
+
+// Warps 0-7: warp w converts blocks 9 (w / 4) .. 9 (w / 4) + 8 of tile rows
+// 32 (w % 4) .. + 31 (its tensor-memory lane quarter) into tensor memory, and
+// once the V stage is free copies the V dims among them into it. The V stage
+// is thus held only from that copy to the tile's P.V, not through the
+// conversion, Q.K^T and softmax.
 __device__ void converter_role(const Cx& cx, PieceCursor cur, int warp, int lane) {
   const uint32_t ntiles = static_cast<uint32_t>(count_tiles(cur));
   volatile uint32_t* meta_slot = reinterpret_cast<volatile uint32_t*>(cx.g + L::kOffMeta);
   MetaTileWalker rw;
   rw.init(cur);
-  const int row = 32 * warp + lane, hh = warp >> 1, rr = 32 * (warp & 1) + lane;
-  const uint32_t lane_base = static_cast<uint32_t>(32 * warp) << 16;
+  const int q4 = warp & 3, part = warp >> 2;
+  const int row = 32 * q4 + lane, hh = q4 >> 1, rr = 32 * (q4 & 1) + lane;
+  const uint32_t lane_base = static_cast<uint32_t>(32 * q4) << 16;
   for (uint32_t i = 0; i < ntiles; ++i) {
     int32_t row0 = 0;
     uint32_t meta = 0;
     rw.next(row0, meta);
     const uint32_t b = i & 1u;
-    // stage b and K buffer b are free once the P.V of tile i - 2 is done
-    if (i >= 2 && !cx.wait(L::kPvDone + b, ((i - 2) >> 1) & 1u)) return;
+    const uint32_t tk = cx.tmem + lane_base + kTmK + b * kTmKStride;
+    // K buffer b is free once the Q.K^T of tile i - 2 is done (this warp's
+    // copy out of it came before, in program order)
+    if (i >= 2 && !cx.wait(L::kSFull + b, ((i - 2) >> 1) & 1u)) return;
     const uint32_t j = 2 * i + static_cast<uint32_t>(hh), s = j % kRawStages;
     if (!cx.wait(L::kRawFull + s, (j / kRawStages) & 1u)) return;
     tc_fence_after();
-    convert_row(cx.g + L::kOffRaw + s * kRawStageBytes, rr, cx.g + L::kOffKv + b * kVBytes, row,
-                cx.tmem + lane_base + kTmK + b * kTmKStride, cx.g + L::kOffRexp + b * kTileRows);
+    const int sc0 = static_cast<int>((static_cast<int64_t>(row0 + hh * kHalfRows) * kRowScales) & 15);
+    const uint32_t R = convert_half_row(cx.g + L::kOffRaw + s * kRawStageBytes, sc0, rr, tk, 9 * part);
     __syncwarp();
     if (lane == 0) mbar_arrive(cx.bar(L::kRawEmpty + s));
+    if (part == 0) cx.g[L::kOffRexp + (i & 3u) * kTileRows + row] = static_cast<uint8_t>(R);
     if (warp == 0 && lane == 0) meta_slot[i & 3u] = meta;
-    // the stage's shared-memory bytes and the tensor-memory stores, visible to the tensor core
+    // the tensor-memory stores, visible to the tensor core
     tmem_wait_st();
+    tc_fence_before();
+    __syncwarp();
+    if (lane == 0) mbar_arrive(cx.bar(L::kKvFull + (i & 3u)));
+    // V stage b is free once the P.V of tile i - 2 is done
+    if (i >= 2 && !cx.wait(L::kPvDone + b, ((i - 2) >> 1) & 1u)) return;
+    tc_fence_after();
+    copy_v_blocks(tk, cx.g + L::kOffKv + b * kVBytes, row, part == 0 ? 0 : 9, part == 0 ? 9 : 16);
     fence_async_smem();
     tc_fence_before();
     __syncwarp();
-    if (lane == 0) mbar_arrive(cx.bar(L::kKvFull + b));
+    if (lane == 0) mbar_arrive(cx.bar(L::kVFull + b));
   }
 }
 
 // ---------------------------------------------------------------------------
-// Warp 8, lane 0: issues Q.K^T of tile qi and P.V of tile pi as soon as each
+// Warp 12, lane 0: issues Q.K^T of tile qi and P.V of tile pi as soon as each
 // is ready (non-blocking tests, bounded overall), in tile order for each kind.
 constexpr uint32_t kIdQK = umma_idesc(128, 32, 1, 0, false, false);  // A e5m2 from tensor memory, B e4m3
 constexpr uint32_t kIdPV = umma_idesc(128, 32, 1, 0, true, true);    // A = V^T MN-major, B = P^T MN-major
@@ -291,10 +319,11 @@ constexpr uint32_t kIdPV = umma_idesc(128, 32, 1, 0, true, true);    // A = V^T 
 __device__ __forceinline__ void issue_qk(const Cx& cx, uint32_t i, const TileMeta& t) {
   const uint32_t b = i & 1u;
   tc_fence_after();
-  const uint32_t qbuf = cx.s + L::kOffQ, ka = cx.tmem + kTmK + b * kTmKStride;
-  const uint32_t d = cx.tmem + kTmS + 32 * b;
+  const uint32_t ka = cx.tmem + kTmK + b * kTmKStride, d = cx.tmem + kTmS + 32 * b;
+  const uint64_t qb = qk_desc_b(cx.s + L::kOffQ, 0);
 #pragma unroll
-  for (int ks = 0; ks < kDqk / 32; ++ks) umma_e4m3_ta(d, ka + 8 * ks, qk_desc_b(qbuf, ks), kIdQK, ks > 0 ? 1u : 0u);
+  for (int ks = 0; ks < kDqk / 32; ++ks)
+    umma_e4m3_ta(d, ka + 8 * ks, desc_add(qb, (ks >> 2) * kQChunkBytes + (ks & 3) * 32), kIdQK, ks > 0 ? 1u : 0u);
   umma_commit(cx.bar(L::kSFull + b));
   if (t.last) umma_commit(cx.bar(L::kQEmpty));
 }
@@ -302,13 +331,14 @@ __device__ __forceinline__ void issue_qk(const Cx& cx, uint32_t i, const TileMet
 __device__ __forceinline__ void issue_pv(const Cx& cx, uint32_t i, const TileMeta& t) {
   const uint32_t b = i & 1u;
   tc_fence_after();
-  const uint32_t stage = cx.s + L::kOffKv + b * kVBytes, pbuf = cx.s + L::kOffP + b * kPBytes;
+  const uint64_t va = pv_desc_a(cx.s + L::kOffKv + b * kVBytes, 0, 0), pb = pv_desc_b(cx.s + L::kOffP + b * kPBytes, 0);
   const uint32_t obuf = cx.tmem + kTmO;
 #pragma unroll
   for (int mb = 0; mb < 4; ++mb)
 #pragma unroll
     for (int ks = 0; ks < 4; ++ks)
-      umma_e4m3(obuf + 32 * mb, pv_desc_a(stage, mb, ks), pv_desc_b(pbuf, ks), kIdPV, (ks > 0 || !t.first) ? 1u : 0u);
+      umma_e4m3(obuf + 32 * mb, desc_add(va, mb * kChunkBytes + ks * 4096), desc_add(pb, ks * 1024), kIdPV,
+                (ks > 0 || !t.first) ? 1u : 0u);
   umma_commit(cx.bar(L::kPvDone + b));
   if (t.last) umma_commit(cx.bar(L::kOFull));
 }
@@ -320,7 +350,8 @@ __device__ void issuer_role(const Cx& cx, PieceCursor cur) {
   long long t0 = clock64();
   while (pi < n) {
     bool progressed = false;
-    if (pi < qi && mbar_test_wait(cx.bar(L::kPFull + (pi & 1u)), (pi >> 1) & 1u)) {
+    if (pi < qi && mbar_test_wait(cx.bar(L::kPFull + (pi & 1u)), (pi >> 1) & 1u) &&
+        mbar_test_wait(cx.bar(L::kVFull + (pi & 1u)), (pi >> 1) & 1u)) {
       const TileMeta t = TileMeta::unpack(meta[pi & 3u]);
       // the first P.V of piece k overwrites O: the epilogue of piece k - 1 has read it
       if (!t.first || t.k == 0 || mbar_test_wait(cx.bar(L::kOEmpty), (t.k - 1) & 1u)) {
@@ -329,7 +360,7 @@ __device__ void issuer_role(const Cx& cx, PieceCursor cur) {
         progressed = true;
       }
     }
-    if (qi < n && mbar_test_wait(cx.bar(L::kKvFull + (qi & 1u)), (qi >> 1) & 1u) &&
+    if (qi < n && mbar_test_wait(cx.bar(L::kKvFull + (qi & 3u)), (qi >> 2) & 1u) &&
         (qi < 2 || mbar_test_wait(cx.bar(L::kSEmpty + (qi & 1u)), ((qi - 2) >> 1) & 1u))) {
       const TileMeta t = TileMeta::unpack(meta[qi & 3u]);
       if (!t.first || mbar_test_wait(cx.bar(L::kQFull), t.k & 1u)) {
@@ -354,12 +385,12 @@ __device__ void issuer_role(const Cx& cx, PieceCursor cur) {
 }
 
 // ---------------------------------------------------------------------------
-// Softmax (warps 4-7).
+// Softmax (warps 8-11).
 template <int QF>
 __device__ void softmax_role(const Stage1Params& p, const Cx& cx, PieceCursor cur, int warp, int lane) {
   SoftmaxCtx sx;
   sx.lane = lane;
-  sx.wi = warp - 4;
+  sx.wi = warp - kSoftWarp0;
   sx.row = 32 * (warp & 3) + lane;
   sx.lane_base = static_cast<uint32_t>(32 * (warp & 3)) << 16;
   sx.gcount = 0;
@@ -387,9 +418,9 @@ __device__ void softmax_role(const Stage1Params& p, const Cx& cx, PieceCursor cu
       const uint32_t b = i & 1u;
       const bool valid = sx.row < nr;
       if (!cx.wait(L::kSFull + b, (i >> 1) & 1u)) return;
-      // the converters' row exponents of this stage (already complete: Q.K^T read the stage)
-      if (!cx.wait(L::kKvFull + b, (i >> 1) & 1u)) return;
-      const int r = row_exp(cx.g[L::kOffRexp + b * kTileRows + sx.row]);
+      // the converters' row exponents of this tile (already complete: Q.K^T read its K operand)
+      if (!cx.wait(L::kKvFull + (i & 3u), (i >> 2) & 1u)) return;
+      const int r = row_exp(cx.g[L::kOffRexp + (i & 3u) * kTileRows + sx.row]);
       tc_fence_after();
       uint32_t sr[32];
       tmem_ld32(cx.tmem + sx.lane_base + kTmS + 32 * b, sr);
@@ -503,11 +534,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   PieceCursor cur;
   if (!cta_begin(p, cx, smem_raw, kIssuerWarp, cur)) return;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  if (warp < 4) {
+  if (warp < kSoftWarp0) {
     setmaxnreg_dec<kConvRegs>();
     converter_role(cx, cur, warp, lane);
-  } else if (warp < 8) {
-    setmaxnreg_inc<kSoftRegs>();  // granted once warpgroups 0 and 2 have made their decreases (unconditional)
+  } else if (warp < kIssuerWarp) {
+    setmaxnreg_inc<kSoftRegs>();  // granted once warpgroups 0, 1 and 3 have made their decreases (unconditional)
     softmax_role<QF>(p, cx, cur, warp, lane);
     setmaxnreg_dec<kLaunchRegs>();
   } else {
@@ -519,10 +550,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       producer_role(p, cx, &maps, cur, lane);
     }
   }
-  // Warpgroup 1 returned its extra registers before this barrier: the
-  // increases below are always granted at once.
+  // The softmax warpgroup returned its extra registers before this barrier:
+  // the increases below are always granted at once.
   __syncthreads();
-  if (warp < 4 || warp >= 8) setmaxnreg_inc<kLaunchRegs>();
+  if (warp < kSoftWarp0 || warp >= kIssuerWarp) setmaxnreg_inc<kLaunchRegs>();
   cta_end(p, cx, kIssuerWarp);
 }
 

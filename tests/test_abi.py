@@ -121,6 +121,11 @@ def test_argument_checks_fail_before_any_device_work(lib):
                       ctypes.c_void_p(aligned), ctypes.c_void_p(aligned), m.BF16, ctypes.byref(opts), None)
     assert st == m.MLA_ERR_UNSUPPORTED
     opts.quantize_q = 0
+    # mxfp4 block scales must be 16-byte aligned (they come in by bulk copies)
+    st = L.mla_decode(ctypes.c_void_p(aligned), ctypes.c_void_p(aligned), ctypes.c_void_p(aligned + 2),
+                      ctypes.c_void_p(aligned), ctypes.c_void_p(aligned), ctypes.c_void_p(aligned), m.MXFP4,
+                      ctypes.byref(opts), None)
+    assert st == m.MLA_ERR_INVALID_ARG
     # missing workspace
     opts.q_dtype = m.BF16
     st = L.mla_decode(ctypes.c_void_p(aligned), ctypes.c_void_p(aligned), None, ctypes.c_void_p(aligned),
