@@ -60,6 +60,8 @@ enum HeaderWord : int { kHdrFlags = 0, kHdrCounters = 1, kHdrQAmax = 2, kHdrQSca
 cudaError_t launch_stage1(int kv_fmt, int q_fmt, const Stage1Params& p, cudaStream_t stream);
 // fp8 KV on the tcgen05 tensor cores (mla_stage1_tc.cu)
 cudaError_t launch_stage1_tc_fp8(int q_fmt, const Stage1Params& p, cudaStream_t stream);
+// bf16 KV on the tcgen05 tensor cores (mla_stage1_bf.cu)
+cudaError_t launch_stage1_tc_bf16(int q_fmt, const Stage1Params& p, cudaStream_t stream);
 // mxfp4 KV on the tcgen05 tensor cores (mla_stage1_mx.cu)
 cudaError_t launch_stage1_tc_mxfp4(int q_fmt, const Stage1Params& p, cudaStream_t stream);
 cudaError_t launch_dequant(const void* kv, const void* kv_scale, int kv_fmt, int32_t total_kv, int32_t row0,

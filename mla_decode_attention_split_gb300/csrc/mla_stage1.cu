@@ -757,9 +757,7 @@ bool stage1_supported(int kv_fmt, int q_fmt) {
 cudaError_t launch_stage1(int kv_fmt, int q_fmt, const Stage1Params& p, cudaStream_t stream) {
   if (kv_fmt == kKvFp8) return launch_stage1_tc_fp8(q_fmt, p, stream);
   if (kv_fmt == kKvMxfp4) return launch_stage1_tc_mxfp4(q_fmt, p, stream);
-  if (kv_fmt == kKvBf16) {
-    return q_fmt == kQBf16 ? launch_t<kKvBf16, kQBf16>(p, stream) : launch_t<kKvBf16, kQFp8>(p, stream);
-  }
+  if (kv_fmt == kKvBf16) return launch_stage1_tc_bf16(q_fmt, p, stream);
   return cudaErrorInvalidValue;
 }
 
