@@ -508,8 +508,11 @@ __device__ __forceinline__ bool finish_partial(const Stage1Params& p, const Ctx<
 }
 
 // The end-of-CTA merges, by all kThreads threads. Slots come into the stage
-// buffers in batches of up to kSlots by bulk copies (one round trip a batch);
-// each thread keeps an online (running max) merge of its float4 elements.
+// buffers in batches of up to kSlots by bulk copies (one round trip a batch).
+// The merge weights depend only on (slot, head): per batch, 16 threads (one
+// per head) update the running maximum M of the LSEs, the rescale factor of
+// what was merged so far, the batch's weights 2^(lse - M) and their running
+// sum, and every thread then accumulates its float4 elements with FMAs.
 template <class LL>
 __device__ void merge_listed(const Stage1Params& p, const Ctx<LL>& cx) {
   constexpr int kThr = LL::kThreads;
@@ -519,17 +522,23 @@ __device__ void merge_listed(const Stage1Params& p, const Ctx<LL>& cx) {
   static_assert(kSlots >= 1, "merge buffers");
   const MergeList* ml = reinterpret_cast<const MergeList*>(cx.g + LL::kOffMList);
   const uint32_t nm = ml->n;
-  const float* lsebuf = reinterpret_cast<const float*>(cx.g + LL::kOffQ);
+  // scratch in the (free) Q buffer: the batch's LSEs [kSlots][16], weights
+  // [kSlots][16], and per head the rescale factor, running max and sum
+  float* lsebuf = reinterpret_cast<float*>(cx.g + LL::kOffQ);
+  float* wbuf = lsebuf + kSlots * kHeads;
+  float* scbuf = wbuf + kSlots * kHeads;
+  float* mbuf = scbuf + kHeads;
+  float* sbuf = mbuf + kHeads;
   uint32_t batch = 0;
   for (uint32_t e = 0; e < nm; ++e) {
     const int token = ml->token[e];
     const int64_t c0 = ml->c0[e], np = static_cast<int64_t>(ml->c1[e]) - c0 + 1;
-    float acc[kF][4], mrun[kF], wsum[kF];
+    float4 acc[kF];
 #pragma unroll
-    for (int i = 0; i < kF; ++i) {
-      mrun[i] = -INFINITY;
-      wsum[i] = 0.f;
-      acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = 0.f;
+    for (int i = 0; i < kF; ++i) acc[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (threadIdx.x < kHeads) {
+      mbuf[threadIdx.x] = -INFINITY;
+      sbuf[threadIdx.x] = 0.f;
     }
     for (int64_t s0 = 0; s0 < np; s0 += kSlots) {
       const int nb = static_cast<int>(np - s0 < kSlots ? np - s0 : static_cast<int64_t>(kSlots));
@@ -548,24 +557,39 @@ __device__ void merge_listed(const Stage1Params& p, const Ctx<LL>& cx) {
       // leave the others at the barrier below)
       if (!__syncthreads_and(cx.wait(LL::kMerge, batch & 1u) ? 1 : 0)) return;
       ++batch;
+      if (threadIdx.x < kHeads) {
+        const int h = threadIdx.x;
+        float mn = mbuf[h];
+        for (int j = 0; j < nb; ++j) mn = fmaxf(mn, lsebuf[j * kHeads + h]);
+        const float sc = fast_exp2(mbuf[h] - mn);
+        float sum = sbuf[h] * sc;
+        for (int j = 0; j < nb; ++j) {
+          const float w = fast_exp2(lsebuf[j * kHeads + h] - mn);
+          wbuf[j * kHeads + h] = w;
+          sum += w;
+        }
+        scbuf[h] = sc;
+        mbuf[h] = mn;
+        sbuf[h] = sum;
+      }
+      __syncthreads();
       const float4* obuf = reinterpret_cast<const float4*>(cx.g + LL::kOffKv);
 #pragma unroll
       for (int i = 0; i < kF; ++i) {
         const int f = threadIdx.x + i * kThr;
         if (f < kHeads * kDv / 4) {
           const int h = f >> 7;  // 128 float4 per head
+          const float sc = scbuf[h];
+          float4 a = make_float4(acc[i].x * sc, acc[i].y * sc, acc[i].z * sc, acc[i].w * sc);
           for (int j = 0; j < nb; ++j) {
-            const float lse = lsebuf[j * kHeads + h];
-            const float mn = fmaxf(mrun[i], lse);
-            const float sc = fast_exp2(mrun[i] - mn), w = fast_exp2(lse - mn);
+            const float w = wbuf[j * kHeads + h];
             const float4 v = obuf[j * (kSlotBytes / 16) + f];
-            acc[i][0] = acc[i][0] * sc + w * v.x;
-            acc[i][1] = acc[i][1] * sc + w * v.y;
-            acc[i][2] = acc[i][2] * sc + w * v.z;
-            acc[i][3] = acc[i][3] * sc + w * v.w;
-            wsum[i] = wsum[i] * sc + w;
-            mrun[i] = mn;
+            a.x = fmaf(w, v.x, a.x);
+            a.y = fmaf(w, v.y, a.y);
+            a.z = fmaf(w, v.z, a.z);
+            a.w = fmaf(w, v.w, a.w);
           }
+          acc[i] = a;
         }
       }
       __syncthreads();  // the buffers are free for the next batch
@@ -575,12 +599,13 @@ __device__ void merge_listed(const Stage1Params& p, const Ctx<LL>& cx) {
     for (int i = 0; i < kF; ++i) {
       const int f = threadIdx.x + i * kThr;
       if (f < kHeads * kDv / 4) {
-        const float inv = 1.0f / wsum[i];
+        const float inv = 1.0f / sbuf[f >> 7];
         *reinterpret_cast<uint2*>(dst + 4 * f) =
-            make_uint2(pack_bf16x2(acc[i][0] * inv, acc[i][1] * inv), pack_bf16x2(acc[i][2] * inv, acc[i][3] * inv));
+            make_uint2(pack_bf16x2(acc[i].x * inv, acc[i].y * inv), pack_bf16x2(acc[i].z * inv, acc[i].w * inv));
       }
     }
     if (threadIdx.x == 0) p.tok_cnt[token] = 0u;
+    __syncthreads();  // the per-head sums are read before the next token resets them
   }
 }
 
