@@ -117,8 +117,9 @@ typedef struct {
   int32_t token_pairs;    /* nonzero: the query tokens of each segment are taken
                              in pairs (the last one alone if q_len is odd) that
                              share one pass over the segment's KV rows, for
-                             multi-token decode (q_len > 1). fp8 KV only (else
-                             MLA_ERR_UNSUPPORTED), not with a page table. The
+                             multi-token decode (q_len > 1). fp8 or bf16 KV
+                             (mxfp4: MLA_ERR_UNSUPPORTED), not with a page
+                             table. The
                              workspace must be sized by
                              mla_decode_pairs_workspace_size(). Each token's
                              arithmetic is unchanged: with num_splits = 1 the

@@ -160,7 +160,7 @@ def decode(q, kv, kv_scale, qo_indptr, kv_indptr, out, kv_dtype: int, *, workspa
     """mla_decode() on torch CUDA tensors (layouts as in mla_decode.h). Asynchronous.
     events: optional three CUDA events recorded before and after the launch (1 and 2 back to back).
     quantize_q: quantise bf16 q to e4m3 per tensor inside the call (the a8w8 mode; fp8 KV only).
-    token_pairs: a segment's query tokens share each pass over its KV rows in pairs (fp8 KV only;
+    token_pairs: a segment's query tokens share each pass over its KV rows in pairs (fp8 or bf16 KV;
     the workspace comes from pairs_workspace_size)."""
     opts = make_opts(qo_indptr.numel() - 1, q.shape[0], kv.shape[0], q_dtype=q_dtype, q_scale=q_scale,
                      sm_scale=sm_scale, num_splits=num_splits, workspace=workspace, events=events,

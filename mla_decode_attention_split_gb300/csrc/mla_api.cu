@@ -162,7 +162,7 @@ mla_status_t decode_impl(const void* q, const void* kv, const void* kv_scale, co
   if (opts->q_dtype == MLA_DTYPE_FP8_E4M3 && !opts->q_scale) return MLA_ERR_INVALID_ARG;
   if (opts->quantize_q && opts->q_dtype != MLA_DTYPE_BF16) return MLA_ERR_UNSUPPORTED;
   const bool pairs = opts->token_pairs != 0;
-  if (pairs && (kv_dtype != MLA_DTYPE_FP8_E4M3 || pg)) return MLA_ERR_UNSUPPORTED;
+  if (pairs && (kv_dtype == MLA_DTYPE_MXFP4 || pg)) return MLA_ERR_UNSUPPORTED;
   const int q_fmt = opts->quantize_q ? static_cast<int>(mla::kQBf16Quant) : static_cast<int>(opts->q_dtype);
   if (!mla::stage1_supported(kv_dtype, q_fmt)) return MLA_ERR_UNSUPPORTED;
   int32_t splits = opts->num_splits;
@@ -221,7 +221,9 @@ mla_status_t decode_impl(const void* q, const void* kv, const void* kv_scale, co
     if (opts->quantize_q &&
         mla::launch_q_scale(q, static_cast<int64_t>(total_q) * mla::kHeads * mla::kDqk, p.dev_flags, st) != cudaSuccess)
       return MLA_ERR_CUDA;
-    const cudaError_t le = pairs ? mla::launch_stage1_pair(q_fmt, p, st) : mla::launch_stage1(kv_dtype, q_fmt, p, st);
+    // fp8 KV pairs have their own kernel; the bf16 kernel takes p.group itself
+    const cudaError_t le = (pairs && kv_dtype == MLA_DTYPE_FP8_E4M3) ? mla::launch_stage1_pair(q_fmt, p, st)
+                                                                      : mla::launch_stage1(kv_dtype, q_fmt, p, st);
     if (le != cudaSuccess) return MLA_ERR_CUDA;
   } else if (cudaMemsetAsync(out, 0, static_cast<size_t>(total_q) * mla::kHeads * mla::kDv * 2, st) != cudaSuccess) {
     return MLA_ERR_CUDA;

@@ -1,5 +1,5 @@
 """GPU parity of the token-pair decode (opts.token_pairs: two query tokens of a
-segment share each pass over its KV rows; fp8 KV).
+segment share each pass over its KV rows; fp8 and bf16 KV).
 
 Checked against the fp64 oracle (same tolerance as the other parity tests)
 over ragged token and row counts, odd q_len (a one-token last group), empty
@@ -103,8 +103,29 @@ def test_pairs_workspace_is_reused_and_left_clean():
     check(outs[0].float().cpu().numpy(), oracle_ref(inp))
 
 
-def test_pairs_need_fp8_kv():
-    w = synth.Workload("pairsbf", 2, 2, 100, synth.BF16, synth.BF16, seed=65)
+@pytest.mark.parametrize("q_dtype", [synth.BF16, synth.FP8_E4M3])
+@pytest.mark.parametrize("num_splits", [1, 7, 40, 0])
+def test_pairs_bf16_kv_against_oracle(q_dtype, num_splits):
+    w = synth.Workload("pairsbf", len(KV), 1, 0, q_dtype, synth.BF16, seed=66)
+    inp = synth.make_inputs(w, "cuda", kv_lens=KV, q_lens=QL)
+    got = run_pairs(inp, num_splits=num_splits).float().cpu().numpy()
+    ref = oracle_ref(inp)
+    qo = inp.qo_indptr.cpu().numpy()
+    for b in np.nonzero(np.array(KV) == 0)[0]:  # empty KV: zeros
+        assert np.array_equal(got[qo[b]:qo[b + 1]], np.zeros_like(got[qo[b]:qo[b + 1]]))
+    check(got, ref)
+
+
+@pytest.mark.parametrize("q_dtype", [synth.BF16, synth.FP8_E4M3])
+def test_pairs_bf16_kv_equal_single_token_decode_with_one_partition(q_dtype):
+    w = synth.Workload("pairsbf1", len(KV), 1, 0, q_dtype, synth.BF16, seed=67)
+    inp = synth.make_inputs(w, "cuda", kv_lens=KV, q_lens=QL)
+    got = run_pairs(inp, num_splits=1)
+    assert torch.equal(got, run_decode(inp, num_splits=1))
+
+
+def test_pairs_need_fp8_or_bf16_kv():
+    w = synth.Workload("pairsmx", 2, 2, 100, synth.BF16, synth.MXFP4, seed=65)
     inp = synth.make_inputs(w, "cuda")
     out = torch.empty((inp.total_q, 16, 512), dtype=torch.bfloat16, device="cuda")
     ws = m.alloc_pairs_workspace(inp.batch, inp.total_q, inp.total_kv, inp.kv_dtype, num_splits=4)
