@@ -528,8 +528,10 @@ def finish(args, line, rank, world, w, m, synth, torch, inp):
             table[qq] = {"cold": time_workload(m, synth, torch, "a8w8_bs64_kv1024", 30, 5, True, quantize_q=True),
                          "warm": time_workload(m, synth, torch, "a8w8_bs64_kv1024", 30, 5, False, quantize_q=True)}
             # two query tokens per segment (multi-token decode), with and without token pairs
-            for qd, qn in ((synth.BF16, "bf16q"), (synth.FP8_E4M3, "fp8q")):
-                wq = synth.Workload(f"fp8kv_bs128_q2_kv8192_{qn}", 128, 2, 8192, qd, synth.FP8_E4M3)
+            for kd, kn, bs, qd, qn in ((synth.FP8_E4M3, "fp8kv", 128, synth.BF16, "bf16q"),
+                                       (synth.FP8_E4M3, "fp8kv", 128, synth.FP8_E4M3, "fp8q"),
+                                       (synth.BF16, "bf16kv", 32, synth.BF16, "bf16q")):
+                wq = synth.Workload(f"{kn}_bs{bs}_q2_kv8192_{qn}", bs, 2, 8192, qd, kd)
                 for pairs in (False, True):
                     key = wq.name + ("+token_pairs" if pairs else "")
                     table[key] = {"cold": time_workload(m, synth, torch, None, 30, 5, True, w=wq, token_pairs=pairs),
