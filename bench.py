@@ -168,6 +168,17 @@ def workload_by_name(synth, name):
     return synth.Workload(name, int(bs[2:]), q_len, int(kvl[2:]), q_dtype, kv_dtype)
 
 
+L2_FLUSHED = "flushed before each call (256 MB written, then read back)"
+
+
+def l2_flush(buf, i):
+    """Evicts the timed call's inputs from L2: writes a 256 MB buffer (twice the L2), then reads it
+    back, so that L2 holds only clean lines of that buffer and the call is not charged for writing
+    back the flush's own dirty lines."""
+    buf.fill_(i & 0xFF)
+    buf.amax()
+
+
 def time_workload(m, synth, torch, name, steps, warmup, flush_l2: bool, quantize_q: bool = False, w=None,
                   token_pairs: bool = False):
     """Per-call device time of one workload (stage-1 and total), median over steps.
@@ -185,7 +196,7 @@ def time_workload(m, synth, torch, name, steps, warmup, flush_l2: bool, quantize
     tot, st1 = [], []
     for i in range(warmup + steps):
         if flush is not None:
-            flush.fill_(i & 0xFF)
+            l2_flush(flush, i)
         m.decode(inp.q, inp.kv, inp.kv_scale, inp.qo_indptr, inp.kv_indptr, out, inp.kv_dtype, workspace=ws,
                  q_dtype=inp.q_dtype, q_scale=inp.q_scale, events=ev, quantize_q=quantize_q, token_pairs=token_pairs)
         torch.cuda.synchronize()
@@ -198,7 +209,7 @@ def time_workload(m, synth, torch, name, steps, warmup, flush_l2: bool, quantize
     return {"us_per_call": round(us, 2), "stage1_us": round(statistics.median(st1), 2),
             "kv_gbs": round(kv_bytes(inp) / (us * 1e-6) / 1e9, 1), "kv_bytes": kv_bytes(inp),
             "num_splits": m.plan(inp.batch, inp.total_q, inp.total_kv, inp.kv_dtype),
-            "l2": "flushed (256 MB write) before each call" if flush_l2 else "back-to-back"}
+            "l2": L2_FLUSHED if flush_l2 else "back-to-back"}
 
 
 def time_paged_workload(m, synth, torch, name, page_size, steps, warmup, flush_l2: bool, in_order: bool = False):
@@ -216,7 +227,7 @@ def time_paged_workload(m, synth, torch, name, page_size, steps, warmup, flush_l
     tot = []
     for i in range(warmup + steps):
         if flush is not None:
-            flush.fill_(i & 0xFF)
+            l2_flush(flush, i)
         m.decode_paged(pin.q, pin.kv_pages, pin.kv_scale, pin.qo_indptr, pin.page_indptr, pin.page_indices,
                        pin.last_page_len, page_size, out, synth.FP8_E4M3, total_kv=pin.total_kv, workspace=ws,
                        q_dtype=pin.q_dtype, q_scale=pin.q_scale, events=ev)
@@ -229,7 +240,7 @@ def time_paged_workload(m, synth, torch, name, page_size, steps, warmup, flush_l
     kvb = pin.total_kv * synth.D_QK  # the rows read (the pool's spare pages are not)
     return {"us_per_call": round(us, 2), "kv_gbs": round(kvb / (us * 1e-6) / 1e9, 1), "kv_bytes": kvb,
             "page_size": page_size, "pages": pin.num_pages, "page_order": "pool order" if in_order else "random",
-            "l2": "flushed (256 MB write) before each call" if flush_l2 else "back-to-back"}
+            "l2": L2_FLUSHED if flush_l2 else "back-to-back"}
 
 
 def _first_rows(h, rows):

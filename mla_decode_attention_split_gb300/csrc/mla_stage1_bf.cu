@@ -42,6 +42,9 @@ constexpr int kBoxes = 9;                   // 64-dim boxes of a tile: 8 V + 1 r
 constexpr int kRopeBox = 8;
 constexpr int kBoxBytes = kTileRows * 128;  // 16 KB
 constexpr int kTileBytes = kBoxes * kBoxBytes;  // 144 KB
+// Lazy rescaling: a head's reference max moves only when a tile's max exceeds
+// it by more than this (log2 units), so bf16 weights stay below 2^8.
+constexpr float kMaxSlackBf = 8.0f;
 
 // Layout for G tokens per pass.
 template <int G>
@@ -386,10 +389,10 @@ __device__ void softmax_role(const Stage1Params& p, const CxB<G>& cx, PieceCurso
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
             const int h = 4 * q + e;
-            const float mn = fmaxf(m[g][h], t4[e]);
-            alpha[g][h] = fast_exp2(m[g][h] - mn);
-            grew_any |= mn > m[g][h];
-            m[g][h] = mn;
+            const bool up = t4[e] > m[g][h] + kMaxSlackBf;
+            alpha[g][h] = up ? fast_exp2(m[g][h] - t4[e]) : 1.0f;
+            grew_any |= up;
+            m[g][h] = up ? t4[e] : m[g][h];
           }
         }
 #pragma unroll

@@ -468,12 +468,12 @@ __device__ void softmax_role(const Stage1Params& p, const Cx& cx, PieceCursor cu
 #pragma unroll
       for (int h = 0; h < 16; ++h) {
         const float mn = fmaxf(m[h], tm[h]);
-        const float un = fmaxf(mu[h], tz[h]);
+        const bool up = tz[h] > mu[h] + kMaxSlack;  // O's reference moves lazily
         alpha[h] = fast_exp2(m[h] - mn);
-        alpha_o[h] = fast_exp2(mu[h] - un);
-        grew |= un > mu[h];
+        alpha_o[h] = up ? fast_exp2(mu[h] - tz[h]) : 1.0f;
+        grew |= up;
         m[h] = mn;
-        mu[h] = un;
+        mu[h] = up ? tz[h] : mu[h];
       }
       float pv[16];
 #pragma unroll

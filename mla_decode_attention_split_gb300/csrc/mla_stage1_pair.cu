@@ -346,18 +346,18 @@ __device__ __forceinline__ void store_o_tok(const Stage1Params& p, const Piece& 
   }
 }
 
-// Running max, weights and row sums of one token for one tile; returns
-// whether some head's max grew.
+// Reference max (lazy, see kMaxSlack), weights and row sums of one token for
+// one tile; returns whether some head's reference moved.
 __device__ __forceinline__ bool softmax_tok(const float* rm, const float (&x)[16], float (&m)[16], float (&l)[16],
                                             float (&alpha)[16], float (&pv)[16]) {
   bool grew = false;
 #pragma unroll
   for (int h = 0; h < 16; ++h) {
     const float tm = fmaxf(fmaxf(rm[h], rm[16 + h]), fmaxf(rm[32 + h], rm[48 + h]));
-    const float mn = fmaxf(m[h], tm);
-    alpha[h] = fast_exp2(m[h] - mn);
-    grew |= mn > m[h];
-    m[h] = mn;
+    const bool up = tm > m[h] + kMaxSlack;
+    alpha[h] = up ? fast_exp2(m[h] - tm) : 1.0f;
+    grew |= up;
+    m[h] = up ? tm : m[h];
   }
 #pragma unroll
   for (int h = 0; h < 16; ++h) {

@@ -644,10 +644,10 @@ __device__ void softmax_role(const Stage1Params& p, const Cx& cx, PieceCursor cu
 #pragma unroll
       for (int h = 0; h < 16; ++h) {
         const float tm = fmaxf(fmaxf(rm[h], rm[16 + h]), fmaxf(rm[32 + h], rm[48 + h]));
-        const float mn = fmaxf(m[h], tm);
-        alpha[h] = fast_exp2(m[h] - mn);
-        grew |= mn > m[h];
-        m[h] = mn;
+        const bool up = tm > m[h] + kMaxSlack;
+        alpha[h] = up ? fast_exp2(m[h] - tm) : 1.0f;
+        grew |= up;
+        m[h] = up ? tm : m[h];
       }
       const bool rescale = grew && r0 > 0;
       float pv[16];

@@ -31,7 +31,14 @@ constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kTmemS = 0;                // 2 buffers x 32 columns
 constexpr uint32_t kTmemO = 64;               // 2 buffers x (4 blocks x 32 columns)
 constexpr float kLoScale = 16.0f;
-constexpr float kPScale = 256.0f;
+// Lazy rescaling (the e4m3-P kernels): a head's reference max m moves only
+// when a tile's max exceeds it by more than kMaxSlack (log2 units). Until then
+// the weights exp2(x - m) may reach 2^kMaxSlack, so they are scaled by
+// kPScale, with kPScale * 2^kMaxSlack (362) below e4m3's largest value (448).
+// O, l and the LSE share the reference, so the softmax is the same; O in
+// tensor memory is rescaled only when the reference moves.
+constexpr float kMaxSlack = 3.5f;
+constexpr float kPScale = 32.0f;
 constexpr float kLog2e = 1.4426950408889634f;
 
 // Shared-memory context of one CTA; LL is the kernel's layout (offsets and
