@@ -114,17 +114,25 @@ typedef struct {
                              (else MLA_ERR_UNSUPPORTED); adds one small launch
                              (the amax). The scale is kept in the workspace
                              header.                                            */
-  int32_t token_pairs;    /* nonzero: the query tokens of each segment are taken
-                             in pairs (the last one alone if q_len is odd) that
-                             share one pass over the segment's KV rows, for
-                             multi-token decode (q_len > 1). fp8 or bf16 KV
-                             (mxfp4: MLA_ERR_UNSUPPORTED), not with a page
-                             table. The
+  int32_t token_group;    /* query tokens of a segment that share one pass over
+                             its KV rows (multi-token decode, q_len > 1; the
+                             grouping of kernelbot-amd-mixed-mla-586148
+                             `_flash_splitk`, whose Q block spans the q_len x
+                             16 rows of a segment): 0 or 1 = one token per
+                             pass; 2 = pairs (fp8 or bf16 KV; mxfp4:
+                             MLA_ERR_UNSUPPORTED); 4 = groups of four (fp8 KV
+                             with fp8 q or quantize_q; otherwise
+                             MLA_ERR_UNSUPPORTED). The last group of a segment
+                             holds the remaining tokens. Other values:
+                             MLA_ERR_INVALID_ARG. Not with a page table. The
                              workspace must be sized by
-                             mla_decode_pairs_workspace_size(). Each token's
-                             arithmetic is unchanged: with num_splits = 1 the
-                             output equals that of the call without pairs bit
-                             for bit.                                           */
+                             mla_decode_group_workspace_size(). With pairs each
+                             token's arithmetic is unchanged (with
+                             num_splits = 1 the output equals that of the call
+                             without grouping bit for bit); groups of four add
+                             a weight's e4m3 remainder into the same
+                             accumulator as its leading part (same tolerance,
+                             different rounding).                            */
 } mla_decode_opts;
 
 /* Split planner (the pages choose the split count from batch size and KV
@@ -177,10 +185,17 @@ mla_status_t mla_decode(const void* q, const void* kv, const void* kv_scale,
                         const int32_t* qo_indptr, const int32_t* kv_indptr, void* out,
                         mla_dtype_t kv_dtype, const mla_decode_opts* opts, void* stream);
 
-/* Bytes of device workspace for a call with opts->token_pairs set: as
- * mla_decode_workspace_size(), with 2 * num_splits + total_q partial slots
- * (a piece of a token pair writes two partials). Host only. Errors as
- * mla_decode_workspace_size().                                               */
+/* Bytes of device workspace for a call with opts->token_group = G > 1: as
+ * mla_decode_workspace_size(), with G * num_splits + total_q partial slots
+ * (a piece of a group writes one partial per token). token_group 0 or 1 gives
+ * the size of mla_decode_workspace_size(). Host only. Errors as
+ * mla_decode_workspace_size(); MLA_ERR_INVALID_ARG for a token_group other
+ * than 0, 1, 2 or 4.                                                         */
+mla_status_t mla_decode_group_workspace_size(int32_t batch, int32_t total_q, int32_t total_kv,
+                                             mla_dtype_t kv_dtype, int32_t num_splits, int32_t token_group,
+                                             size_t* bytes);
+
+/* mla_decode_group_workspace_size() with token_group = 2.                    */
 mla_status_t mla_decode_pairs_workspace_size(int32_t batch, int32_t total_q, int32_t total_kv,
                                              mla_dtype_t kv_dtype, int32_t num_splits, size_t* bytes);
 

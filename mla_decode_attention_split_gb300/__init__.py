@@ -26,6 +26,7 @@ DEVFLAG_TIMEOUT, DEVFLAG_BAD_INDPTR = 0x1, 0x2
 EXPORTED = ("mla_plan", "mla_decode_workspace_size", "mla_decode", "mla_decode_from_host", "mla_dequant_rows",
             "mla_get_device_error", "mla_reset_device_error", "mla_event_elapsed_ms", "mla_decode_static_workspace",
             "mla_decode_paged_workspace_size", "mla_decode_paged", "mla_decode_pairs_workspace_size",
+            "mla_decode_group_workspace_size",
             "mla_validate_inputs", "mla_static_workspace_device_error", "mla_status_string")
 DEVFLAG_BAD_PAGE = 0x4
 MLA_ERR_TOO_LARGE = 7
@@ -43,7 +44,7 @@ class DecodeOpts(ctypes.Structure):
                 ("sm_scale", ctypes.c_float), ("q_dtype", ctypes.c_int), ("q_scale", ctypes.c_void_p),
                 ("num_splits", ctypes.c_int32), ("workspace", ctypes.c_void_p), ("workspace_bytes", ctypes.c_size_t),
                 ("profile_events", ctypes.c_void_p * 3), ("quantize_q", ctypes.c_int32),
-                ("token_pairs", ctypes.c_int32)]
+                ("token_group", ctypes.c_int32)]
 
 
 class DeviceBuffers(ctypes.Structure):
@@ -87,6 +88,8 @@ def lib():
             L.mla_decode_static_workspace.argtypes = [P, P, P, P, P, P, st, ctypes.POINTER(DecodeOpts), P]
             L.mla_decode_paged_workspace_size.argtypes = [i32, i32, i32, st, i32, ctypes.POINTER(ctypes.c_size_t)]
             L.mla_decode_pairs_workspace_size.argtypes = [i32, i32, i32, st, i32, ctypes.POINTER(ctypes.c_size_t)]
+            L.mla_decode_group_workspace_size.argtypes = [i32, i32, i32, st, i32, i32,
+                                                          ctypes.POINTER(ctypes.c_size_t)]
             L.mla_decode_paged.argtypes = [P, P, P, P, ctypes.POINTER(PagedKV), P, st, ctypes.POINTER(DecodeOpts), P]
             L.mla_validate_inputs.argtypes = [P, P, i32, i32, i32, st, P, P, ctypes.POINTER(ctypes.c_int64)]
             L.mla_static_workspace_device_error.argtypes = [P, ctypes.POINTER(ctypes.c_uint32)]
@@ -140,12 +143,14 @@ def alloc_workspace(batch: int, total_q: int, total_kv: int, kv_dtype: int, num_
 
 
 def make_opts(batch, total_q, total_kv, *, q_dtype=BF16, q_scale=None, sm_scale=0.0, num_splits=0,
-              workspace=None, events=None, quantize_q=False, token_pairs=False) -> DecodeOpts:
+              workspace=None, events=None, quantize_q=False, token_pairs=False, token_group=0) -> DecodeOpts:
+    """token_group: query tokens per KV pass (0/1, 2, 4); token_pairs=True is token_group=2."""
     o = DecodeOpts(batch=batch, total_q=total_q, total_kv=total_kv, sm_scale=float(sm_scale), q_dtype=q_dtype,
                    q_scale=None if q_scale is None else q_scale.data_ptr(), num_splits=num_splits,
                    workspace=None if workspace is None else workspace.data_ptr(),
                    workspace_bytes=0 if workspace is None else workspace.numel() * workspace.element_size(),
-                   quantize_q=1 if quantize_q else 0, token_pairs=1 if token_pairs else 0)
+                   quantize_q=1 if quantize_q else 0,
+                   token_group=int(token_group) if token_group else (2 if token_pairs else 0))
     if events is not None:  # three torch.cuda.Event(enable_timing=True)
         for i, ev in enumerate(events):
             if ev is not None and not ev.cuda_event:
@@ -156,15 +161,16 @@ def make_opts(batch, total_q, total_kv, *, q_dtype=BF16, q_scale=None, sm_scale=
 
 def decode(q, kv, kv_scale, qo_indptr, kv_indptr, out, kv_dtype: int, *, workspace, q_dtype: int = BF16,
            q_scale=None, sm_scale: float = 0.0, num_splits: int = 0, stream=None, events=None,
-           quantize_q: bool = False, token_pairs: bool = False) -> None:
+           quantize_q: bool = False, token_pairs: bool = False, token_group: int = 0) -> None:
     """mla_decode() on torch CUDA tensors (layouts as in mla_decode.h). Asynchronous.
     events: optional three CUDA events recorded before and after the launch (1 and 2 back to back).
     quantize_q: quantise bf16 q to e4m3 per tensor inside the call (the a8w8 mode; fp8 KV only).
-    token_pairs: a segment's query tokens share each pass over its KV rows in pairs (fp8 or bf16 KV;
-    the workspace comes from pairs_workspace_size)."""
+    token_group: a segment's query tokens share each pass over its KV rows in groups of 2 (fp8 or
+    bf16 KV) or 4 (fp8 KV, fp8 q or quantize_q); the workspace comes from group_workspace_size.
+    token_pairs=True is token_group=2."""
     opts = make_opts(qo_indptr.numel() - 1, q.shape[0], kv.shape[0], q_dtype=q_dtype, q_scale=q_scale,
                      sm_scale=sm_scale, num_splits=num_splits, workspace=workspace, events=events,
-                     quantize_q=quantize_q, token_pairs=token_pairs)
+                     quantize_q=quantize_q, token_pairs=token_pairs, token_group=token_group)
     _check(lib().mla_decode(_ptr(q), _ptr(kv), _ptr(kv_scale), _ptr(qo_indptr), _ptr(kv_indptr), _ptr(out),
                             kv_dtype, ctypes.byref(opts), _stream_handle(stream)), "mla_decode")
 
@@ -174,6 +180,22 @@ def pairs_workspace_size(batch: int, total_q: int, total_kv: int, kv_dtype: int,
     _check(lib().mla_decode_pairs_workspace_size(batch, total_q, total_kv, kv_dtype, num_splits, ctypes.byref(out)),
            "mla_decode_pairs_workspace_size")
     return out.value
+
+
+def group_workspace_size(batch: int, total_q: int, total_kv: int, kv_dtype: int, token_group: int,
+                         num_splits: int = 0) -> int:
+    out = ctypes.c_size_t(0)
+    _check(lib().mla_decode_group_workspace_size(batch, total_q, total_kv, kv_dtype, num_splits, token_group,
+                                                 ctypes.byref(out)), "mla_decode_group_workspace_size")
+    return out.value
+
+
+def alloc_group_workspace(batch: int, total_q: int, total_kv: int, kv_dtype: int, token_group: int,
+                          num_splits: int = 0, device="cuda"):
+    """A zeroed device workspace for decode(..., token_group=token_group)."""
+    import torch
+    n = group_workspace_size(batch, total_q, total_kv, kv_dtype, token_group, num_splits)
+    return torch.zeros(n, dtype=torch.uint8, device=device)
 
 
 def alloc_pairs_workspace(batch: int, total_q: int, total_kv: int, kv_dtype: int, num_splits: int = 0,

@@ -161,15 +161,18 @@ mla_status_t decode_impl(const void* q, const void* kv, const void* kv_scale, co
   if (kv_dtype == MLA_DTYPE_MXFP4 && !aligned16(kv_scale)) return MLA_ERR_INVALID_ARG;
   if (opts->q_dtype == MLA_DTYPE_FP8_E4M3 && !opts->q_scale) return MLA_ERR_INVALID_ARG;
   if (opts->quantize_q && opts->q_dtype != MLA_DTYPE_BF16) return MLA_ERR_UNSUPPORTED;
-  const bool pairs = opts->token_pairs != 0;
-  if (pairs && (kv_dtype == MLA_DTYPE_MXFP4 || pg)) return MLA_ERR_UNSUPPORTED;
+  // query tokens per KV pass: 1, 2 (fp8 or bf16 KV) or 4 (fp8 KV with fp8 q)
+  const int32_t G = opts->token_group <= 1 ? 1 : opts->token_group;
+  if (opts->token_group < 0 || (G != 1 && G != 2 && G != 4)) return MLA_ERR_INVALID_ARG;
+  if (G > 1 && (kv_dtype == MLA_DTYPE_MXFP4 || pg)) return MLA_ERR_UNSUPPORTED;
   const int q_fmt = opts->quantize_q ? static_cast<int>(mla::kQBf16Quant) : static_cast<int>(opts->q_dtype);
+  if (G == 4 && (kv_dtype != MLA_DTYPE_FP8_E4M3 || q_fmt == mla::kQBf16)) return MLA_ERR_UNSUPPORTED;
   if (!mla::stage1_supported(kv_dtype, q_fmt)) return MLA_ERR_UNSUPPORTED;
   int32_t splits = opts->num_splits;
   if (splits < 0 || splits > kMaxSplits) return MLA_ERR_INVALID_ARG;
   if (splits == 0) splits = plan_splits(total_q, batch, total_kv, sm_count_of_current_device());
-  // pairs: G = 2 tokens per group, so 2 num_splits + total_q partial slots
-  const size_t base = mla::workspace_bytes_for(pairs ? 2 * static_cast<int64_t>(splits) : splits, total_q);
+  // G tokens per group: G num_splits + total_q partial slots
+  const size_t base = mla::workspace_bytes_for(G * static_cast<int64_t>(splits), total_q);
   const size_t need = base + (pg ? mla::paged_extra_bytes(batch) : 0);
   if (!opts->workspace || opts->workspace_bytes < need ||
       (reinterpret_cast<uintptr_t>(opts->workspace) & 255u) != 0)
@@ -189,7 +192,7 @@ mla_status_t decode_impl(const void* q, const void* kv, const void* kv_scale, co
   p.page_indices = pg ? pg->page_indices : nullptr;
   p.page_size = pg ? pg->page_size : 0;
   p.wait_late = (!pg && opts->quantize_q) ? 1 : 0;
-  p.group = pairs ? 2 : 1;
+  p.group = G;
   p.page_shift = -1;
   for (int32_t sh = 0; sh < 31 && pg; ++sh)
     if ((int32_t{1} << sh) == pg->page_size) p.page_shift = sh;
@@ -202,7 +205,7 @@ mla_status_t decode_impl(const void* q, const void* kv, const void* kv_scale, co
   p.out = out;
   uint8_t* ws = static_cast<uint8_t*>(opts->workspace);
   p.dev_flags = reinterpret_cast<uint32_t*>(ws);
-  const int64_t slots = (pairs ? 2 * static_cast<int64_t>(splits) : splits) + total_q;
+  const int64_t slots = G * static_cast<int64_t>(splits) + total_q;
   p.tok_cnt = reinterpret_cast<uint32_t*>(ws + mla::kHeaderBytes);
   p.part_o = reinterpret_cast<float*>(ws + mla::kHeaderBytes + mla::counter_bytes(total_q));
   p.part_lse = p.part_o + slots * mla::kHeads * mla::kDv;
@@ -221,9 +224,11 @@ mla_status_t decode_impl(const void* q, const void* kv, const void* kv_scale, co
     if (opts->quantize_q &&
         mla::launch_q_scale(q, static_cast<int64_t>(total_q) * mla::kHeads * mla::kDqk, p.dev_flags, st) != cudaSuccess)
       return MLA_ERR_CUDA;
-    // fp8 KV pairs have their own kernel; the bf16 kernel takes p.group itself
-    const cudaError_t le = (pairs && kv_dtype == MLA_DTYPE_FP8_E4M3) ? mla::launch_stage1_pair(q_fmt, p, st)
-                                                                      : mla::launch_stage1(kv_dtype, q_fmt, p, st);
+    // fp8 KV groups have their own kernels; the bf16 kernel takes p.group itself
+    const bool fp8 = kv_dtype == MLA_DTYPE_FP8_E4M3;
+    const cudaError_t le = (G == 4)           ? mla::launch_stage1_quad(q_fmt, p, st)
+                           : (G == 2 && fp8) ? mla::launch_stage1_pair(q_fmt, p, st)
+                                             : mla::launch_stage1(kv_dtype, q_fmt, p, st);
     if (le != cudaSuccess) return MLA_ERR_CUDA;
   } else if (cudaMemsetAsync(out, 0, static_cast<size_t>(total_q) * mla::kHeads * mla::kDv * 2, st) != cudaSuccess) {
     return MLA_ERR_CUDA;
@@ -243,16 +248,23 @@ mla_status_t mla_decode(const void* q, const void* kv, const void* kv_scale, con
   return decode_impl(q, kv, kv_scale, qo_indptr, kv_indptr, out, kv_dtype, opts, nullptr, stream);
 }
 
-mla_status_t mla_decode_pairs_workspace_size(int32_t batch, int32_t total_q, int32_t total_kv, mla_dtype_t kv_dtype,
-                                             int32_t num_splits, size_t* bytes) {
-  if (!bytes || batch < 0 || total_q < 0 || total_kv < 0 || num_splits < 0 || num_splits > kMaxSplits)
+mla_status_t mla_decode_group_workspace_size(int32_t batch, int32_t total_q, int32_t total_kv, mla_dtype_t kv_dtype,
+                                             int32_t num_splits, int32_t token_group, size_t* bytes) {
+  if (!bytes || batch < 0 || total_q < 0 || total_kv < 0 || num_splits < 0 || num_splits > kMaxSplits ||
+      token_group < 0 || (token_group > 2 && token_group != 4))
     return MLA_ERR_INVALID_ARG;
   if (num_splits == 0) {
     const mla_status_t st = mla_plan(batch, total_q, total_kv, kv_dtype, 0, &num_splits);
     if (st != MLA_OK) return st;
   }
-  *bytes = mla::workspace_bytes_for(2 * static_cast<int64_t>(num_splits), total_q);
+  const int64_t g = token_group > 1 ? token_group : 1;
+  *bytes = mla::workspace_bytes_for(g * num_splits, total_q);
   return MLA_OK;
+}
+
+mla_status_t mla_decode_pairs_workspace_size(int32_t batch, int32_t total_q, int32_t total_kv, mla_dtype_t kv_dtype,
+                                             int32_t num_splits, size_t* bytes) {
+  return mla_decode_group_workspace_size(batch, total_q, total_kv, kv_dtype, num_splits, 2, bytes);
 }
 
 mla_status_t mla_decode_paged_workspace_size(int32_t batch, int32_t total_q, int32_t total_kv, mla_dtype_t kv_dtype,
@@ -439,9 +451,10 @@ extern "C" mla_status_t mla_decode_static_workspace(const void* q, const void* k
     if (cudaGetSymbolAddress(&ptr, g_static_workspace) != cudaSuccess || !ptr) return MLA_ERR_CUDA;
     g_static_ws_ptr[dev] = ptr;
   }
+  if (opts->token_group < 0 || (opts->token_group > 2 && opts->token_group != 4)) return MLA_ERR_INVALID_ARG;
   mla_decode_opts o = *opts;
   if (o.num_splits == 0) o.num_splits = plan_splits(o.total_q, o.batch, o.total_kv, sm_count_of_current_device());
-  const int64_t slot_splits = o.token_pairs ? 2 * static_cast<int64_t>(o.num_splits) : o.num_splits;
+  const int64_t slot_splits = (o.token_group > 1 ? o.token_group : 1) * static_cast<int64_t>(o.num_splits);
   if (mla::workspace_bytes_for(slot_splits, o.total_q) > MLA_STATIC_WORKSPACE_BYTES) return MLA_ERR_TOO_LARGE;
   // the error flags and the token counters are the scratch that must start at zero
   if (cudaMemsetAsync(g_static_ws_ptr[dev], 0, mla::kHeaderBytes + mla::counter_bytes(o.total_q),

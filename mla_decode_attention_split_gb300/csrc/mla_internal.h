@@ -46,7 +46,7 @@ struct Stage1Params {
   int32_t page_shift;  // log2(page_size) when it is a power of two, else -1
   int32_t num_pages;
   int32_t paged;
-  int32_t group;      // query tokens per group sharing a pass over the KV rows (1 or 2)
+  int32_t group;      // query tokens per group sharing a pass over the KV rows (1, 2 or 4)
   int32_t wait_late;  // the kernel just before is this call's q amax: wait for it only before reading the scale
 };
 
@@ -70,6 +70,9 @@ bool stage1_supported(int kv_fmt, int q_fmt);
 // amax of bf16 q over n elements -> header word kHdrQScale = max(amax, 1e-12) / 448 (mla_qquant.cu)
 // fp8 KV, query tokens of a segment in pairs sharing each KV tile (p.group = 2; mla_stage1_pair.cu)
 cudaError_t launch_stage1_pair(int q_fmt, const Stage1Params& p, cudaStream_t stream);
+// fp8 KV and fp8 q, query tokens of a segment in groups of four sharing each KV tile (p.group = 4;
+// mla_stage1_quad.cu)
+cudaError_t launch_stage1_quad(int q_fmt, const Stage1Params& p, cudaStream_t stream);
 cudaError_t launch_q_scale(const void* q, int64_t n, uint32_t* header, cudaStream_t stream);
 // paged KV: logical row offsets [batch+1] from the page table (mla_paged.cu)
 cudaError_t launch_paged_prepare(const int32_t* page_indptr, const int32_t* last_page_len, int32_t batch,

@@ -62,8 +62,8 @@ struct LB {
   static constexpr int kOffRedMax = kOffP + 2 * kPBytes;           // [2 buffers][G tokens][4 warps][16] f32
   static constexpr int kOffRedL = kOffRedMax + 2 * G * 4 * 16 * 4; // [G][4][16] f32
   static constexpr int kOffAmax = kOffRedL + G * 4 * 16 * 4;       // [4] u32 (unused by bf16 q)
-  static constexpr int kOffMList = kOffAmax + 16;                  // MergeList (64 B)
-  static constexpr int kOffScan = kOffMList + 64;                  // 16 x i64
+  static constexpr int kOffMList = kOffAmax + 16;                  // MergeList (128 B)
+  static constexpr int kOffScan = kOffMList + 128;                  // 16 x i64
   static constexpr int kOffBars = kOffScan + 16 * 8;
   enum {
     kKvFull = 0, kKvEmpty = 9, kSFull = 18, kSEmpty = 20, kPFull = 22, kPvDone = 24, kQFull = 26, kQEmpty = 27,

@@ -97,8 +97,8 @@ struct L {
   static constexpr int kOffRedMu = kOffRedMax + 2 * 4 * 16 * 4;          // [2][4][16] f32
   static constexpr int kOffRedL = kOffRedMu + 2 * 4 * 16 * 4;            // [4][16] f32
   static constexpr int kOffAmax = kOffRedL + 4 * 16 * 4;                 // [4] u32
-  static constexpr int kOffMList = kOffAmax + 16;                        // MergeList (64 B)
-  static constexpr int kOffScan = kOffMList + 64;                        // 24 x i64
+  static constexpr int kOffMList = kOffAmax + 16;                        // MergeList (128 B)
+  static constexpr int kOffScan = kOffMList + 128;                        // 24 x i64
   static constexpr int kOffMeta = kOffScan + 24 * 8;                     // [4] u32: tile i in slot i % 4
   static constexpr int kOffBars = kOffMeta + 16;
   // kKvFull and the row exponents have four slots (tile i in slot i % 4): the

@@ -58,8 +58,8 @@ struct LT {
   static constexpr int kOffRedMax = kOffP + kPBytes2;                // [2 buffers][2 tokens][4 warps][16] f32
   static constexpr int kOffRedL = kOffRedMax + 2 * 2 * 4 * 16 * 4;   // [2 tokens][4][16] f32
   static constexpr int kOffAmax = kOffRedL + 2 * 4 * 16 * 4;         // [2 tokens][4 warps] u32
-  static constexpr int kOffMList = kOffAmax + 32;                    // MergeList (64 B)
-  static constexpr int kOffScan = kOffMList + 64;                    // 16 x i64
+  static constexpr int kOffMList = kOffAmax + 32;                    // MergeList (128 B)
+  static constexpr int kOffScan = kOffMList + 128;                    // 16 x i64
   static constexpr int kOffBars = kOffScan + 16 * 8;
   enum {
     kKvFull = 0, kKvEmpty = 3, kSFull = 6, kSEmpty = 8, kRopeFull = 10, kPFull = 11, kPEmpty = 12, kQFull = 13,

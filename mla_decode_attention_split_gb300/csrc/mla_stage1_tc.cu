@@ -58,8 +58,8 @@ struct L {
   static constexpr int kOffRedMax = kOffP + kPBytes;              // [2][4][16] f32
   static constexpr int kOffRedL = kOffRedMax + 2 * 4 * 16 * 4;    // [4][16] f32
   static constexpr int kOffAmax = kOffRedL + 4 * 16 * 4;          // [4] u32
-  static constexpr int kOffMList = kOffAmax + 16;                 // MergeList (64 B)
-  static constexpr int kOffScan = kOffMList + 64;                 // 16 x i64
+  static constexpr int kOffMList = kOffAmax + 16;                 // MergeList (128 B)
+  static constexpr int kOffScan = kOffMList + 128;                 // 16 x i64
   static constexpr int kOffCRing = kOffScan + 16 * 8;             // score scale of piece k: f32 [4] + tag u32 [4]
   static constexpr int kOffQpAmax = kOffCRing + 32;               // [2] u32: the q-prep warps' maxima
   static constexpr int kOffBars = kOffQpAmax + 16;

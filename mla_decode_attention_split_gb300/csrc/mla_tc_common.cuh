@@ -478,14 +478,15 @@ __device__ __forceinline__ void store_o(const Stage1Params& p, const Piece& pc, 
 // are free: with L = max_s lse_s, out = sum_s 2^(lse_s - L) O_s /
 // sum_s 2^(lse_s - L) over the partial slots G c + token of the CTAs c0..c1 that
 // hold pieces of the token. A CTA holds at most two split pieces (the first
-// and the last of its range) of at most two tokens each, so it merges at most
-// four tokens.
+// and the last of its range) of at most four tokens each, so it merges at most
+// eight tokens.
+constexpr uint32_t kMergeMax = 8;
 struct MergeList {
-  uint32_t n;                      // tokens this CTA merges (at most 4)
-  int32_t token[4], c0[4], c1[4];  // token and the CTAs that hold its pieces
-  uint32_t pad[3];
+  uint32_t n;                                           // tokens this CTA merges
+  int32_t token[kMergeMax], c0[kMergeMax], c1[kMergeMax];  // token and the CTAs that hold its pieces
+  uint32_t pad[7];
 };
-static_assert(sizeof(MergeList) == 64, "merge list slot");
+static_assert(sizeof(MergeList) == 128, "merge list slot");
 
 // After the 128 softmax threads wrote this CTA's partial of a split token:
 // publish it and count it on the token's counter; if it completes the count,
@@ -503,7 +504,7 @@ __device__ __forceinline__ bool finish_partial(const Stage1Params& p, const Ctx<
     MergeList* ml = reinterpret_cast<MergeList*>(cx.g + LL::kOffMList);
     for (int i = 0; i < pc.ntok; ++i) {  // every token of the group
       const uint32_t arrived = atomicAdd(p.tok_cnt + pc.token + i, 1u) + 1u;
-      if (arrived == static_cast<uint32_t>(c1 - c0 + 1) && ml->n < 4) {
+      if (arrived == static_cast<uint32_t>(c1 - c0 + 1) && ml->n < kMergeMax) {
         ml->token[ml->n] = pc.token + i;
         ml->c0[ml->n] = static_cast<int32_t>(c0);
         ml->c1[ml->n] = static_cast<int32_t>(c1);
@@ -528,7 +529,7 @@ __device__ void merge_listed(const Stage1Params& p, const Ctx<LL>& cx) {
   constexpr int kF = (kHeads * kDv / 4 + kThr - 1) / kThr;  // float4 elements per thread
   static_assert(kSlots >= 1, "merge buffers");
   const MergeList* ml = reinterpret_cast<const MergeList*>(cx.g + LL::kOffMList);
-  const uint32_t nm = ml->n;
+  const uint32_t nm = ml->n < kMergeMax ? ml->n : kMergeMax;
   // scratch in the (free) Q buffer: the batch's LSEs [kSlots][16], weights
   // [kSlots][16], and per head the rescale factor, running max and sum
   float* lsebuf = reinterpret_cast<float*>(cx.g + LL::kOffQ);

@@ -165,10 +165,11 @@ def test_paged_workspace_size_and_argument_checks(lib):
     pg.num_pages = 3
     for dt in (m.BF16, m.MXFP4):  # the paged path is the fp8 tensor-core kernel
         assert L.mla_decode_paged(*args(dt)) == m.MLA_ERR_UNSUPPORTED
-    # token pairs are not combined with a page table
-    opts.token_pairs = 1
-    assert L.mla_decode_paged(*args(m.FP8_E4M3)) == m.MLA_ERR_UNSUPPORTED
-    opts.token_pairs = 0
+    # token groups are not combined with a page table
+    for g in (2, 4):
+        opts.token_group = g
+        assert L.mla_decode_paged(*args(m.FP8_E4M3)) == m.MLA_ERR_UNSUPPORTED
+    opts.token_group = 0
     # a workspace sized for the contiguous call is too small for the paged one
     n = m.workspace_size(1, 1, 10, m.FP8_E4M3, num_splits=1)
     opts.workspace, opts.workspace_bytes = 256, n
@@ -183,6 +184,47 @@ def test_pairs_workspace_size(lib):
     assert n == m.workspace_size(4, 8, 4096, m.FP8_E4M3, num_splits=64)
     with pytest.raises(m.MlaError):
         m.pairs_workspace_size(4, 8, 4096, m.FP8_E4M3, num_splits=-1)
+
+
+def test_group_workspace_size(lib):
+    # groups of G tokens: G num_splits + total_q partial slots
+    for g in (0, 1, 2, 4):
+        n = m.group_workspace_size(4, 8, 4096, m.FP8_E4M3, g, num_splits=32)
+        assert n == m.workspace_size(4, 8, 4096, m.FP8_E4M3, num_splits=32 * max(g, 1))
+    assert m.group_workspace_size(4, 8, 4096, m.FP8_E4M3, 2, num_splits=32) == \
+        m.pairs_workspace_size(4, 8, 4096, m.FP8_E4M3, num_splits=32)
+    for g in (-1, 3, 5, 8):
+        with pytest.raises(m.MlaError):
+            m.group_workspace_size(4, 8, 4096, m.FP8_E4M3, g, num_splits=32)
+
+
+def test_token_group_argument_checks(lib):
+    """token_group: 0/1/2/4 only; 4 needs an fp8 cache and fp8 q (given or quantised in the call);
+    no grouping with an mxfp4 cache. All of it is checked before any device work."""
+    L = lib
+    buf = (ctypes.c_uint8 * 64)()
+    a = ctypes.c_void_p((ctypes.addressof(buf) + 15) & ~15)
+    opts = m.DecodeOpts(batch=1, total_q=4, total_kv=8, sm_scale=0.0, q_dtype=m.FP8_E4M3, q_scale=a.value,
+                        num_splits=1, workspace=None, workspace_bytes=0)
+
+    def call(kv_dtype, group, q_dtype=m.FP8_E4M3, quantize=0):
+        opts.token_group, opts.q_dtype, opts.quantize_q = group, q_dtype, quantize
+        return L.mla_decode(a, a, a, a, a, a, kv_dtype, ctypes.byref(opts), None)
+
+    for g in (-1, 3, 5, 8):
+        assert call(m.FP8_E4M3, g) == m.MLA_ERR_INVALID_ARG
+    for g in (0, 1, 2, 4):  # accepted: the call gets as far as the (missing) workspace
+        assert call(m.FP8_E4M3, g) == m.MLA_ERR_WORKSPACE
+    assert call(m.FP8_E4M3, 4, q_dtype=m.BF16, quantize=1) == m.MLA_ERR_WORKSPACE
+    assert call(m.FP8_E4M3, 4, q_dtype=m.BF16) == m.MLA_ERR_UNSUPPORTED  # bf16 q needs hi + lo rows
+    assert call(m.BF16, 4, q_dtype=m.BF16) == m.MLA_ERR_UNSUPPORTED
+    assert call(m.BF16, 2, q_dtype=m.BF16) == m.MLA_ERR_WORKSPACE
+    for g in (2, 4):
+        assert call(m.MXFP4, g, q_dtype=m.BF16) == m.MLA_ERR_UNSUPPORTED
+    # the allocation-free entry checks the group before sizing its scratch
+    opts.token_group = 3
+    assert L.mla_decode_static_workspace(a, a, a, a, a, a, m.FP8_E4M3, ctypes.byref(opts), None) in (
+        m.MLA_ERR_INVALID_ARG, m.MLA_ERR_CUDA)
 
 
 def test_validate_inputs_argument_errors(lib):
