@@ -168,29 +168,25 @@ def workload_by_name(synth, name):
     return synth.Workload(name, int(bs[2:]), q_len, int(kvl[2:]), q_dtype, kv_dtype)
 
 
-L2_FLUSHED = "flushed before each call (256 MB written, then read back)"
+L2_FLUSHED = "flushed (256 MB write) before each call"
 
 
 def l2_flush(buf, i):
-    """Evicts the timed call's inputs from L2: writes a 256 MB buffer (twice the L2), then reads it
-    back, so that L2 holds only clean lines of that buffer and the call is not charged for writing
-    back the flush's own dirty lines."""
+    """Evicts the timed call's inputs from L2: writes a 256 MB buffer (twice the L2)."""
     buf.fill_(i & 0xFF)
-    buf.amax()
 
 
 def time_workload(m, synth, torch, name, steps, warmup, flush_l2: bool, quantize_q: bool = False, w=None,
-                  token_pairs: bool = False):
+                  token_group: int = 0):
     """Per-call device time of one workload (stage-1 and total), median over steps.
     quantize_q: pass bf16 q and let the call quantise it (the pages' a8w8 flow).
-    w: a Workload instead of a named one; token_pairs: a segment's tokens share KV tiles in pairs."""
+    w: a Workload instead of a named one; token_group: a segment's tokens share KV tiles in groups of 2 or 4."""
     w = synth.WORKLOADS[name] if w is None else w
     if quantize_q:
         w = synth.Workload(w.name, w.batch, w.q_len, w.kv_len, synth.BF16, w.kv_dtype, w.ragged_max, w.seed)
     inp = synth.make_inputs(w, "cuda")
     out = torch.empty((inp.total_q, 16, 512), dtype=torch.bfloat16, device="cuda")
-    ws = (m.alloc_pairs_workspace if token_pairs else m.alloc_workspace)(inp.batch, inp.total_q, inp.total_kv,
-                                                                         inp.kv_dtype)
+    ws = m.alloc_group_workspace(inp.batch, inp.total_q, inp.total_kv, inp.kv_dtype, token_group)
     flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device="cuda") if flush_l2 else None
     ev = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
     tot, st1 = [], []
@@ -198,7 +194,7 @@ def time_workload(m, synth, torch, name, steps, warmup, flush_l2: bool, quantize
         if flush is not None:
             l2_flush(flush, i)
         m.decode(inp.q, inp.kv, inp.kv_scale, inp.qo_indptr, inp.kv_indptr, out, inp.kv_dtype, workspace=ws,
-                 q_dtype=inp.q_dtype, q_scale=inp.q_scale, events=ev, quantize_q=quantize_q, token_pairs=token_pairs)
+                 q_dtype=inp.q_dtype, q_scale=inp.q_scale, events=ev, quantize_q=quantize_q, token_group=token_group)
         torch.cuda.synchronize()
         if i >= warmup:
             tot.append(m.elapsed_ms(ev[0], ev[2]) * 1e3)
@@ -364,9 +360,13 @@ def main():
     ap.add_argument("--workload", default=HEADLINE,
                     help="workload name (the five benchmark workloads, or kv{fp8,fp8a8,bf16,mx}_bs<B>[_q<N>]_kv<L> "
                          "for profiling)")
-    ap.add_argument("--token-pairs", action="store_true",
-                    help="the tokens of a segment share each KV tile in pairs (fp8 KV, q_len > 1)")
+    ap.add_argument("--token-pairs", action="store_true", help="same as --token-group 2")
+    ap.add_argument("--token-group", type=int, default=0,
+                    help="the tokens of a segment share each KV tile in groups of 2 (fp8 or bf16 KV) or 4 (fp8 KV "
+                         "and fp8 q); for q_len > 1")
     args = ap.parse_args()
+    if args.token_pairs and not args.token_group:
+        args.token_group = 2
     if args.impl == "reference":
         return run_reference(args)
 
@@ -388,8 +388,8 @@ def main():
     kvb = kv_bytes(inp)
     out = torch.empty((inp.total_q, 16, 512), dtype=torch.bfloat16, device=device)
     splits = m.plan(inp.batch, inp.total_q, inp.total_kv, inp.kv_dtype)
-    alloc = m.alloc_pairs_workspace if args.token_pairs else m.alloc_workspace
-    ws = alloc(inp.batch, inp.total_q, inp.total_kv, inp.kv_dtype, num_splits=splits)
+    ws = m.alloc_group_workspace(inp.batch, inp.total_q, inp.total_kv, inp.kv_dtype, args.token_group,
+                                 num_splits=splits)
     stream = torch.cuda.current_stream()
     K, W = args.steps, args.warmup
     # the per-launch profile events run in a second, shorter pass: an event
@@ -402,7 +402,7 @@ def main():
     def step(events=None):
         m.decode(inp.q, inp.kv, inp.kv_scale, inp.qo_indptr, inp.kv_indptr, out, inp.kv_dtype, workspace=ws,
                  q_dtype=inp.q_dtype, q_scale=inp.q_scale, num_splits=splits, events=events, stream=stream,
-                 token_pairs=args.token_pairs)
+                 token_group=args.token_group)
 
     for _ in range(W):
         step()
@@ -441,7 +441,7 @@ def main():
 
     # end to end through the host-buffer entry point: every input H2D from
     # pinned memory and the output D2H inside the timed region, every step
-    e2e = None if (args.no_e2e or args.token_pairs) else measure_e2e(m, torch, inp, out, ws, splits, stream, K,
+    e2e = None if (args.no_e2e or args.token_group > 1) else measure_e2e(m, torch, inp, out, ws, splits, stream, K,
                                                                        world, device, kvb)
     line = build_line(args, w, inp, kvb, splits, world, K, W, value, ms_step, achieved, peak, peak_kind, s1_avg_s,
                       stage2_ms, clocks, e2e)
@@ -477,7 +477,7 @@ def measure_e2e(m, torch, inp, out, ws, splits, stream, K, world, device, kvb):
 
 def _kernel_name(synth, w) -> str:
     k = {synth.FP8_E4M3: "stage1_tc_kernel (tcgen05, e4m3 codes)", synth.MXFP4: "stage1_mx_kernel (tcgen05, e5m2 rebase)",
-         synth.BF16: "mla_stage1_kernel (warp MMA)"}[w.kv_dtype]
+         synth.BF16: "stage1_bf_kernel (tcgen05 kind::f16)"}[w.kv_dtype]
     return k + f" <{synth.DTYPE_NAMES[w.kv_dtype]} KV, {synth.DTYPE_NAMES[w.q_dtype]} q>"
 
 
@@ -509,7 +509,8 @@ def build_line(args, w, inp, kvb, splits, world, K, W, value, ms_step, achieved,
                        "parallelism": f"{world} independent replicas (weak scaling)"},
             "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                          "frac": round(achieved / peak, 4), "traffic": _ncu_traffic(w.name),
-                         "kernel": ("stage1_pair_kernel (tcgen05, token pairs) " if args.token_pairs else "")
+                         "kernel": {2: "stage1_pair_kernel (tcgen05, token pairs) ",
+                                    4: "stage1_quad_kernel (tcgen05, groups of four tokens) "}.get(args.token_group, "")
                                    + _kernel_name(synth, w),
                          "algorithmic_bytes": f"{kvb} per launch = {kvb // inp.total_kv} B x {inp.total_kv} KV rows",
                          "peak_kind": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)",
@@ -538,16 +539,18 @@ def finish(args, line, rank, world, w, m, synth, torch, inp):
             qq = "a8w8_bs64_kv1024+in_call_q_quantisation"
             table[qq] = {"cold": time_workload(m, synth, torch, "a8w8_bs64_kv1024", 30, 5, True, quantize_q=True),
                          "warm": time_workload(m, synth, torch, "a8w8_bs64_kv1024", 30, 5, False, quantize_q=True)}
-            # two query tokens per segment (multi-token decode), with and without token pairs
-            for kd, kn, bs, qd, qn in ((synth.FP8_E4M3, "fp8kv", 128, synth.BF16, "bf16q"),
-                                       (synth.FP8_E4M3, "fp8kv", 128, synth.FP8_E4M3, "fp8q"),
-                                       (synth.BF16, "bf16kv", 32, synth.BF16, "bf16q")):
-                wq = synth.Workload(f"{kn}_bs{bs}_q2_kv8192_{qn}", bs, 2, 8192, qd, kd)
-                for pairs in (False, True):
-                    key = wq.name + ("+token_pairs" if pairs else "")
-                    table[key] = {"cold": time_workload(m, synth, torch, None, 30, 5, True, w=wq, token_pairs=pairs),
-                                  "warm": time_workload(m, synth, torch, None, 30, 5, False, w=wq,
-                                                        token_pairs=pairs)}
+            # several query tokens per segment (multi-token decode), one token per KV pass
+            # and tokens sharing each pass in pairs or groups of four
+            for kd, kn, bs, ql, qd, qn, groups in ((synth.FP8_E4M3, "fp8kv", 128, 2, synth.BF16, "bf16q", (0, 2)),
+                                                   (synth.FP8_E4M3, "fp8kv", 128, 2, synth.FP8_E4M3, "fp8q", (0, 2)),
+                                                   (synth.BF16, "bf16kv", 32, 2, synth.BF16, "bf16q", (0, 2)),
+                                                   (synth.FP8_E4M3, "fp8kv", 64, 4, synth.FP8_E4M3, "fp8q",
+                                                    (0, 2, 4))):
+                wq = synth.Workload(f"{kn}_bs{bs}_q{ql}_kv8192_{qn}", bs, ql, 8192, qd, kd)
+                for g in groups:
+                    key = wq.name + {0: "", 2: "+token_pairs", 4: "+token_group4"}[g]
+                    table[key] = {"cold": time_workload(m, synth, torch, None, 30, 5, True, w=wq, token_group=g),
+                                  "warm": time_workload(m, synth, torch, None, 30, 5, False, w=wq, token_group=g)}
             # the headline shape with the cache in pages scattered over a pool
             for ps, in_order in ((1, True), (1, False), (16, False), (64, False)):
                 key = f"fp8kv_bs256_kv8192+paged_ps{ps}_{'in_order' if in_order else 'random'}"
