@@ -42,14 +42,16 @@ constexpr int32_t kMaxSplits = 4096;
 // Segments are taken as equally long (the planner sees only the totals).
 // Constants from decode timings on the fp8 tensor-core kernel over split
 // counts: one piece costs about 4 tiles, one merged partial a quarter tile.
+// With query tokens in groups of g sharing each pass, a unit of work is a
+// group, and its merge reads g partials per split.
 constexpr double kPieceCost = 4.0, kMergeCost = 0.25;
 
-double split_cost(int64_t p, int64_t nseg, int64_t lv) {
+double split_cost(int64_t p, int64_t nseg, int64_t lv, int64_t g) {
   if (p % nseg == 0) {  // k CTAs per segment, one piece each
     const int64_t k = p / nseg;
     const int64_t rows = (lv + k - 1) / k;
     const int64_t lead = (lv % k == 0 && (lv / k) % 8 == 0) ? 0 : 7;
-    return kPieceCost + static_cast<double>((rows + lead + 127) / 128) + (k > 1 ? kMergeCost * k : 0.0);
+    return kPieceCost + static_cast<double>((rows + lead + 127) / 128) + (k > 1 ? kMergeCost * k * g : 0.0);
   }
   if (nseg % p == 0) {  // whole segments per CTA, no merges
     const int64_t j = nseg / p;
@@ -60,20 +62,21 @@ double split_cost(int64_t p, int64_t nseg, int64_t lv) {
   const double pieces = std::min(static_cast<double>(nseg), std::ceil(r / lvd) + 1.0);
   const double tiles = std::ceil(r / 128.0) + pieces;
   const double k = r < lvd ? std::ceil(lvd / r) + 1.0 : 2.0;
-  return kPieceCost * pieces + tiles + kMergeCost * k;
+  return kPieceCost * pieces + tiles + kMergeCost * k * g;
 }
 
-int32_t plan_splits(int64_t total_q, int64_t batch, int64_t total_kv, int sm_count) {
+int32_t plan_splits(int64_t total_q, int64_t batch, int64_t total_kv, int sm_count, int64_t group = 1) {
   if (sm_count <= 0) sm_count = 1;
   if (total_q <= 0 || batch <= 0 || total_kv <= 0) return 1;
-  // one unit of work per query token: its segment's rows (average length)
-  const int64_t nseg = total_q;
+  // one unit of work per group of query tokens: its segment's rows (average length)
+  const int64_t g = group > 1 ? group : 1;
+  const int64_t nseg = (total_q + g - 1) / g;
   const int64_t lv = std::max<int64_t>(1, total_kv / batch);
   const int64_t maxp = std::min<int64_t>(sm_count, nseg * lv);  // at least one row per CTA
   int64_t best = 1;
-  double best_cost = split_cost(1, nseg, lv);
+  double best_cost = split_cost(1, nseg, lv, g);
   for (int64_t p = 2; p <= maxp; ++p) {
-    const double c = split_cost(p, nseg, lv);
+    const double c = split_cost(p, nseg, lv, g);
     if (c <= best_cost + 1e-9) {  // ties go to more CTAs
       best = p;
       best_cost = std::min(best_cost, c);
@@ -170,7 +173,7 @@ mla_status_t decode_impl(const void* q, const void* kv, const void* kv_scale, co
   if (!mla::stage1_supported(kv_dtype, q_fmt)) return MLA_ERR_UNSUPPORTED;
   int32_t splits = opts->num_splits;
   if (splits < 0 || splits > kMaxSplits) return MLA_ERR_INVALID_ARG;
-  if (splits == 0) splits = plan_splits(total_q, batch, total_kv, sm_count_of_current_device());
+  if (splits == 0) splits = plan_splits(total_q, batch, total_kv, sm_count_of_current_device(), G);
   // G tokens per group: G num_splits + total_q partial slots
   const size_t base = mla::workspace_bytes_for(G * static_cast<int64_t>(splits), total_q);
   const size_t need = base + (pg ? mla::paged_extra_bytes(batch) : 0);
@@ -193,6 +196,10 @@ mla_status_t decode_impl(const void* q, const void* kv, const void* kv_scale, co
   p.page_size = pg ? pg->page_size : 0;
   p.wait_late = (!pg && opts->quantize_q) ? 1 : 0;
   p.group = G;
+  // the cooperative merge pays when a group's merge is spread over two or more CTAs on average; it needs
+  // every CTA resident at once (one CTA per SM)
+  const int64_t groups = (static_cast<int64_t>(total_q) + G - 1) / G;
+  p.coop_merge = (splits <= sm_count_of_current_device() && 2 * groups <= splits) ? 1 : 0;
   p.page_shift = -1;
   for (int32_t sh = 0; sh < 31 && pg; ++sh)
     if ((int32_t{1} << sh) == pg->page_size) p.page_shift = sh;
@@ -253,11 +260,8 @@ mla_status_t mla_decode_group_workspace_size(int32_t batch, int32_t total_q, int
   if (!bytes || batch < 0 || total_q < 0 || total_kv < 0 || num_splits < 0 || num_splits > kMaxSplits ||
       token_group < 0 || (token_group > 2 && token_group != 4))
     return MLA_ERR_INVALID_ARG;
-  if (num_splits == 0) {
-    const mla_status_t st = mla_plan(batch, total_q, total_kv, kv_dtype, 0, &num_splits);
-    if (st != MLA_OK) return st;
-  }
   const int64_t g = token_group > 1 ? token_group : 1;
+  if (num_splits == 0) num_splits = plan_splits(total_q, batch, total_kv, sm_count_of_current_device(), g);
   *bytes = mla::workspace_bytes_for(g * num_splits, total_q);
   return MLA_OK;
 }
@@ -453,7 +457,9 @@ extern "C" mla_status_t mla_decode_static_workspace(const void* q, const void* k
   }
   if (opts->token_group < 0 || (opts->token_group > 2 && opts->token_group != 4)) return MLA_ERR_INVALID_ARG;
   mla_decode_opts o = *opts;
-  if (o.num_splits == 0) o.num_splits = plan_splits(o.total_q, o.batch, o.total_kv, sm_count_of_current_device());
+  if (o.num_splits == 0)
+    o.num_splits = plan_splits(o.total_q, o.batch, o.total_kv, sm_count_of_current_device(),
+                               o.token_group > 1 ? o.token_group : 1);
   const int64_t slot_splits = (o.token_group > 1 ? o.token_group : 1) * static_cast<int64_t>(o.num_splits);
   if (mla::workspace_bytes_for(slot_splits, o.total_q) > MLA_STATIC_WORKSPACE_BYTES) return MLA_ERR_TOO_LARGE;
   // the error flags and the token counters are the scratch that must start at zero

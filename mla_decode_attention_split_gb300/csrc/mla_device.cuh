@@ -117,8 +117,6 @@ __device__ __forceinline__ void cp_async16(uint32_t dst_smem, const void* src, u
                : "memory");
 }
 
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-
 // The mbarrier gets an arrival once all of this thread's earlier cp.async
 // copies have completed; its pending count is raised by one first, so the
 // current phase waits for that arrival without a change of its count.
@@ -129,12 +127,7 @@ __device__ __forceinline__ void cp_async_mbar_arrive(uint32_t bar) {
 // Waits for all of this thread's cp.async copies.
 __device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
 
-// Waits until at most N of this thread's committed copy groups are pending.
-template <int N>
-__device__ __forceinline__ void cp_async_wait() {
-  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
-}
-
+// L2 policy: lines read with it are the first to be evicted.
 __device__ __forceinline__ uint64_t policy_evict_first() {
   uint64_t p;
   asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
@@ -145,21 +138,6 @@ __device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t nthreads) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
 }
 
-// ---- shared memory vector loads ------------------------------------------
-__device__ __forceinline__ uint4 lds128(uint32_t addr) {
-  uint4 v;
-  asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];"
-               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-               : "r"(addr));
-  return v;
-}
-
-__device__ __forceinline__ uint32_t lds32(uint32_t addr) {
-  uint32_t v;
-  asm volatile("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(addr));
-  return v;
-}
-
 // ---- warp-level MMA --------------------------------------------------------
 // D(16x8 f32) += A(16x32 e4m3) * B(32x8 e4m3). Fragments (g = lane/4,
 // t = lane%4): a0 = A[g][4t..4t+3], a1 = A[g+8][4t..], a2 = A[g][16+4t..],
@@ -168,15 +146,6 @@ __device__ __forceinline__ uint32_t lds32(uint32_t addr) {
 __device__ __forceinline__ void mma_e4m3(float (&c)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
   asm volatile(
       "mma.sync.aligned.m16n8k32.row.col.f32.e4m3.e4m3.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
-      "{%0,%1,%2,%3};\n"
-      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
-      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
-}
-
-// Same with an e5m2 B operand (used for rebased mxfp4 values).
-__device__ __forceinline__ void mma_e4m3_e5m2(float (&c)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
-  asm volatile(
-      "mma.sync.aligned.m16n8k32.row.col.f32.e4m3.e5m2.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
       "{%0,%1,%2,%3};\n"
       : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
       : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
@@ -227,19 +196,6 @@ __device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
   uint32_t r;
   asm("prmt.b32 %0, %1, %2, %3;" : "=r"(r) : "r"(a), "r"(b), "r"(sel));
   return r;
-}
-
-// 4x4 byte transpose: in[r] holds bytes (r,0..3); out[c] gets bytes (0..3,c).
-__device__ __forceinline__ void transpose4x4_bytes(uint32_t r0, uint32_t r1, uint32_t r2, uint32_t r3,
-                                                   uint32_t& c0, uint32_t& c1, uint32_t& c2, uint32_t& c3) {
-  const uint32_t t0 = prmt(r0, r1, 0x5140);  // r0.b0 r1.b0 r0.b1 r1.b1
-  const uint32_t t1 = prmt(r0, r1, 0x7362);  // r0.b2 r1.b2 r0.b3 r1.b3
-  const uint32_t t2 = prmt(r2, r3, 0x5140);
-  const uint32_t t3 = prmt(r2, r3, 0x7362);
-  c0 = prmt(t0, t2, 0x5410);
-  c1 = prmt(t0, t2, 0x7632);
-  c2 = prmt(t1, t3, 0x5410);
-  c3 = prmt(t1, t3, 0x7632);
 }
 
 __device__ __forceinline__ float bf16_bits_to_f32(uint32_t bits16) { return __uint_as_float(bits16 << 16); }

@@ -48,6 +48,9 @@ struct Stage1Params {
   int32_t paged;
   int32_t group;      // query tokens per group sharing a pass over the KV rows (1, 2 or 4)
   int32_t wait_late;  // the kernel just before is this call's q amax: wait for it only before reading the scale
+  // nonzero when every CTA of the launch is resident at once (num_splits <= SM count, one CTA per SM):
+  // the CTAs that hold pieces of a split token then share its merge at their end (merge_coop)
+  int32_t coop_merge;
 };
 
 // KV formats / query formats as template tags (values match mla_dtype_t).

@@ -45,7 +45,7 @@ constexpr int kQChunk = kQRows * 128;            // 8 KB per 128-dim chunk
 constexpr int kPPart = kTileRows * 64;           // 8 KB: one part (hi or lo) of P
 constexpr uint32_t kSCols = 64;
 constexpr uint32_t kTmO = 2 * kSCols;            // O: 4 blocks x 64 columns
-constexpr uint32_t kLaunchRegs = 168, kAuxRegs = 120, kSoftRegs = 192;
+constexpr uint32_t kLaunchRegs = 168, kAuxRegs = 88, kSoftRegs = 208;
 static_assert(kAuxRegs * 128 + kSoftRegs * 256 == kLaunchRegs * kThreads, "register split");
 
 struct L {
@@ -135,20 +135,29 @@ __device__ void producer(const Cx& cx, const CUtensorMap* map, PieceCursor cur, 
   }
 }
 
-// Warp 1 (one thread): QK(n) into S[n % 2], then PV(n-1) into O. O has one
+// Warp 1 (one thread): QK(n) into S[n % 2] and PV(n) into O, each issued as
+// soon as its inputs are ready (a polling loop, not a fixed order): with two
+// stages, a P.V must not wait behind the landing of the next tile, whose load
+// starts only when the P.V before it has released its stage. O has one
 // buffer: the first P.V of piece k waits until the epilogue of piece k-1 has
 // read O.
-struct PendingPV {
-  uint32_t n, k;
-  bool first, last, valid;
-};
-
-__device__ bool issue_pv(const Cx& cx, const PendingPV& t) {
-  constexpr uint32_t id_pv = umma_idesc(128, 64, 0, 0, true, true);
-  if (!cx.wait(L::kPFull, t.n & 1u)) return false;
-  if (t.first && t.k >= 1 && !cx.wait(L::kOEmpty, (t.k - 1) & 1u)) return false;
+__device__ void issue_qk(const Cx& cx, uint32_t n, const TileMeta& t) {
+  constexpr uint32_t id_qk = umma_idesc(128, kSCols, 0, 0, false, false);
   tc_fence_after();
-  const uint32_t stage = cx.s + L::kOffKv + (t.n % kStages) * kStageBytes;
+  const uint32_t stage = cx.s + L::kOffKv + (n % kStages) * kStageBytes;
+  const uint32_t sbuf = cx.tmem + kSCols * (n & 1u);
+  const uint32_t qbuf = cx.s + L::kOffQ;
+#pragma unroll
+  for (int ks = 0; ks < 18; ++ks)  // the 512 V dims, then the 64 rope dims (box 4)
+    umma_e4m3(sbuf, qk_desc_a(stage, ks), qk_desc_b4(qbuf, ks), id_qk, ks > 0 ? 1u : 0u);
+  umma_commit(cx.bar(L::kSFull + (n & 1u)));
+  if (t.last) umma_commit(cx.bar(L::kQEmpty));
+}
+
+__device__ void issue_pv(const Cx& cx, uint32_t n, const TileMeta& t) {
+  constexpr uint32_t id_pv = umma_idesc(128, 64, 0, 0, true, true);
+  tc_fence_after();
+  const uint32_t stage = cx.s + L::kOffKv + (n % kStages) * kStageBytes;
   const uint32_t phi = cx.s + L::kOffP, plo = phi + kPPart;
 #pragma unroll
   for (int mb = 0; mb < 4; ++mb)
@@ -158,47 +167,57 @@ __device__ bool issue_pv(const Cx& cx, const PendingPV& t) {
       umma_e4m3(cx.tmem + kTmO + 64 * mb, a, pv_desc_b4(phi, ks), id_pv, (ks > 0 || !t.first) ? 1u : 0u);
       umma_e4m3(cx.tmem + kTmO + 64 * mb, a, pv_desc_b4(plo, ks), id_pv, 1u);
     }
-  umma_commit(cx.bar(L::kKvEmpty + (t.n % kStages)));
+  umma_commit(cx.bar(L::kKvEmpty + (n % kStages)));
   umma_commit(cx.bar(L::kPEmpty));
   if (t.last) umma_commit(cx.bar(L::kOFull));
-  return true;
 }
 
+// Phases tested below cannot run ahead by two: stage s is refilled only after
+// the P.V of its tile, the P buffer only after its P.V, the S buffer only
+// after the Q.K^T that read it back, and the next Q only after the last Q.K^T
+// of the piece.
 __device__ void mma_issuer(const Cx& cx, PieceCursor cur) {
-  constexpr uint32_t id_qk = umma_idesc(128, kSCols, 0, 0, false, false);
-  Piece pc;
-  uint32_t n = 0, k = 0;
-  PendingPV pend{0, 0, false, false, false};
-  bool ok = true;
-  while (ok && cur.next(pc)) {
-    if (!cx.wait(L::kQFull, k & 1u)) break;
-    const uint32_t qbuf = cx.s + L::kOffQ;
-    for (int r0 = 0; r0 < pc.nrows; r0 += kTileRows) {
-      const uint32_t s = n & 1u, st = n % kStages;
-      if (!cx.wait(L::kKvFull + st, (n / kStages) & 1u) ||
-          (n >= 2 && !cx.wait(L::kSEmpty + s, ((n >> 1) - 1) & 1u))) {
-        ok = false;
-        break;
+  const uint32_t n = static_cast<uint32_t>(count_tiles(cur));
+  MetaTileWalker wq, wp;
+  wq.init(cur);
+  wp.init(cur);
+  int32_t row;
+  uint32_t mq = 0, mp = 0;
+  wq.next(row, mq);
+  wp.next(row, mp);
+  uint32_t qi = 0, pi = 0;
+  long long t0 = clock64();
+  while (pi < n) {
+    bool progressed = false;
+    if (pi < qi && mbar_test_wait(cx.bar(L::kPFull), pi & 1u)) {
+      const TileMeta t = TileMeta::unpack(mp);
+      if (!t.first || t.k == 0 || mbar_test_wait(cx.bar(L::kOEmpty), (t.k - 1) & 1u)) {
+        issue_pv(cx, pi, t);
+        ++pi;
+        wp.next(row, mp);
+        progressed = true;
       }
-      tc_fence_after();
-      const uint32_t stage = cx.s + L::kOffKv + st * kStageBytes;
-      const uint32_t sbuf = cx.tmem + kSCols * s;
-#pragma unroll
-      for (int ks = 0; ks < 18; ++ks)  // the 512 V dims, then the 64 rope dims (box 4)
-        umma_e4m3(sbuf, qk_desc_a(stage, ks), qk_desc_b4(qbuf, ks), id_qk, ks > 0 ? 1u : 0u);
-      umma_commit(cx.bar(L::kSFull + s));
-      const bool last = r0 + kTileRows >= pc.nrows;
-      if (last) umma_commit(cx.bar(L::kQEmpty));
-      if (pend.valid && !issue_pv(cx, pend)) {
-        ok = false;
-        break;
-      }
-      pend = PendingPV{n, k, r0 == 0, last, true};
-      ++n;
     }
-    ++k;
+    if (qi < n && mbar_test_wait(cx.bar(L::kKvFull + qi % kStages), (qi / kStages) & 1u) &&
+        (qi < 2 || mbar_test_wait(cx.bar(L::kSEmpty + (qi & 1u)), ((qi - 2) >> 1) & 1u))) {
+      const TileMeta t = TileMeta::unpack(mq);
+      if (!t.first || mbar_test_wait(cx.bar(L::kQFull), t.k & 1u)) {
+        issue_qk(cx, qi, t);
+        ++qi;
+        wq.next(row, mq);
+        progressed = true;
+      }
+    }
+    if (progressed) {
+      t0 = clock64();
+    } else if (*cx.abort_word) {
+      break;
+    } else if (clock64() - t0 > kWaitLimitCycles) {
+      *cx.abort_word = 1u;
+      atomicOr(cx.flags, kFlagTimeout);
+      break;
+    }
   }
-  if (ok && pend.valid) issue_pv(cx, pend);
   // every issued tcgen05 operation completes before tensor memory is freed
   umma_commit(cx.bar(L::kDrain));
   mbar_wait_drain_tc(cx.bar(L::kDrain), 0);
@@ -335,14 +354,15 @@ __device__ __forceinline__ bool finish_half(const Stage1Params& p, const Cx& cx,
   if (!half_sync(cx, sx, hf)) return false;
   if (sx.wi == 0 && sx.lane == 0) {
     __threadfence();
-    const int64_t P = p.num_splits;
+    const int64_t P = cx.parts;
     const int64_t c0 = part_of_row(pc.tok_vs, cx.total, P), c1 = part_of_row(pc.tok_vs + pc.kvlen - 1, cx.total, P);
     MergeList* ml = reinterpret_cast<MergeList*>(cx.g + L::kOffMList);
     for (int t = 0; t < 2; ++t) {
       const int j = 2 * hf + t;
       if (j >= pc.ntok) break;
       const uint32_t arrived = atomicAdd(p.tok_cnt + pc.token + j, 1u) + 1u;
-      if (arrived == static_cast<uint32_t>(c1 - c0 + 1)) {
+      // cooperative merge: every CTA of the token lists it; otherwise the one that completes its count
+      if (p.coop_merge || arrived == static_cast<uint32_t>(c1 - c0 + 1)) {
         const uint32_t e = atomicAdd(&ml->n, 1u);
         if (e < kMergeMax) {
           ml->token[e] = pc.token + j;

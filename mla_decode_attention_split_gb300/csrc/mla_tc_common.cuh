@@ -51,6 +51,7 @@ struct Ctx {
   uint32_t* flags;
   uint32_t tmem;
   int64_t total;  // virtual rows of the whole launch
+  int64_t parts;  // CTAs that share them: min(num_splits, total), so that no range is empty
   __device__ __forceinline__ uint32_t bar(int i) const { return s + LL::kOffBars + 8u * i; }
   __device__ __forceinline__ bool wait(int i, uint32_t parity) const { return mbar_wait(bar(i), parity, abort_word, flags); }
 };
@@ -499,12 +500,13 @@ __device__ __forceinline__ bool finish_partial(const Stage1Params& p, const Ctx<
   if (!group_sync(cx, sx)) return false;
   if (sx.wi == 0 && sx.lane == 0) {
     __threadfence();
-    const int64_t P = p.num_splits;
+    const int64_t P = cx.parts;
     const int64_t c0 = part_of_row(pc.tok_vs, cx.total, P), c1 = part_of_row(pc.tok_vs + pc.kvlen - 1, cx.total, P);
     MergeList* ml = reinterpret_cast<MergeList*>(cx.g + LL::kOffMList);
     for (int i = 0; i < pc.ntok; ++i) {  // every token of the group
       const uint32_t arrived = atomicAdd(p.tok_cnt + pc.token + i, 1u) + 1u;
-      if (arrived == static_cast<uint32_t>(c1 - c0 + 1) && ml->n < kMergeMax) {
+      // cooperative merge: every CTA of the token lists it; otherwise the one that completes its count
+      if ((p.coop_merge || arrived == static_cast<uint32_t>(c1 - c0 + 1)) && ml->n < kMergeMax) {
         ml->token[ml->n] = pc.token + i;
         ml->c0[ml->n] = static_cast<int32_t>(c0);
         ml->c1[ml->n] = static_cast<int32_t>(c1);
@@ -617,6 +619,163 @@ __device__ void merge_listed(const Stage1Params& p, const Ctx<LL>& cx) {
   }
 }
 
+__device__ __forceinline__ uint32_t ld_acquire_u32(const uint32_t* p) {
+  uint32_t v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
+// The cooperative end-of-CTA merge, when every CTA of the launch is resident
+// at once (p.coop_merge). The n CTAs c0..c1 that hold pieces of a split token
+// share its merge: once the token's count has reached n (all its partials
+// published), CTA c0 + r takes units [64 r / n, 64 (r + 1) / n) of the 64
+// units (head h, 128-dim quarter q) = 4 h + q. Each unit is the pages' stage 2
+// over the token's n slots G c + token: L = max lse, w = 2^(lse - L),
+// out = sum w O / sum w, bf16 RNE. The units' slot rows (512 B each) come into
+// the free stage buffers by 16-byte asynchronous copies, one warp per row and
+// all of a batch in flight at once, as many units at a time as fit; one
+// thread per unit computes its weights from the LSEs (L2 loads), and one warp
+// then merges a unit (lane l: float4 l of the quarter). A second round of
+// counts returns the
+// token's counter to zero: the CTA that brings it to 2 n resets it, after all n
+// have passed their wait. All LL::kThreads threads call this.
+template <class LL>
+__device__ void merge_coop(const Stage1Params& p, const Ctx<LL>& cx) {
+  constexpr int kWarps = LL::kThreads / 32;
+  constexpr int kRowBytes = 128 * 4;                      // one unit row of one slot
+  constexpr int kCap = LL::kMergeBytes / kRowBytes;       // rows per batch
+  constexpr int kMaxUnits = kCap / 2;                     // a split token has n >= 2 slots
+  static_assert(kMaxUnits <= LL::kThreads, "one thread per unit of a batch");
+  static_assert(LL::kOffMList - LL::kOffQ >= 24 * kCap, "merge scratch between the Q buffer and the merge list");
+  const MergeList* ml = reinterpret_cast<const MergeList*>(cx.g + LL::kOffMList);
+  const int nm = static_cast<int>(ml->n < kMergeMax ? ml->n : kMergeMax);
+  bool ok = true;
+  if (threadIdx.x < nm) {
+    const uint32_t need = static_cast<uint32_t>(ml->c1[threadIdx.x] - ml->c0[threadIdx.x] + 1);
+    const uint32_t* cnt = p.tok_cnt + ml->token[threadIdx.x];
+    const long long t0 = clock64();
+    while (ld_acquire_u32(cnt) < need) {
+      if (*cx.abort_word) {
+        ok = false;
+        break;
+      }
+      if (clock64() - t0 > kWaitLimitCycles) {
+        atomicOr(cx.flags, kFlagTimeout);
+        ok = false;
+        break;
+      }
+    }
+  }
+  if (!__syncthreads_and(ok ? 1 : 0)) return;
+  // this CTA's units of each listed token: units [ub[e], ub[e] + cnt[e]) of n[e] rows each
+  int cnt[kMergeMax], ub[kMergeMax], nn[kMergeMax], units = 0;
+#pragma unroll
+  for (int e = 0; e < static_cast<int>(kMergeMax); ++e) {
+    cnt[e] = ub[e] = nn[e] = 0;
+    if (e < nm) {
+      const int n = ml->c1[e] - ml->c0[e] + 1, r = static_cast<int>(blockIdx.x) - ml->c0[e];
+      nn[e] = n;
+      ub[e] = 64 * r / n;
+      cnt[e] = 64 * (r + 1) / n - ub[e];
+      units += cnt[e];
+    }
+  }
+  // scratch in the (free) Q buffer: per unit of a batch {token, n, unit}, its first row and 1 / sum of its
+  // weights; per row its weight and the float offset of its source in the partials
+  int4* uinfo = reinterpret_cast<int4*>(cx.g + LL::kOffQ);
+  int* urow = reinterpret_cast<int*>(uinfo + kMaxUnits);
+  float* uinv = reinterpret_cast<float*>(urow + kMaxUnits);
+  float* rw = uinv + kMaxUnits;
+  int64_t* rsrc = reinterpret_cast<int64_t*>(rw + kCap);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint64_t pol = policy_evict_first();
+  int e0 = 0, i0 = 0;  // the batch's first unit: unit i0 of entry e0
+  while (e0 < nm) {
+    // the batch: whole units while their rows fit (the same walk in every thread)
+    int rows = 0, nb = 0, e1 = e0, i1 = i0;
+    while (e1 < nm) {
+      const int take = min(min(cnt[e1] - i1, (kCap - rows) / nn[e1]), kMaxUnits - nb);
+      rows += take * nn[e1];
+      nb += take;
+      i1 += take;
+      if (i1 < cnt[e1]) break;  // full
+      ++e1;
+      i1 = 0;
+    }
+    if (static_cast<int>(threadIdx.x) < nb) {
+      // unit t of the batch: entry e, index i; rows before it in the batch
+      int t = threadIdx.x, e = e0, i = i0, before = 0;
+      while (t >= cnt[e] - i) {
+        t -= cnt[e] - i;
+        before += (cnt[e] - i) * nn[e];
+        ++e;
+        i = 0;
+      }
+      i += t;
+      before += t * nn[e];
+      const int token = ml->token[e], n = nn[e], u = ub[e] + i, h = u >> 2, q = u & 3;
+      const int64_t c0 = ml->c0[e];
+      float mx = -INFINITY;
+      for (int j0 = 0; j0 < n; j0 += 8) {  // eight LSE loads in flight, then their stores
+        float l8[8];
+#pragma unroll
+        for (int k = 0; k < 8; ++k)
+          l8[k] = j0 + k < n ? __ldcg(p.part_lse + (p.group * (c0 + j0 + k) + token) * kHeads + h) : -INFINITY;
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+          if (j0 + k < n) {
+            rsrc[before + j0 + k] = ((p.group * (c0 + j0 + k) + token) * kHeads + h) * kDv + 128 * q;
+            rw[before + j0 + k] = l8[k];
+          }
+          mx = fmaxf(mx, l8[k]);
+        }
+      }
+      float sum = 0.f;
+      for (int j = 0; j < n; ++j) {
+        const float w = fast_exp2(rw[before + j] - mx);
+        rw[before + j] = w;
+        sum += w;
+      }
+      uinfo[threadIdx.x] = make_int4(token, n, u, 0);
+      urow[threadIdx.x] = before;
+      uinv[threadIdx.x] = 1.0f / sum;
+    }
+    __syncthreads();
+    for (int r = warp; r < rows; r += kWarps)
+      cp_async16(cx.s + LL::kOffKv + r * kRowBytes + 16 * lane, p.part_o + rsrc[r] + 4 * lane, pol);
+    cp_async_wait_all();
+    __syncthreads();
+    for (int t = warp; t < nb; t += kWarps) {
+      const int4 ui = uinfo[t];
+      const int rb = urow[t];
+      const float4* src = reinterpret_cast<const float4*>(cx.g + LL::kOffKv + static_cast<int64_t>(rb) * kRowBytes);
+      float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+      for (int j = 0; j < ui.y; ++j) {
+        const float w = rw[rb + j];
+        const float4 v = src[j * (kRowBytes / 16) + lane];
+        acc.x = fmaf(w, v.x, acc.x);
+        acc.y = fmaf(w, v.y, acc.y);
+        acc.z = fmaf(w, v.z, acc.z);
+        acc.w = fmaf(w, v.w, acc.w);
+      }
+      const float inv = uinv[t];
+      const int h = ui.z >> 2, q = ui.z & 3;
+      __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(p.out) + (static_cast<int64_t>(ui.x) * kHeads + h) * kDv +
+                           128 * q + 4 * lane;
+      *reinterpret_cast<uint2*>(dst) =
+          make_uint2(pack_bf16x2(acc.x * inv, acc.y * inv), pack_bf16x2(acc.z * inv, acc.w * inv));
+    }
+    __syncthreads();  // the buffers are free for the next batch
+    e0 = e1;
+    i0 = i1;
+  }
+  if (threadIdx.x < nm) {
+    const uint32_t need = static_cast<uint32_t>(ml->c1[threadIdx.x] - ml->c0[threadIdx.x] + 1);
+    uint32_t* cnt_w = p.tok_cnt + ml->token[threadIdx.x];
+    if (atomicAdd(cnt_w, 1u) + 1u == 2u * need) *cnt_w = 0u;
+  }
+}
+
 // Barrier setup, the block's partition and tensor-memory allocation, common to
 // both kernels. Returns false (before any allocation) when the CTA has no work
 // or the indptrs are invalid.
@@ -642,11 +801,13 @@ __device__ __forceinline__ bool cta_begin(const Stage1Params& p, Ctx<LL>& cx, ui
   // scale, and the q set-up waits for it instead.
   griddep_launch_dependents();
   if (!p.wait_late) griddep_wait();
-  const int64_t parts = p.num_splits, c = blockIdx.x;
+  const int64_t c = blockIdx.x;
+  // with fewer virtual rows than CTAs, the last CTAs get none (no range is empty)
+  auto eff_parts = [&](int64_t total) { return total < p.num_splits ? (total > 0 ? total : 1) : p.num_splits; };
   int64_t* sh = reinterpret_cast<int64_t*>(cx.g + LL::kOffScan);
   const SegLocate loc = block_locate<LL::kThreads, 1>(
       p.qo_indptr, p.kv_indptr, p.batch, p.total_q, p.total_kv, p.group,
-      [=](int64_t total) { return part_start(c, total, parts); }, 0, sh);
+      [=](int64_t total) { return part_start(c, total, eff_parts(total)); }, 0, sh);
   if (!loc.ok) {
     if (threadIdx.x == 0) atomicOr(p.dev_flags, kFlagBadIndptr);
     return false;
@@ -654,7 +815,9 @@ __device__ __forceinline__ bool cta_begin(const Stage1Params& p, Ctx<LL>& cx, ui
   if (blockIdx.x == 0 && threadIdx.x == 0) p.dev_flags[1] = static_cast<uint32_t>(p.total_q);  // counters in use
   zero_empty_tokens<LL::kThreads>(p);
   cx.total = loc.total;
-  const int64_t x0 = part_start(c, loc.total, parts), x1 = part_start(c + 1, loc.total, parts);
+  cx.parts = eff_parts(loc.total);
+  if (c >= cx.parts) return false;
+  const int64_t x0 = part_start(c, loc.total, cx.parts), x1 = part_start(c + 1, loc.total, cx.parts);
   if (x0 >= x1 || loc.seg < 0) return false;  // uniform across the block
   if ((threadIdx.x >> 5) == alloc_warp) tmem_alloc(cx.s + LL::kOffSlot, kTmemCols);
   tc_fence_before();
@@ -674,7 +837,11 @@ __device__ __forceinline__ void cta_end(const Stage1Params& p, const Ctx<LL>& cx
     tc_fence_after();
     tmem_dealloc(cx.tmem, kTmemCols);
   }
-  if (!*cx.abort_word) merge_listed(p, cx);
+  if (*cx.abort_word) return;
+  if (p.coop_merge)
+    merge_coop(p, cx);
+  else
+    merge_listed(p, cx);
 }
 
 // Host: the tensor map of a KV cache of `rows` rows of 576 bytes, boxes of

@@ -80,6 +80,26 @@ def test_ragged_segments_all_split_counts(q_dtype, kv_dtype, num_splits):
     check(got.float().cpu().numpy(), oracle_ref(inp))
 
 
+@pytest.mark.parametrize("kv_dtype", [synth.FP8_E4M3, synth.BF16, synth.MXFP4])
+@pytest.mark.parametrize("num_splits", [9, 40, 151, 152, 300])
+def test_more_splits_than_rows(kv_dtype, num_splits):
+    # 9 KV rows in all: every CTA past the ninth gets none, and a token's pieces
+    # are one row each (the merge of up to 5 one-row partials), for the
+    # cooperative end-of-CTA merge (<= SM count) and the last-CTA merge (300)
+    w = synth.Workload("tiny", 3, 1, 0, synth.BF16, kv_dtype, seed=23)
+    inp = synth.make_inputs(w, "cuda", kv_lens=[3, 5, 1], q_lens=[1, 2, 1])
+    ref = oracle_ref(inp)
+    ws = m.alloc_workspace(inp.batch, inp.total_q, inp.total_kv, inp.kv_dtype, num_splits=num_splits)
+    for _ in range(2):  # the counters are left at zero for the next call
+        out = torch.full((inp.total_q, 16, 512), float("nan"), dtype=torch.bfloat16, device="cuda")
+        m.decode(inp.q, inp.kv, inp.kv_scale, inp.qo_indptr, inp.kv_indptr, out, inp.kv_dtype, workspace=ws,
+                 q_dtype=inp.q_dtype, q_scale=inp.q_scale, num_splits=num_splits)
+        torch.cuda.synchronize()
+        assert m.device_error(ws)[0] == m.MLA_OK
+        assert int(torch.count_nonzero(ws[256:512])) == 0
+        check(out.float().cpu().numpy(), ref)
+
+
 @pytest.mark.parametrize("q_dtype,kv_dtype", [(synth.BF16, synth.FP8_E4M3), (synth.BF16, synth.BF16),
                                               (synth.BF16, synth.MXFP4)])
 def test_multi_token_and_empty_segments(q_dtype, kv_dtype):
