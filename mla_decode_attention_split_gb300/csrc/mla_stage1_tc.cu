@@ -163,40 +163,54 @@ __device__ PagedDrain producer_paged(const Stage1Params& p, const Cx& cx, const 
   for (uint32_t n = 0; have; ++n) {
     const uint32_t s = n % kStages, rnd = n / kStages;
     // the tile's rows and runs are worked out before its stage is free
-    int32_t phys[4];      // tile rows lane + 32 j
+    int32_t phys[4];  // tile rows lane + 32 j
+#pragma unroll
+    for (int j = 0; j < 4; ++j) phys[j] = phys_row(p, id[j]);
     uint32_t contig = 0;  // bit g: rows 8g..8g+7 are consecutive rows of the pool
     uint32_t linked = 0;  // bit g: row 8g follows row 8g-1 in the pool
-    int32_t last_prev = -1;
+    int32_t run_y = 0, run_len = 0;
+    // the whole tile one run of the pool (pages laid out in order, or pages of
+    // 128 rows and more): one box per chunk
+    const int32_t phys0 = __shfl_sync(0xffffffffu, phys[0], 0);
+    const bool whole = __all_sync(0xffffffffu, phys0 >= 0 && phys[0] == phys0 + lane && phys[1] == phys0 + 32 + lane &&
+                                                   phys[2] == phys0 + 64 + lane && phys[3] == phys0 + 96 + lane);
+    if (whole) {
+      contig = 0xFFFFu;
+      linked = 0xFFFEu;
+      run_y = phys0;
+      run_len = lane == 0 ? 16 : 0;
+    } else {
+      int32_t last_prev = -1;
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      phys[j] = phys_row(p, id[j]);
-      int32_t prev = __shfl_up_sync(0xffffffffu, phys[j], 1);
-      if (lane == 0) prev = last_prev;
-      last_prev = __shfl_sync(0xffffffffu, phys[j], 31);
-      const bool follows = phys[j] >= 0 && prev >= 0 && phys[j] == prev + 1;
-      const uint32_t b = __ballot_sync(0xffffffffu, phys[j] >= 0 && ((lane & 7) == 0 || follows));
-      const uint32_t l = __ballot_sync(0xffffffffu, follows);
+      for (int j = 0; j < 4; ++j) {
+        int32_t prev = __shfl_up_sync(0xffffffffu, phys[j], 1);
+        if (lane == 0) prev = last_prev;
+        last_prev = __shfl_sync(0xffffffffu, phys[j], 31);
+        const bool follows = phys[j] >= 0 && prev >= 0 && phys[j] == prev + 1;
+        const uint32_t b = __ballot_sync(0xffffffffu, phys[j] >= 0 && ((lane & 7) == 0 || follows));
+        const uint32_t l = __ballot_sync(0xffffffffu, follows);
 #pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        if (((b >> (8 * q)) & 0xFFu) == 0xFFu) contig |= 1u << (4 * j + q);
-        if ((l >> (8 * q)) & 1u) linked |= 1u << (4 * j + q);
+        for (int q = 0; q < 4; ++q) {
+          if (((b >> (8 * q)) & 0xFFu) == 0xFFu) contig |= 1u << (4 * j + q);
+          if ((l >> (8 * q)) & 1u) linked |= 1u << (4 * j + q);
+        }
+      }
+      // runs: a contiguous group starts one unless it continues the previous
+      // contiguous group; lane g < 16 holds the first pool row and the length
+      // (in groups) of the run that starts at group g
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const int32_t v = __shfl_sync(0xffffffffu, phys[j], (lane & 3) * 8);
+        if ((lane >> 2) == j) run_y = v;
+      }
+      const uint32_t starts0 = contig & ~((contig << 1) & linked);
+      if (lane < 16 && ((starts0 >> lane) & 1u)) {
+        // groups lane + 1.. that continue the run: the trailing ones of (contig & linked) >> (lane + 1)
+        const uint32_t cont = (contig & linked) >> (lane + 1);
+        run_len = min(__ffs(~cont), 16 - lane);
       }
     }
-    // runs: a contiguous group starts one unless it continues the previous
-    // contiguous group; lane g < 16 holds the first pool row and the length
-    // (in groups) of the run that starts at group g
     const uint32_t starts = contig & ~((contig << 1) & linked);
-    int32_t run_y = 0, run_len = 0;
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      const int32_t v = __shfl_sync(0xffffffffu, phys[j], (lane & 3) * 8);
-      if ((lane >> 2) == j) run_y = v;
-    }
-    if (lane < 16 && ((starts >> lane) & 1u)) {
-      run_len = 1;
-      while (lane + run_len < 16 && ((contig >> (lane + run_len)) & 1u) && ((linked >> (lane + run_len)) & 1u))
-        ++run_len;
-    }
     if (rnd >= 1 && !cx.wait(L::kKvEmpty + s, (rnd - 1) & 1u)) break;
     const uint32_t bar = cx.bar(L::kKvFull + s);
     const uint32_t stage = cx.s + L::kOffKv + s * kStageBytes;
