@@ -65,7 +65,7 @@ struct L {
   static constexpr int kOffBars = kOffQpAmax + 16;
   enum {
     kKvFull = 0, kKvEmpty = 3, kSFull = 6, kSEmpty = 8, kRopeFull = 10, kPFull = 11, kPEmpty = 12, kQFull = 13,
-    kQEmpty = 14, kOFull = 15, kOEmpty = 17, kGrp = 19, kDrain = 21, kMerge = 22, kNumBars = 23
+    kQEmpty = 14, kOFull = 15, kOEmpty = 17, kGrp = 19, kDrain = 21, kMerge = 22, kQ0 = 23, kNumBars = 24
   };
   static constexpr int kMergeBytes = kStages * kStageBytes;  // the stages hold partials for the end-of-CTA merge
   static constexpr int kOffSlot = kOffBars + kNumBars * 8;
@@ -91,6 +91,7 @@ struct L {
     mbar_init(cx.bar(kQFull), 4);  // piece 0: the 4 softmax warps; later pieces: the 2 q-prep warps, 2 each
     mbar_init(cx.bar(kQEmpty), 1);
     mbar_init(cx.bar(kDrain), 1);
+    mbar_init(cx.bar(kQ0), 4);  // the CTA's first Q operand is in (one phase)
     for (int i = 0; i < 4; ++i) reinterpret_cast<volatile uint32_t*>(cx.g + kOffCRing + 16)[i] = 0u;
   }
 };
@@ -99,7 +100,9 @@ static_assert(L::kOffQ % 1024 == 0 && L::kOffRope % 1024 == 0, "operands need 10
 using Cx = Ctx<L>;
 
 // Warp 0: the V dims of each tile, four 128-row x 128-byte boxes, into stage
-// (tile % 3) once the tile three back has been released by its P.V.
+// (tile % 3) once the tile three back has been released by its P.V. Tiles
+// after the first wait until the CTA's first Q operand is in: the q (and rope)
+// loads of the call's start then do not queue behind every CTA's full ring.
 __device__ void producer(const Cx& cx, const CUtensorMap* map, PieceCursor cur, int lane) {
   const uint64_t pol = policy_evict_first();
   Piece pc;
@@ -108,7 +111,7 @@ __device__ void producer(const Cx& cx, const CUtensorMap* map, PieceCursor cur, 
   while (ok && cur.next(pc)) {
     for (int r0 = 0; r0 < pc.nrows; r0 += kTileRows) {
       const uint32_t s = n % kStages, rnd = n / kStages;
-      if (rnd >= 1 && !cx.wait(L::kKvEmpty + s, (rnd - 1) & 1u)) {
+      if ((n == 1 && !cx.wait(L::kQ0, 0)) || (rnd >= 1 && !cx.wait(L::kKvEmpty + s, (rnd - 1) & 1u))) {
         ok = false;
         break;
       }
@@ -586,6 +589,7 @@ __device__ void softmax_role(const Stage1Params& p, const Cx& cx, PieceCursor cu
   }
   float c = setup_q<L, QF>(p, cx, sx, pc.token, 0, kvsc);
   if (c < 0.f) return;
+  if (lane == 0) mbar_arrive(cx.bar(L::kQ0));
   uint32_t n = 0, k = 0;
   int tiles_left = 0;  // tiles of the CTA after the current one (for the rope slot)
   {
