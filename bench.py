@@ -176,6 +176,38 @@ def l2_flush(buf, i):
     buf.fill_(i & 0xFF)
 
 
+BACK_TO_BACK = "back to back: the calls issued without a host synchronisation, timed as a sequence"
+
+
+def time_calls(m, torch, call, steps, warmup, flush_l2: bool) -> float:
+    """Device µs per call. Cold: L2 flushed before each call, CUDA events around the call (the
+    GPU is busy with the flush while the host prepares the launch), median over steps. Warm:
+    `steps` calls back to back with no host synchronisation in between (consecutive launches
+    overlap through programmatic dependent launch), events at the two ends of the sequence."""
+    if flush_l2:
+        flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device="cuda")
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
+        tot = []
+        for i in range(warmup + steps):
+            l2_flush(flush, i)
+            call(ev)
+            torch.cuda.synchronize()
+            if i >= warmup:
+                tot.append(m.elapsed_ms(ev[0], ev[2]) * 1e3)
+        del flush
+        return statistics.median(tot)
+    for _ in range(warmup):
+        call()
+    torch.cuda.synchronize()
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t0.record()
+    for _ in range(steps):
+        call()
+    t1.record()
+    torch.cuda.synchronize()
+    return t0.elapsed_time(t1) * 1e3 / steps
+
+
 def time_workload(m, synth, torch, name, steps, warmup, flush_l2: bool, quantize_q: bool = False, w=None,
                   token_group: int = 0):
     """Per-call device time of one workload (stage-1 and total), median over steps.
@@ -187,25 +219,17 @@ def time_workload(m, synth, torch, name, steps, warmup, flush_l2: bool, quantize
     inp = synth.make_inputs(w, "cuda")
     out = torch.empty((inp.total_q, 16, 512), dtype=torch.bfloat16, device="cuda")
     ws = m.alloc_group_workspace(inp.batch, inp.total_q, inp.total_kv, inp.kv_dtype, token_group)
-    flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device="cuda") if flush_l2 else None
-    ev = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
-    tot, st1 = [], []
-    for i in range(warmup + steps):
-        if flush is not None:
-            l2_flush(flush, i)
+
+    def call(events=None):
         m.decode(inp.q, inp.kv, inp.kv_scale, inp.qo_indptr, inp.kv_indptr, out, inp.kv_dtype, workspace=ws,
-                 q_dtype=inp.q_dtype, q_scale=inp.q_scale, events=ev, quantize_q=quantize_q, token_group=token_group)
-        torch.cuda.synchronize()
-        if i >= warmup:
-            tot.append(m.elapsed_ms(ev[0], ev[2]) * 1e3)
-            st1.append(m.elapsed_ms(ev[0], ev[1]) * 1e3)
+                 q_dtype=inp.q_dtype, q_scale=inp.q_scale, events=events, quantize_q=quantize_q,
+                 token_group=token_group)
+
+    us = time_calls(m, torch, call, steps, warmup, flush_l2)
     st, flags = m.device_error(ws)
     assert st == m.MLA_OK, (name, flags)
-    us = statistics.median(tot)
-    return {"us_per_call": round(us, 2), "stage1_us": round(statistics.median(st1), 2),
-            "kv_gbs": round(kv_bytes(inp) / (us * 1e-6) / 1e9, 1), "kv_bytes": kv_bytes(inp),
-            "num_splits": m.plan(inp.batch, inp.total_q, inp.total_kv, inp.kv_dtype),
-            "l2": L2_FLUSHED if flush_l2 else "back-to-back"}
+    return {"us_per_call": round(us, 2), "kv_gbs": round(kv_bytes(inp) / (us * 1e-6) / 1e9, 1),
+            "kv_bytes": kv_bytes(inp), "l2": L2_FLUSHED if flush_l2 else BACK_TO_BACK}
 
 
 def time_paged_workload(m, synth, torch, name, page_size, steps, warmup, flush_l2: bool, in_order: bool = False):
@@ -218,25 +242,19 @@ def time_paged_workload(m, synth, torch, name, page_size, steps, warmup, flush_l
         pin = dataclasses.replace(pin, page_indices=torch.sort(pin.page_indices).values.contiguous())
     out = torch.empty((pin.total_q, 16, 512), dtype=torch.bfloat16, device="cuda")
     ws = m.alloc_paged_workspace(pin.batch, pin.total_q, pin.total_kv, synth.FP8_E4M3)
-    flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device="cuda") if flush_l2 else None
-    ev = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
-    tot = []
-    for i in range(warmup + steps):
-        if flush is not None:
-            l2_flush(flush, i)
+
+    def call(events=None):
         m.decode_paged(pin.q, pin.kv_pages, pin.kv_scale, pin.qo_indptr, pin.page_indptr, pin.page_indices,
                        pin.last_page_len, page_size, out, synth.FP8_E4M3, total_kv=pin.total_kv, workspace=ws,
-                       q_dtype=pin.q_dtype, q_scale=pin.q_scale, events=ev)
-        torch.cuda.synchronize()
-        if i >= warmup:
-            tot.append(m.elapsed_ms(ev[0], ev[2]) * 1e3)
+                       q_dtype=pin.q_dtype, q_scale=pin.q_scale, events=events)
+
+    us = time_calls(m, torch, call, steps, warmup, flush_l2)
     st, flags = m.device_error(ws)
     assert st == m.MLA_OK, (name, page_size, flags)
-    us = statistics.median(tot)
     kvb = pin.total_kv * synth.D_QK  # the rows read (the pool's spare pages are not)
     return {"us_per_call": round(us, 2), "kv_gbs": round(kvb / (us * 1e-6) / 1e9, 1), "kv_bytes": kvb,
             "page_size": page_size, "pages": pin.num_pages, "page_order": "pool order" if in_order else "random",
-            "l2": L2_FLUSHED if flush_l2 else "back-to-back"}
+            "l2": L2_FLUSHED if flush_l2 else BACK_TO_BACK}
 
 
 def _first_rows(h, rows):

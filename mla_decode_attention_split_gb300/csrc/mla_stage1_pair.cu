@@ -387,16 +387,16 @@ __device__ void softmax_role(const Stage1Params& p, const CxT<kQ8>& cx, PieceCur
   Piece pc, nxt;
   bool have = ahead.next(pc);
   if (!have) return;
-  // rope of tiles 0 and 1 into registers; tile 0 into the slot; tile 2 loads
+  // rope of tiles 0 and 1 into registers, the first Q, tile 0 into the slot, tile 2 loads
   TileWalker rw;
   rw.init(cur);
   uint4 rb0[4], rb1[4];  // rope of the even / odd tile in flight
   load_rope(p, rw, sx.row, rb0);
   load_rope(p, rw, sx.row, rb1);
+  float ca, cb;  // the first Q operand while those rope rows are in flight
+  if (!setup_q2<kQ8, QF>(p, cx, sx, pc, 0, kvsc, ca, cb)) return;
   store_rope<kQ8>(cx, sx, rb0);
   load_rope(p, rw, sx.row, rb0);
-  float ca, cb;
-  if (!setup_q2<kQ8, QF>(p, cx, sx, pc, 0, kvsc, ca, cb)) return;
   uint32_t n = 0, k = 0;
   int tiles_left = count_tiles(cur) - 1;  // tiles of the CTA after the current one (for the rope slot)
   while (have) {

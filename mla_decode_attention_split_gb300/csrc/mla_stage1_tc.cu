@@ -566,8 +566,8 @@ __device__ void softmax_role(const Stage1Params& p, const Cx& cx, PieceCursor cu
   Piece pc, nxt;
   bool have = ahead.next(pc);
   if (!have) return;
-  // rope of tiles 0 and 1 into registers; tile 0 into the slot; tile 2 loads
-  // (a paged cache: the rope warp does this)
+  // rope of tiles 0 and 1 into registers, the first Q operand, tile 0 into the
+  // slot, tile 2 loads (a paged cache: through the rows' page ids)
   TileWalker rw;
   uint4 rb0[4], rb1[4];  // rope of the even / odd tile in flight
   PagedRow rid = page_of_none();  // paged: the page id of this row of the tile after the next rope load
@@ -575,21 +575,24 @@ __device__ void softmax_role(const Stage1Params& p, const Cx& cx, PieceCursor cu
   if constexpr (!kPaged) {
     load_rope(p, rw, sx.row, rb0);
     load_rope(p, rw, sx.row, rb1);
-    store_rope(cx, sx, rb0);
-    load_rope(p, rw, sx.row, rb0);
   } else {
     rid = next_rope_id(p, rw, sx.row);
     load_rope_paged(p, rid, rb0);
     rid = next_rope_id(p, rw, sx.row);
     load_rope_paged(p, rid, rb1);
-    store_rope(cx, sx, rb0);
+  }
+  // the first Q operand while those rope rows are in flight
+  float c = setup_q<L, QF>(p, cx, sx, pc.token, 0, kvsc);
+  if (c < 0.f) return;
+  if (lane == 0) mbar_arrive(cx.bar(L::kQ0));
+  store_rope(cx, sx, rb0);
+  if constexpr (!kPaged) {
+    load_rope(p, rw, sx.row, rb0);
+  } else {
     rid = next_rope_id(p, rw, sx.row);
     load_rope_paged(p, rid, rb0);
     rid = next_rope_id(p, rw, sx.row);
   }
-  float c = setup_q<L, QF>(p, cx, sx, pc.token, 0, kvsc);
-  if (c < 0.f) return;
-  if (lane == 0) mbar_arrive(cx.bar(L::kQ0));
   uint32_t n = 0, k = 0;
   int tiles_left = 0;  // tiles of the CTA after the current one (for the rope slot)
   {
