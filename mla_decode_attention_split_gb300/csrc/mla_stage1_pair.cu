@@ -176,6 +176,90 @@ __device__ bool issue_pv(const CxT<kQ8>& cx, const PendingPV& t) {
   return true;
 }
 
+// With two stages (bf16 q), Q.K^T(n) and P.V(n) are each issued as soon as
+// their inputs are ready (a polling loop): a P.V must not wait behind the
+// landing of the next tile, whose load starts only when the P.V before it has
+// released its stage. The phases tested cannot run ahead by two: stage s is
+// refilled only after the P.V of its tile, the P buffer only after its P.V,
+// the S buffer only after the Q.K^T that read it back, the rope slot only
+// after the Q.K^T that read it, and the next Q only after the last Q.K^T of
+// the piece.
+template <bool kQ8>
+__device__ void issue_qk_at(const CxT<kQ8>& cx, uint32_t n, const TileMeta& t) {
+  using L = LT<kQ8>;
+  constexpr int kStages = L::kStages;
+  constexpr uint32_t id_qk = umma_idesc(128, L::kSCols, 0, 0, false, false);
+  const uint32_t s = n & 1u, st = n % kStages;
+  tc_fence_after();
+  const uint32_t stage = cx.s + L::kOffKv + st * kStageBytes;
+  const uint32_t sbuf = cx.tmem + L::kSCols * s;
+  const uint32_t qbuf = cx.s + L::kOffQ;
+#pragma unroll
+  for (int ks = 0; ks < 16; ++ks)  // the 512 V dims, from the stage
+    umma_e4m3(sbuf, qk_desc_a(stage, ks), qk_desc_b2<kQ8>(qbuf, ks), id_qk, ks > 0 ? 1u : 0u);
+#pragma unroll
+  for (int ks = 0; ks < 2; ++ks) {  // the 64 rope dims, from tensor memory or the rope slot
+    if constexpr (kQ8)
+      umma_e4m3_ta(sbuf, cx.tmem + L::kTmemRope + 8 * ks, qk_desc_b2<kQ8>(qbuf, 16 + ks), id_qk, 1u);
+    else
+      umma_e4m3(sbuf, rope_desc_a(cx.s + L::kOffRope, ks), qk_desc_b2<kQ8>(qbuf, 16 + ks), id_qk, 1u);
+  }
+  umma_commit(cx.bar(L::kSFull + s));
+  if (t.last) umma_commit(cx.bar(L::kQEmpty));
+}
+
+template <bool kQ8>
+__device__ void mma_issuer_polling(const CxT<kQ8>& cx, PieceCursor cur) {
+  using L = LT<kQ8>;
+  constexpr int kStages = L::kStages;
+  const uint32_t n = static_cast<uint32_t>(count_tiles(cur));
+  MetaTileWalker wq, wp;
+  wq.init(cur);
+  wp.init(cur);
+  int32_t row;
+  uint32_t mq = 0, mp = 0;
+  wq.next(row, mq);
+  wp.next(row, mp);
+  uint32_t qi = 0, pi = 0;
+  long long t0 = clock64();
+  while (pi < n) {
+    bool progressed = false;
+    if (pi < qi && mbar_test_wait(cx.bar(L::kPFull), pi & 1u)) {
+      const TileMeta t = TileMeta::unpack(mp);
+      if (!t.first || t.k == 0 || mbar_test_wait(cx.bar(L::kOEmpty), (t.k - 1) & 1u)) {
+        // its own waits (P full, O free) pass at once
+        if (!issue_pv<kQ8>(cx, PendingPV{pi, t.k, t.first, t.last, true})) break;
+        ++pi;
+        wp.next(row, mp);
+        progressed = true;
+      }
+    }
+    if (qi < n && mbar_test_wait(cx.bar(L::kKvFull + qi % kStages), (qi / kStages) & 1u) &&
+        mbar_test_wait(cx.bar(L::kRopeFull), qi & 1u) &&
+        (qi < 2 || mbar_test_wait(cx.bar(L::kSEmpty + (qi & 1u)), ((qi - 2) >> 1) & 1u))) {
+      const TileMeta t = TileMeta::unpack(mq);
+      if (!t.first || mbar_test_wait(cx.bar(L::kQFull), t.k & 1u)) {
+        issue_qk_at<kQ8>(cx, qi, t);
+        ++qi;
+        wq.next(row, mq);
+        progressed = true;
+      }
+    }
+    if (progressed) {
+      t0 = clock64();
+    } else if (*cx.abort_word) {
+      break;
+    } else if (clock64() - t0 > kWaitLimitCycles) {
+      *cx.abort_word = 1u;
+      atomicOr(cx.flags, kFlagTimeout);
+      break;
+    }
+  }
+  // every issued tcgen05 operation completes before tensor memory is freed
+  umma_commit(cx.bar(L::kDrain));
+  mbar_wait_drain_tc(cx.bar(L::kDrain), 0);
+}
+
 template <bool kQ8>
 __device__ void mma_issuer(const CxT<kQ8>& cx, PieceCursor cur) {
   using L = LT<kQ8>;
@@ -540,7 +624,12 @@ __global__ void __launch_bounds__(kThreads, 1) stage1_pair_kernel(const Stage1Pa
   if (warp == 0) {
     producer<kQ8>(cx, &kvmap, cur, lane);
   } else if (warp == 1) {
-    if (lane == 0) mma_issuer<kQ8>(cx, cur);
+    if (lane == 0) {
+      if constexpr (kQ8)
+        mma_issuer<kQ8>(cx, cur);
+      else
+        mma_issuer_polling<kQ8>(cx, cur);
+    }
     __syncwarp();
   } else if (warp < 6) {
     softmax_role<QF, kQ8>(p, cx, cur, warp, lane);
