@@ -21,8 +21,10 @@
 //  * with fp8 q (a8w8, or q quantised in the call) q has no lo rows, so the
 //    two tokens' codes fill one 32-row Q buffer (Q.K^T at N = 32) and the
 //    rope operand moves into tensor memory (A read from TMEM): that frees
-//    room for a third 64 KB stage, which the two-stage ring lacks (its MMA
-//    waits for KV at every tile).
+//    room for a third 64 KB stage;
+//  * with bf16 q (two stages) the MMA warp issues each product from a
+//    polling loop as soon as its inputs are ready, so a P.V does not wait
+//    behind the landing of the next tile.
 // A token's arithmetic (tiles, maxima, weights, accumulation) is the same as
 // in the single-token kernel, so with one partition per segment both give the
 // same bits.
