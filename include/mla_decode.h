@@ -84,7 +84,13 @@ typedef enum {
 } mla_status_t;
 
 /* Device error flags, as returned by mla_get_device_error().                  */
-#define MLA_DEVFLAG_TIMEOUT 0x1u
+#define MLA_DEVFLAG_TIMEOUT 0x1u  /* a bounded wait (~1 s) ran out. Besides a fault of
+                                     the library, this can happen when a call that
+                                     splits query tokens over two or more CTAs each
+                                     (its CTAs then share the merges at their end and
+                                     wait for one another) cannot place all of its
+                                     CTAs on the GPU within that time, e.g. next to a
+                                     long persistent kernel on another stream */
 #define MLA_DEVFLAG_BAD_INDPTR 0x2u
 #define MLA_DEVFLAG_BAD_PAGE 0x4u  /* mla_decode_paged: a page id >= num_pages */
 

@@ -88,6 +88,22 @@ def test_token_pairs_decode_replays_bitwise(q_dtype):
         assert torch.equal(r, eager)
 
 
+def test_token_groups_of_four_replay_bitwise():
+    w = synth.Workload("graphquad", 4, 1, 0, synth.FP8_E4M3, synth.FP8_E4M3, seed=55)
+    inp = synth.make_inputs(w, "cuda", kv_lens=[700, 64, 1301, 3], q_lens=[4, 3, 5, 1])
+    out = torch.empty((inp.total_q, 16, 512), dtype=torch.bfloat16, device="cuda")
+    ws = m.alloc_group_workspace(inp.batch, inp.total_q, inp.total_kv, inp.kv_dtype, 4, num_splits=11)
+
+    def call():
+        m.decode(inp.q, inp.kv, inp.kv_scale, inp.qo_indptr, inp.kv_indptr, out, inp.kv_dtype, workspace=ws,
+                 q_dtype=inp.q_dtype, q_scale=inp.q_scale, num_splits=11, token_group=4)
+
+    eager, replays = _captured(call, out)
+    assert m.device_error(ws)[0] == m.MLA_OK
+    for r in replays:
+        assert torch.equal(r, eager)
+
+
 def test_paged_decode_replays_bitwise():
     lens = [700, 0, 1301, 65]
     w = synth.Workload("graphpaged", len(lens), 1, 0, synth.BF16, synth.FP8_E4M3, seed=52)

@@ -118,6 +118,27 @@ def test_static_workspace_with_token_pairs():
     assert torch.equal(out, ref)
 
 
+def test_static_workspace_with_token_groups_of_four():
+    # groups of four need 4 num_splits + total_q partial slots; the fixed array serves them too
+    w = synth.Workload("quad", 3, 1, 0, synth.FP8_E4M3, synth.FP8_E4M3, seed=34)
+    inp = synth.make_inputs(w, "cuda", kv_lens=[2000, 64, 700], q_lens=[4, 5, 2])
+    out = torch.full((inp.total_q, 16, 512), float("nan"), dtype=torch.bfloat16, device="cuda")
+    opts = m.make_opts(inp.batch, inp.total_q, inp.total_kv, q_dtype=inp.q_dtype, q_scale=inp.q_scale,
+                       num_splits=9, token_group=4)
+    p = lambda t: None if t is None else ctypes.c_void_p(t.data_ptr())  # noqa: E731
+    st = m.lib().mla_decode_static_workspace(p(inp.q), p(inp.kv), p(inp.kv_scale), p(inp.qo_indptr),
+                                             p(inp.kv_indptr), p(out), inp.kv_dtype, ctypes.byref(opts),
+                                             ctypes.c_void_p(torch.cuda.current_stream().cuda_stream))
+    assert st == m.MLA_OK
+    assert m.static_workspace_device_error() == (m.MLA_OK, 0)
+    ref = torch.empty_like(out)
+    ws = m.alloc_group_workspace(inp.batch, inp.total_q, inp.total_kv, inp.kv_dtype, 4, num_splits=9)
+    m.decode(inp.q, inp.kv, inp.kv_scale, inp.qo_indptr, inp.kv_indptr, ref, inp.kv_dtype, workspace=ws,
+             q_dtype=inp.q_dtype, q_scale=inp.q_scale, num_splits=9, token_group=4)
+    torch.cuda.synchronize()
+    assert torch.equal(out, ref)
+
+
 def test_static_workspace_rejects_oversize_requests():
     # (num_splits + total_q) slots of 16 x 512 fp32 must fit in the fixed array
     slots = m.STATIC_WORKSPACE_BYTES // (16 * 512 * 4 + 64) + 1
