@@ -524,3 +524,51 @@ def test_workload_large_full(name):
                        "segment_rel_l2_median": float(np.median(seg)), "segment_rel_l2_max": float(seg.max()),
                        "worst_segment": worst, "worst_segment_kv_len": int(kvp[worst + 1] - kvp[worst]),
                        "num_splits": m.plan(inp.batch, inp.total_q, inp.total_kv, inp.kv_dtype)}, f, indent=1)
+
+
+def _rising_inputs(q_dtype, kv_dtype, q_lens, kv_lens, seed):
+    """Scores that rise along each segment (rope dim 512 of K, which is not a V dim, is a ramp
+    0..300 and q's dim 512 is 1 in every head) with N(0,1) elsewhere, plus one spike row in the
+    middle: in log2 units the softmax reference of a head moves several times within a segment,
+    and after the spike it stays above the rising rows."""
+    g = torch.Generator(device="cpu").manual_seed(seed)
+    qo = torch.tensor([0] + list(np.cumsum(q_lens)), dtype=torch.int32)
+    kvp = torch.tensor([0] + list(np.cumsum(kv_lens)), dtype=torch.int32)
+    qf = torch.randn((int(qo[-1]), 16, 576), generator=g)
+    qf[:, :, 512] = 1.0
+    kvf = torch.randn((int(kvp[-1]), 576), generator=g)
+    for b, n in enumerate(kv_lens):
+        k0 = int(kvp[b])
+        kvf[k0:k0 + n, 512] = torch.linspace(0.0, 300.0, n)
+        kvf[k0 + n // 2, 512] = 330.0
+    if q_dtype == synth.BF16:
+        q, q_scale = qf.to(torch.bfloat16), None
+    else:
+        q, q_scale = synth.quantize_fp8_per_tensor(qf)
+    if kv_dtype == synth.BF16:
+        kv, kv_scale = kvf.to(torch.bfloat16), None
+    elif kv_dtype == synth.FP8_E4M3:
+        kv, kv_scale = synth.quantize_fp8_per_tensor(kvf)
+    else:
+        kv, kv_scale = synth.quantize_mxfp4(kvf)
+    dev = lambda t: None if t is None else t.contiguous().cuda()  # noqa: E731
+    return synth.Inputs(q=dev(q), q_scale=dev(q_scale), kv=dev(kv), kv_scale=dev(kv_scale), qo_indptr=qo.cuda(),
+                        kv_indptr=kvp.cuda(), q_dtype=q_dtype, kv_dtype=kv_dtype)
+
+
+@pytest.mark.parametrize("q_dtype,kv_dtype,group", [
+    (synth.BF16, synth.FP8_E4M3, 0), (synth.BF16, synth.BF16, 0), (synth.BF16, synth.MXFP4, 0),
+    (synth.BF16, synth.FP8_E4M3, 2), (synth.FP8_E4M3, synth.FP8_E4M3, 2), (synth.BF16, synth.BF16, 2),
+    (synth.FP8_E4M3, synth.FP8_E4M3, 4)])
+def test_rising_scores_move_the_softmax_reference(q_dtype, kv_dtype, group):
+    # the kernels keep a lazy reference max per head (it moves only when a tile's max exceeds it
+    # by more than 3.5 in log2 units); the output must still be the softmax of the oracle
+    inp = _rising_inputs(q_dtype, kv_dtype, [3, 4], [2000, 1300], seed=91)
+    out = torch.full((inp.total_q, 16, 512), float("nan"), dtype=torch.bfloat16, device="cuda")
+    for ns in (1, 5):
+        ws = m.alloc_group_workspace(inp.batch, inp.total_q, inp.total_kv, inp.kv_dtype, group, num_splits=ns)
+        m.decode(inp.q, inp.kv, inp.kv_scale, inp.qo_indptr, inp.kv_indptr, out, inp.kv_dtype, workspace=ws,
+                 q_dtype=inp.q_dtype, q_scale=inp.q_scale, num_splits=ns, token_group=group)
+        torch.cuda.synchronize()
+        assert m.device_error(ws)[0] == m.MLA_OK
+        check(out.float().cpu().numpy(), oracle_ref(inp))
