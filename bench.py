@@ -527,7 +527,10 @@ def build_line(args, w, inp, kvb, splits, world, K, W, value, ms_step, achieved,
                        "parallelism": f"{world} independent replicas (weak scaling)"},
             "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                          "frac": round(achieved / peak, 4), "traffic": _ncu_traffic(w.name),
-                         "kernel": {2: "stage1_pair_kernel (tcgen05, token pairs) ",
+                         "kernel": {2: ("token pairs in " if w.kv_dtype == synth.BF16
+                                        else "stage1_duo_kernel (tcgen05, token pairs, softmax in two warp groups) "
+                                        if w.q_dtype == synth.FP8_E4M3
+                                        else "stage1_pair_kernel (tcgen05, token pairs) "),
                                     4: "stage1_quad_kernel (tcgen05, groups of four tokens) "}.get(args.token_group, "")
                                    + _kernel_name(synth, w),
                          "algorithmic_bytes": f"{kvb} per launch = {kvb // inp.total_kv} B x {inp.total_kv} KV rows",

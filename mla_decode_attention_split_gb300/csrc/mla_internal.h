@@ -76,6 +76,9 @@ cudaError_t launch_stage1_pair(int q_fmt, const Stage1Params& p, cudaStream_t st
 // fp8 KV and fp8 q, query tokens of a segment in groups of four sharing each KV tile (p.group = 4;
 // mla_stage1_quad.cu)
 cudaError_t launch_stage1_quad(int q_fmt, const Stage1Params& p, cudaStream_t stream);
+// fp8 KV and fp8 q, token pairs with the two tokens' softmax in two warp groups (p.group = 2;
+// mla_stage1_duo.cu)
+cudaError_t launch_stage1_duo(int q_fmt, const Stage1Params& p, cudaStream_t stream);
 cudaError_t launch_q_scale(const void* q, int64_t n, uint32_t* header, cudaStream_t stream);
 // paged KV: logical row offsets [batch+1] from the page table (mla_paged.cu)
 cudaError_t launch_paged_prepare(const int32_t* page_indptr, const int32_t* last_page_len, int32_t batch,

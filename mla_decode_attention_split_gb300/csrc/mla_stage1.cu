@@ -1,6 +1,7 @@
 // Stage 1 of split-K MLA decode: the dispatch to the tcgen05 kernels, one per
 // KV format (fp8: mla_stage1_tc.cu, bf16: mla_stage1_bf.cu, mxfp4:
-// mla_stage1_mx.cu; token groups: mla_stage1_pair.cu, mla_stage1_quad.cu).
+// mla_stage1_mx.cu; token groups: mla_stage1_pair.cu, mla_stage1_duo.cu,
+// mla_stage1_quad.cu).
 //
 // The method is the split-K flash-decoding stage 1 of kernelbot-amd-mixed-mla
 // -753817 (`mla_flash_decode_stage1`: 16 heads packed against the single KV
