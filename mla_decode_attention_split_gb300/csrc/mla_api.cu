@@ -236,7 +236,7 @@ mla_status_t decode_impl(const void* q, const void* kv, const void* kv_scale, co
     const bool q8 = q_fmt != mla::kQBf16;
     const cudaError_t le = (G == 4)                 ? mla::launch_stage1_quad(q_fmt, p, st)
                            : (G == 2 && fp8 && q8) ? mla::launch_stage1_duo(q_fmt, p, st)
-                           : (G == 2 && fp8)       ? mla::launch_stage1_pair(q_fmt, p, st)
+                           : (G == 2 && fp8)       ? mla::launch_stage1_pair(p, st)
                                                    : mla::launch_stage1(kv_dtype, q_fmt, p, st);
     if (le != cudaSuccess) return MLA_ERR_CUDA;
   } else if (cudaMemsetAsync(out, 0, static_cast<size_t>(total_q) * mla::kHeads * mla::kDv * 2, st) != cudaSuccess) {

@@ -70,15 +70,16 @@ cudaError_t launch_stage1_tc_mxfp4(int q_fmt, const Stage1Params& p, cudaStream_
 cudaError_t launch_dequant(const void* kv, const void* kv_scale, int kv_fmt, int32_t total_kv, int32_t row0,
                            int32_t nrows, float* out, cudaStream_t stream);
 bool stage1_supported(int kv_fmt, int q_fmt);
-// amax of bf16 q over n elements -> header word kHdrQScale = max(amax, 1e-12) / 448 (mla_qquant.cu)
-// fp8 KV, query tokens of a segment in pairs sharing each KV tile (p.group = 2; mla_stage1_pair.cu)
-cudaError_t launch_stage1_pair(int q_fmt, const Stage1Params& p, cudaStream_t stream);
+// fp8 KV and bf16 q, query tokens of a segment in pairs sharing each KV tile (p.group = 2;
+// mla_stage1_pair.cu)
+cudaError_t launch_stage1_pair(const Stage1Params& p, cudaStream_t stream);
 // fp8 KV and fp8 q, query tokens of a segment in groups of four sharing each KV tile (p.group = 4;
 // mla_stage1_quad.cu)
 cudaError_t launch_stage1_quad(int q_fmt, const Stage1Params& p, cudaStream_t stream);
 // fp8 KV and fp8 q, token pairs with the two tokens' softmax in two warp groups (p.group = 2;
 // mla_stage1_duo.cu)
 cudaError_t launch_stage1_duo(int q_fmt, const Stage1Params& p, cudaStream_t stream);
+// amax of bf16 q over n elements -> header word kHdrQScale = max(amax, 1e-12) / 448 (mla_qquant.cu)
 cudaError_t launch_q_scale(const void* q, int64_t n, uint32_t* header, cudaStream_t stream);
 // paged KV: logical row offsets [batch+1] from the page table (mla_paged.cu)
 cudaError_t launch_paged_prepare(const int32_t* page_indptr, const int32_t* last_page_len, int32_t batch,

@@ -1,5 +1,6 @@
-// Stage 1 for an fp8 (e4m3) KV cache with the query tokens of a segment taken
-// in pairs that share one pass over the KV rows (multi-token decode).
+// Stage 1 for an fp8 (e4m3) KV cache and bf16 q with the query tokens of a
+// segment taken in pairs that share one pass over the KV rows (multi-token
+// decode). fp8 q has its own kernel (mla_stage1_duo.cu).
 //
 // Method: as the single-token tensor-core kernel (split-K flash decoding as in
 // kernelbot-amd-mixed-mla-753817 `mla_flash_decode_stage1`, scores over all
@@ -18,13 +19,9 @@
 //    the 8 KB rope slot and an 8 KB P buffer;
 //  * a segment with an odd token count ends with a one-token group, which
 //    loads that token into both halves and writes only the first;
-//  * with fp8 q (a8w8, or q quantised in the call) q has no lo rows, so the
-//    two tokens' codes fill one 32-row Q buffer (Q.K^T at N = 32) and the
-//    rope operand moves into tensor memory (A read from TMEM): that frees
-//    room for a third 64 KB stage;
-//  * with bf16 q (two stages) the MMA warp issues each product from a
-//    polling loop as soon as its inputs are ready, so a P.V does not wait
-//    behind the landing of the next tile.
+//  * with two stages the MMA warp issues each product from a polling loop as
+//    soon as its inputs are ready, so a P.V does not wait behind the landing
+//    of the next tile.
 // A token's arithmetic (tiles, maxima, weights, accumulation) is the same as
 // in the single-token kernel, so with one partition per segment both give the
 // same bits.
@@ -41,22 +38,18 @@ constexpr int kThreads = 256;  // warp 0 TMA, warp 1 MMA, warps 2-5 softmax, 6-7
 constexpr int kStageBytes = kVBytes;
 constexpr int kPBytes2 = kTileRows * 64;  // [row group][A hi | A lo | B hi | B lo][8 rows][16 heads]
 
-// kQ8 false: bf16 q, Q = 64 rows (both tokens hi + lo), two stages, rope in
-// the shared-memory slot. kQ8 true: fp8 q, Q = 32 rows (both tokens' codes),
-// three stages, rope in tensor memory.
-template <bool kQ8>
-struct LT {
+// Q = 64 rows (both tokens hi + lo), two stages, rope in the shared-memory slot.
+struct L {
   static constexpr int kThreads = pair::kThreads;
-  static constexpr int kStages = kQ8 ? 3 : 2;
-  static constexpr int kQRows = kQ8 ? 32 : 64;
+  static constexpr int kStages = 2;
+  static constexpr int kQRows = 64;
   static constexpr int kQChunk = kQRows * 128;
-  static constexpr uint32_t kSCols = kQRows;           // S columns per buffer (Q.K^T N)
-  static constexpr uint32_t kTmemO = 2 * kSCols;       // O: 4 blocks x 64 columns
-  static constexpr uint32_t kTmemRope = kTmemO + 256;  // rope operand, 16 columns (kQ8)
+  static constexpr uint32_t kSCols = kQRows;      // S columns per buffer (Q.K^T N)
+  static constexpr uint32_t kTmemO = 2 * kSCols;  // O: 4 blocks x 64 columns
   static constexpr int kOffKv = 0;
   static constexpr int kOffQ = kOffKv + kStages * kStageBytes;
   static constexpr int kOffRope = kOffQ + 5 * kQChunk;
-  static constexpr int kOffP = kOffRope + (kQ8 ? 0 : kRopeBytes);
+  static constexpr int kOffP = kOffRope + kRopeBytes;
   static constexpr int kOffRedMax = kOffP + kPBytes2;                // [2 buffers][2 tokens][4 warps][16] f32
   static constexpr int kOffRedL = kOffRedMax + 2 * 2 * 4 * 16 * 4;   // [2 tokens][4][16] f32
   static constexpr int kOffAmax = kOffRedL + 2 * 4 * 16 * 4;         // [2 tokens][4 warps] u32
@@ -93,20 +86,16 @@ struct LT {
     mbar_init(cx.bar(kDrain), 1);
   }
 };
-template <bool kQ8>
-using CxT = Ctx<LT<kQ8>>;
-static_assert(LT<false>::kAlloc <= 227 * 1024 && LT<true>::kAlloc <= 227 * 1024, "shared memory budget");
-static_assert(LT<false>::kOffQ % 1024 == 0 && LT<false>::kOffRope % 1024 == 0 && LT<false>::kOffP % 1024 == 0 &&
-                  LT<true>::kOffQ % 1024 == 0 && LT<true>::kOffP % 1024 == 0,
-              "operand alignment");
-static_assert(LT<false>::kOffScan % 8 == 0 && LT<true>::kOffScan % 8 == 0, "scratch alignment");
-static_assert(LT<false>::kTmemO + 256 <= kTmemCols && LT<true>::kTmemRope + 16 <= kTmemCols, "tensor memory");
+using Cx = Ctx<L>;
+static_assert(L::kAlloc <= 227 * 1024, "shared memory budget");
+static_assert(L::kOffQ % 1024 == 0 && L::kOffRope % 1024 == 0 && L::kOffP % 1024 == 0, "operand alignment");
+static_assert(L::kOffScan % 8 == 0, "scratch alignment");
+static_assert(L::kTmemO + 256 <= kTmemCols, "tensor memory");
 
 // B operands.
 //   Q.K^T k-step ks: the Q rows of chunk ks / 4 (K-major, 128B swizzle).
-template <bool kQ8>
 __device__ __forceinline__ uint64_t qk_desc_b2(uint32_t qbuf, int ks) {
-  return smem_desc(qbuf + (ks >> 2) * LT<kQ8>::kQChunk + (ks & 3) * 32, 16, 1024, kLayoutSw128);
+  return smem_desc(qbuf + (ks >> 2) * L::kQChunk + (ks & 3) * 32, 16, 1024, kLayoutSw128);
 }
 //   P.V k-step ks (32 rows): P^T, 4 N-blocks of 16 columns 128 B apart, 8-row
 //   groups 512 B apart.
@@ -116,9 +105,7 @@ __device__ __forceinline__ uint64_t pv_desc_b2(uint32_t pbuf, int ks) {
 
 // Warp 0: the V dims of each tile, four 128-row x 128-byte boxes, into stage
 // (tile % stages) once the tile that used it last has been released by its P.V.
-template <bool kQ8>
-__device__ void producer(const CxT<kQ8>& cx, const CUtensorMap* map, PieceCursor cur, int lane) {
-  using L = LT<kQ8>;
+__device__ void producer(const Cx& cx, const CUtensorMap* map, PieceCursor cur, int lane) {
   constexpr int kStages = L::kStages;
   const uint64_t pol = policy_evict_first();
   Piece pc;
@@ -156,9 +143,7 @@ struct PendingPV {
   bool first, last, valid;
 };
 
-template <bool kQ8>
-__device__ bool issue_pv(const CxT<kQ8>& cx, const PendingPV& t) {
-  using L = LT<kQ8>;
+__device__ bool issue_pv(const Cx& cx, const PendingPV& t) {
   constexpr int kStages = L::kStages;
   constexpr uint32_t id_pv = umma_idesc(128, 64, 0, 0, true, true);
   if (!cx.wait(L::kPFull, t.n & 1u)) return false;
@@ -186,9 +171,7 @@ __device__ bool issue_pv(const CxT<kQ8>& cx, const PendingPV& t) {
 // the S buffer only after the Q.K^T that read it back, the rope slot only
 // after the Q.K^T that read it, and the next Q only after the last Q.K^T of
 // the piece.
-template <bool kQ8>
-__device__ void issue_qk_at(const CxT<kQ8>& cx, uint32_t n, const TileMeta& t) {
-  using L = LT<kQ8>;
+__device__ void issue_qk_at(const Cx& cx, uint32_t n, const TileMeta& t) {
   constexpr int kStages = L::kStages;
   constexpr uint32_t id_qk = umma_idesc(128, L::kSCols, 0, 0, false, false);
   const uint32_t s = n & 1u, st = n % kStages;
@@ -198,21 +181,15 @@ __device__ void issue_qk_at(const CxT<kQ8>& cx, uint32_t n, const TileMeta& t) {
   const uint32_t qbuf = cx.s + L::kOffQ;
 #pragma unroll
   for (int ks = 0; ks < 16; ++ks)  // the 512 V dims, from the stage
-    umma_e4m3(sbuf, qk_desc_a(stage, ks), qk_desc_b2<kQ8>(qbuf, ks), id_qk, ks > 0 ? 1u : 0u);
+    umma_e4m3(sbuf, qk_desc_a(stage, ks), qk_desc_b2(qbuf, ks), id_qk, ks > 0 ? 1u : 0u);
 #pragma unroll
-  for (int ks = 0; ks < 2; ++ks) {  // the 64 rope dims, from tensor memory or the rope slot
-    if constexpr (kQ8)
-      umma_e4m3_ta(sbuf, cx.tmem + L::kTmemRope + 8 * ks, qk_desc_b2<kQ8>(qbuf, 16 + ks), id_qk, 1u);
-    else
-      umma_e4m3(sbuf, rope_desc_a(cx.s + L::kOffRope, ks), qk_desc_b2<kQ8>(qbuf, 16 + ks), id_qk, 1u);
-  }
+  for (int ks = 0; ks < 2; ++ks)  // the 64 rope dims, from the rope slot
+    umma_e4m3(sbuf, rope_desc_a(cx.s + L::kOffRope, ks), qk_desc_b2(qbuf, 16 + ks), id_qk, 1u);
   umma_commit(cx.bar(L::kSFull + s));
   if (t.last) umma_commit(cx.bar(L::kQEmpty));
 }
 
-template <bool kQ8>
-__device__ void mma_issuer_polling(const CxT<kQ8>& cx, PieceCursor cur) {
-  using L = LT<kQ8>;
+__device__ void mma_issuer_polling(const Cx& cx, PieceCursor cur) {
   constexpr int kStages = L::kStages;
   const uint32_t n = static_cast<uint32_t>(count_tiles(cur));
   MetaTileWalker wq, wp;
@@ -230,7 +207,7 @@ __device__ void mma_issuer_polling(const CxT<kQ8>& cx, PieceCursor cur) {
       const TileMeta t = TileMeta::unpack(mp);
       if (!t.first || t.k == 0 || mbar_test_wait(cx.bar(L::kOEmpty), (t.k - 1) & 1u)) {
         // its own waits (P full, O free) pass at once
-        if (!issue_pv<kQ8>(cx, PendingPV{pi, t.k, t.first, t.last, true})) break;
+        if (!issue_pv(cx, PendingPV{pi, t.k, t.first, t.last, true})) break;
         ++pi;
         wp.next(row, mp);
         progressed = true;
@@ -241,7 +218,7 @@ __device__ void mma_issuer_polling(const CxT<kQ8>& cx, PieceCursor cur) {
         (qi < 2 || mbar_test_wait(cx.bar(L::kSEmpty + (qi & 1u)), ((qi - 2) >> 1) & 1u))) {
       const TileMeta t = TileMeta::unpack(mq);
       if (!t.first || mbar_test_wait(cx.bar(L::kQFull), t.k & 1u)) {
-        issue_qk_at<kQ8>(cx, qi, t);
+        issue_qk_at(cx, qi, t);
         ++qi;
         wq.next(row, mq);
         progressed = true;
@@ -257,59 +234,6 @@ __device__ void mma_issuer_polling(const CxT<kQ8>& cx, PieceCursor cur) {
       break;
     }
   }
-  // every issued tcgen05 operation completes before tensor memory is freed
-  umma_commit(cx.bar(L::kDrain));
-  mbar_wait_drain_tc(cx.bar(L::kDrain), 0);
-}
-
-template <bool kQ8>
-__device__ void mma_issuer(const CxT<kQ8>& cx, PieceCursor cur) {
-  using L = LT<kQ8>;
-  constexpr int kStages = L::kStages;
-  constexpr uint32_t id_qk = umma_idesc(128, L::kSCols, 0, 0, false, false);
-  Piece pc;
-  uint32_t n = 0, k = 0;
-  PendingPV pend{0, 0, false, false, false};
-  bool ok = true;
-  while (ok && cur.next(pc)) {
-    if (!cx.wait(L::kQFull, k & 1u)) break;
-    const uint32_t qbuf = cx.s + L::kOffQ;
-    for (int r0 = 0; r0 < pc.nrows; r0 += kTileRows) {
-      const uint32_t s = n & 1u, st = n % kStages;
-      if (!cx.wait(L::kKvFull + st, (n / kStages) & 1u)) {
-        ok = false;
-        break;
-      }
-      if (!cx.wait(L::kRopeFull, n & 1u) || (n >= 2 && !cx.wait(L::kSEmpty + s, ((n >> 1) - 1) & 1u))) {
-        ok = false;
-        break;
-      }
-      tc_fence_after();
-      const uint32_t stage = cx.s + L::kOffKv + st * kStageBytes;
-      const uint32_t sbuf = cx.tmem + L::kSCols * s;
-#pragma unroll
-      for (int ks = 0; ks < 16; ++ks)  // the 512 V dims, from the stage
-        umma_e4m3(sbuf, qk_desc_a(stage, ks), qk_desc_b2<kQ8>(qbuf, ks), id_qk, ks > 0 ? 1u : 0u);
-#pragma unroll
-      for (int ks = 0; ks < 2; ++ks) {  // the 64 rope dims, from tensor memory or the rope slot
-        if constexpr (kQ8)
-          umma_e4m3_ta(sbuf, cx.tmem + L::kTmemRope + 8 * ks, qk_desc_b2<kQ8>(qbuf, 16 + ks), id_qk, 1u);
-        else
-          umma_e4m3(sbuf, rope_desc_a(cx.s + L::kOffRope, ks), qk_desc_b2<kQ8>(qbuf, 16 + ks), id_qk, 1u);
-      }
-      umma_commit(cx.bar(L::kSFull + s));
-      const bool last = r0 + kTileRows >= pc.nrows;
-      if (last) umma_commit(cx.bar(L::kQEmpty));
-      if (pend.valid && !issue_pv<kQ8>(cx, pend)) {
-        ok = false;
-        break;
-      }
-      pend = PendingPV{n, k, r0 == 0, last, true};
-      ++n;
-    }
-    ++k;
-  }
-  if (ok && pend.valid) issue_pv<kQ8>(cx, pend);
   // every issued tcgen05 operation completes before tensor memory is freed
   umma_commit(cx.bar(L::kDrain));
   mbar_wait_drain_tc(cx.bar(L::kDrain), 0);
@@ -334,36 +258,23 @@ __device__ __forceinline__ void load_rope(const Stage1Params& p, TileWalker& rw,
   }
 }
 
-// One row's rope bytes into the rope operand (the shared-memory slot, or this
-// row's 16 tensor-memory columns) and the hand-off to the MMA warp.
-template <bool kQ8>
-__device__ __forceinline__ void store_rope(const CxT<kQ8>& cx, const SoftmaxCtx& sx, const uint4 (&r)[4]) {
-  using L = LT<kQ8>;
-  if constexpr (kQ8) {
-    const uint32_t w[16] = {r[0].x, r[0].y, r[0].z, r[0].w, r[1].x, r[1].y, r[1].z, r[1].w,
-                            r[2].x, r[2].y, r[2].z, r[2].w, r[3].x, r[3].y, r[3].z, r[3].w};
-    tmem_st16(cx.tmem + sx.lane_base + L::kTmemRope, w);
-    tmem_wait_st();
-    tc_fence_before();
-  } else {
-    put_rope_row(cx.g + L::kOffRope, sx.row, r);
-    fence_async_smem();
-  }
+// One row's rope bytes into the shared-memory rope slot and the hand-off to
+// the MMA warp.
+__device__ __forceinline__ void store_rope(const Cx& cx, const SoftmaxCtx& sx, const uint4 (&r)[4]) {
+  put_rope_row(cx.g + L::kOffRope, sx.row, r);
+  fence_async_smem();
   __syncwarp();
   if (sx.lane == 0) mbar_arrive(cx.bar(L::kRopeFull));
 }
 
-// The q of a piece's tokens: token A into Q rows 0-31 (fp8 q: 0-15), token B
-// into rows 32-63 (fp8 q: 16-31); a one-token group loads its token twice.
-// Returns false on abort.
-template <bool kQ8, int QF>
-__device__ bool setup_q2(const Stage1Params& p, const CxT<kQ8>& cx, SoftmaxCtx& sx, const Piece& pc, uint32_t kk,
+// The q of a piece's tokens: token A into Q rows 0-31 (hi, lo), token B into
+// rows 32-63; a one-token group loads its token twice. Returns false on abort.
+__device__ bool setup_q2(const Stage1Params& p, const Cx& cx, SoftmaxCtx& sx, const Piece& pc, uint32_t kk,
                          float kvsc, float& ca, float& cb) {
-  using L = LT<kQ8>;
   if (kk >= 1 && !cx.wait(L::kQEmpty, (kk - 1) & 1u)) return false;
-  ca = fill_q<L, QF, L::kQChunk, !kQ8>(p, cx, sx, pc.token, 0, kk, kvsc);
+  ca = fill_q<L, kQBf16, L::kQChunk, true>(p, cx, sx, pc.token, 0, kk, kvsc);
   if (ca < 0.f) return false;
-  cb = fill_q<L, QF, L::kQChunk, !kQ8>(p, cx, sx, pc.token + (pc.ntok > 1 ? 1 : 0), L::kQRows / 2, kk, kvsc);
+  cb = fill_q<L, kQBf16, L::kQChunk, true>(p, cx, sx, pc.token + (pc.ntok > 1 ? 1 : 0), L::kQRows / 2, kk, kvsc);
   if (cb < 0.f) return false;
   fence_async_smem();
   __syncwarp();
@@ -454,9 +365,7 @@ __device__ __forceinline__ bool softmax_tok(const float* rm, const float (&x)[16
   return grew;
 }
 
-template <int QF, bool kQ8>
-__device__ void softmax_role(const Stage1Params& p, const CxT<kQ8>& cx, PieceCursor cur, int warp, int lane) {
-  using L = LT<kQ8>;
+__device__ void softmax_role(const Stage1Params& p, const Cx& cx, PieceCursor cur, int warp, int lane) {
   constexpr int kStages = L::kStages;
   SoftmaxCtx sx;
   sx.lane = lane;
@@ -480,8 +389,8 @@ __device__ void softmax_role(const Stage1Params& p, const CxT<kQ8>& cx, PieceCur
   load_rope(p, rw, sx.row, rb0);
   load_rope(p, rw, sx.row, rb1);
   float ca, cb;  // the first Q operand while those rope rows are in flight
-  if (!setup_q2<kQ8, QF>(p, cx, sx, pc, 0, kvsc, ca, cb)) return;
-  store_rope<kQ8>(cx, sx, rb0);
+  if (!setup_q2(p, cx, sx, pc, 0, kvsc, ca, cb)) return;
+  store_rope(cx, sx, rb0);
   load_rope(p, rw, sx.row, rb0);
   uint32_t n = 0, k = 0;
   int tiles_left = count_tiles(cur) - 1;  // tiles of the CTA after the current one (for the rope slot)
@@ -500,10 +409,10 @@ __device__ void softmax_role(const Stage1Params& p, const CxT<kQ8>& cx, PieceCur
       // Q.K^T(n) is done: the rope slot takes tile n+1, its registers tile n+3
       if (tiles_left > 0) {
         if (n & 1u) {
-          store_rope<kQ8>(cx, sx, rb0);
+          store_rope(cx, sx, rb0);
           load_rope(p, rw, sx.row, rb0);
         } else {
-          store_rope<kQ8>(cx, sx, rb1);
+          store_rope(cx, sx, rb1);
           load_rope(p, rw, sx.row, rb1);
         }
       }
@@ -515,25 +424,18 @@ __device__ void softmax_role(const Stage1Params& p, const CxT<kQ8>& cx, PieceCur
         uint32_t sr[32];
         tmem_ld32(cx.tmem + sx.lane_base + L::kSCols * s, sr);
         tmem_wait_ld();
-        if constexpr (kQ8) {  // columns 0-15: token A, 16-31: token B (codes, no lo part)
+        // columns 0-31: token A hi, lo; 32-63: token B hi, lo
 #pragma unroll
-          for (int h = 0; h < 16; ++h) {
-            xa[h] = valid ? __uint_as_float(sr[h]) * ca : -INFINITY;
-            xb[h] = valid ? __uint_as_float(sr[16 + h]) * cb : -INFINITY;
-          }
-        } else {  // columns 0-31: token A hi, lo; 32-63: token B hi, lo
+        for (int h = 0; h < 16; ++h) {
+          const float v = (__uint_as_float(sr[h]) + __uint_as_float(sr[16 + h]) * (1.0f / kLoScale)) * ca;
+          xa[h] = valid ? v : -INFINITY;
+        }
+        tmem_ld32(cx.tmem + sx.lane_base + L::kSCols * s + 32, sr);
+        tmem_wait_ld();
 #pragma unroll
-          for (int h = 0; h < 16; ++h) {
-            const float v = (__uint_as_float(sr[h]) + __uint_as_float(sr[16 + h]) * (1.0f / kLoScale)) * ca;
-            xa[h] = valid ? v : -INFINITY;
-          }
-          tmem_ld32(cx.tmem + sx.lane_base + L::kSCols * s + 32, sr);
-          tmem_wait_ld();
-#pragma unroll
-          for (int h = 0; h < 16; ++h) {
-            const float v = (__uint_as_float(sr[h]) + __uint_as_float(sr[16 + h]) * (1.0f / kLoScale)) * cb;
-            xb[h] = valid ? v : -INFINITY;
-          }
+        for (int h = 0; h < 16; ++h) {
+          const float v = (__uint_as_float(sr[h]) + __uint_as_float(sr[16 + h]) * (1.0f / kLoScale)) * cb;
+          xb[h] = valid ? v : -INFINITY;
         }
       }
       tc_fence_before();
@@ -577,7 +479,7 @@ __device__ void softmax_role(const Stage1Params& p, const CxT<kQ8>& cx, PieceCur
 
     // the next piece's q goes in while this piece's last PV runs
     float ca_next = ca, cb_next = cb;
-    if (have_next && !setup_q2<kQ8, QF>(p, cx, sx, nxt, k + 1, kvsc, ca_next, cb_next)) return;
+    if (have_next && !setup_q2(p, cx, sx, nxt, k + 1, kvsc, ca_next, cb_next)) return;
     // l over the 128 rows, per head and token
     {
       const float wa = warp_reduce16<false>(la, lane);
@@ -614,56 +516,47 @@ __device__ void softmax_role(const Stage1Params& p, const CxT<kQ8>& cx, PieceCur
   }
 }
 
-template <int QF, bool kQ8>
 __global__ void __launch_bounds__(kThreads, 1) stage1_pair_kernel(const Stage1Params p,
                                                                   const __grid_constant__ CUtensorMap kvmap) {
   extern __shared__ uint8_t smem_raw[];
-  CxT<kQ8> cx;
+  Cx cx;
   PieceCursor cur;
   if (!cta_begin(p, cx, smem_raw, 1, cur)) return;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   cur.align8 = 1;  // the tiles of the single-token kernel
   if (warp == 0) {
-    producer<kQ8>(cx, &kvmap, cur, lane);
+    producer(cx, &kvmap, cur, lane);
   } else if (warp == 1) {
-    if (lane == 0) {
-      if constexpr (kQ8)
-        mma_issuer<kQ8>(cx, cur);
-      else
-        mma_issuer_polling<kQ8>(cx, cur);
-    }
+    if (lane == 0) mma_issuer_polling(cx, cur);
     __syncwarp();
   } else if (warp < 6) {
-    softmax_role<QF, kQ8>(p, cx, cur, warp, lane);
+    softmax_role(p, cx, cur, warp, lane);
   }
   cta_end(p, cx, 1);
 }
 
-template <int QF, bool kQ8>
-static cudaError_t launch_q(const Stage1Params& p, cudaStream_t stream) {
-  constexpr int kAlloc = LT<kQ8>::kAlloc;
+static cudaError_t launch(const Stage1Params& p, cudaStream_t stream) {
+  constexpr int kAlloc = L::kAlloc;
   static int configured_device = -1;
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (configured_device != dev) {
-    e = cudaFuncSetAttribute(stage1_pair_kernel<QF, kQ8>, cudaFuncAttributeMaxDynamicSharedMemorySize, kAlloc);
+    e = cudaFuncSetAttribute(stage1_pair_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kAlloc);
     if (e != cudaSuccess) return e;
     configured_device = dev;
   }
   CUtensorMap map;
   e = make_kv_map(&map, p.kv, p.total_kv, kTileRows);
   if (e != cudaSuccess) return e;
-  return launch_dependent(stage1_pair_kernel<QF, kQ8>, p.num_splits, kThreads, kAlloc, stream, p, map);
+  return launch_dependent(stage1_pair_kernel, p.num_splits, kThreads, kAlloc, stream, p, map);
 }
 
 }  // namespace pair
 }  // namespace tc
 
-cudaError_t launch_stage1_pair(int q_fmt, const Stage1Params& p, cudaStream_t stream) {
-  // fp8 q (given, or quantised in the call) takes the three-stage layout
-  if (q_fmt == kQBf16Quant) return tc::pair::launch_q<kQBf16Quant, true>(p, stream);
-  return q_fmt == kQBf16 ? tc::pair::launch_q<kQBf16, false>(p, stream) : tc::pair::launch_q<kQFp8, true>(p, stream);
+cudaError_t launch_stage1_pair(const Stage1Params& p, cudaStream_t stream) {
+  return tc::pair::launch(p, stream);
 }
 
 }  // namespace mla
