@@ -57,7 +57,8 @@ struct L {
   static constexpr int kOffP = kOffRope + kRopeBytes;
   static constexpr int kOffRedMax = kOffP + kPBytes;              // [2][4][16] f32
   static constexpr int kOffRedL = kOffRedMax + 2 * 4 * 16 * 4;    // [4][16] f32
-  static constexpr int kOffAmax = kOffRedL + 4 * 16 * 4;          // [4] u32
+  static constexpr int kOffFac = kOffRedL + 4 * 16 * 4;           // [piece % 2][16] f32: output factors
+  static constexpr int kOffAmax = kOffFac + 2 * 16 * 4;           // [4] u32
   static constexpr int kOffMList = kOffAmax + 16;                 // MergeList (128 B)
   static constexpr int kOffScan = kOffMList + 128;                 // 16 x i64
   static constexpr int kOffCRing = kOffScan + 16 * 8;             // score scale of piece k: f32 [4] + tag u32 [4]
@@ -97,6 +98,7 @@ struct L {
 };
 static_assert(L::kAlloc <= 227 * 1024, "shared memory budget");
 static_assert(L::kOffQ % 1024 == 0 && L::kOffRope % 1024 == 0, "operands need 1024-byte alignment");
+static_assert(L::kOffFac % 16 == 0, "factor buffer alignment");
 using Cx = Ctx<L>;
 
 // Warp 0: the V dims of each tile, four 128-row x 128-byte boxes, into stage
@@ -550,6 +552,39 @@ __device__ __forceinline__ float ring_scale(const Cx& cx, uint32_t k) {
   return ring_c[k & 3u];
 }
 
+// The epilogue of a piece, deferred: its O buffer is written out one 128-dim
+// block at a time in the idle time of the next piece's tiles (each softmax
+// pass ends waiting for the next scores), so the tensor core does not stop at
+// piece boundaries while the softmax warps store a whole partial.
+struct PendingOut {
+  Piece pc;
+  uint32_t k;      // the piece's index (its O buffer k % 2, factors k % 2)
+  int blocks;      // 128-dim blocks still to store (0: none pending)
+};
+
+// Stores one block of the pending piece; after the last one, frees its O
+// buffer and publishes and counts a split partial. Returns false on abort.
+__device__ __forceinline__ bool pending_block(const Stage1Params& p, const Cx& cx, SoftmaxCtx& sx, PendingOut& po) {
+  const int mb = 4 - po.blocks;
+  if (mb == 0) {
+    if (!cx.wait(L::kOFull + (po.k & 1u), (po.k >> 1) & 1u)) return false;
+    tc_fence_after();
+  }
+  const float4* fb = reinterpret_cast<const float4*>(cx.g + L::kOffFac + (po.k & 1u) * 64);
+  float f[16];
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    const float4 v = fb[q];
+    f[4 * q] = v.x; f[4 * q + 1] = v.y; f[4 * q + 2] = v.z; f[4 * q + 3] = v.w;
+  }
+  store_o_block(p, po.pc, cx.tmem + sx.lane_base + kTmemO + (po.k & 1u) * 128, sx.row, f, mb);
+  if (--po.blocks > 0) return true;
+  tc_fence_before();
+  __syncwarp();
+  if (sx.lane == 0) mbar_arrive(cx.bar(L::kOEmpty + (po.k & 1u)));
+  return po.pc.direct || finish_partial(p, cx, sx, po.pc);
+}
+
 template <int QF, bool kPaged>
 __device__ void softmax_role(const Stage1Params& p, const Cx& cx, PieceCursor cur, int warp, int lane) {
   SoftmaxCtx sx;
@@ -594,6 +629,8 @@ __device__ void softmax_role(const Stage1Params& p, const Cx& cx, PieceCursor cu
     rid = next_rope_id(p, rw, sx.row);
   }
   uint32_t n = 0, k = 0;
+  PendingOut po;
+  po.blocks = 0;
   int tiles_left = 0;  // tiles of the CTA after the current one (for the rope slot)
   {
     PieceCursor cnt = cur;
@@ -699,27 +736,37 @@ __device__ void softmax_role(const Stage1Params& p, const Cx& cx, PieceCursor cu
       __syncwarp();
       if (lane == 0) mbar_arrive(cx.bar(L::kPFull));
       ++n;
+      // a block of the previous piece's output while the next scores are computed
+      if (po.blocks > 0 && !pending_block(p, cx, sx, po)) return;
     }
 
     // (the next piece's Q operand comes from warps 6-7, qprep_role)
-    // l over the 128 rows, per head
+    while (po.blocks > 0)  // the previous piece's output, if this piece was too short to take it all
+      if (!pending_block(p, cx, sx, po)) return;
+    // l over the 128 rows, per head; the output factors go to the factor
+    // buffer of this piece (the last reader of that buffer, two pieces back,
+    // is done: its blocks were stored above)
     const float wl = warp_reduce16<false>(l, lane);
     if ((lane & 1) == 0) red_l[sx.wi * 16 + (lane >> 1)] = wl;
     if (!group_sync(cx, sx)) return;
-    float f[16];
+    {
+      float f[16];
 #pragma unroll
-    for (int h = 0; h < 16; ++h) {
-      const float L = red_l[h] + red_l[16 + h] + red_l[32 + h] + red_l[48 + h];
-      f[h] = kvsc / (kPScale * L);
-      if (!pc.direct && sx.row == h) p.part_lse[pc.slot * kHeads + h] = m[h] + fast_log2(L);
+      for (int h = 0; h < 16; ++h) {
+        const float L = red_l[h] + red_l[16 + h] + red_l[32 + h] + red_l[48 + h];
+        f[h] = kvsc / (kPScale * L);
+        if (!pc.direct && sx.row == h) p.part_lse[pc.slot * kHeads + h] = m[h] + fast_log2(L);
+      }
+      if (sx.wi == 0) store16(reinterpret_cast<float*>(cx.g + L::kOffFac) + (k & 1u) * 16, f, lane);
     }
-    if (!cx.wait(L::kOFull + (k & 1u), (k >> 1) & 1u)) return;
-    tc_fence_after();
-    store_o(p, pc, cx.tmem + sx.lane_base + kTmemO + (k & 1u) * 128, sx.row, f);
-    tc_fence_before();
-    __syncwarp();
-    if (lane == 0) mbar_arrive(cx.bar(L::kOEmpty + (k & 1u)));
-    if (!pc.direct && !finish_partial(p, cx, sx, pc)) return;
+    // every warp sees the factors before any stores a block
+    if (!group_sync(cx, sx)) return;
+    po.pc = pc;
+    po.k = k;
+    po.blocks = 4;
+    if (!have_next)  // the CTA's last piece: nothing left to overlap with
+      while (po.blocks > 0)
+        if (!pending_block(p, cx, sx, po)) return;
     pc = nxt;
     have = have_next;
     ++k;

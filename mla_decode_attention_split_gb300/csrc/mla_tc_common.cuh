@@ -451,6 +451,27 @@ __device__ __forceinline__ void rescale_o(uint32_t ob, const float (&alpha)[16])
   tmem_wait_st();
 }
 
+// One 128-dim block mb of a piece's epilogue: O (hi + lo/16 columns) times
+// f[head] to the bf16 output (a whole-run piece) or the fp32 partial slot.
+__device__ __forceinline__ void store_o_block(const Stage1Params& p, const Piece& pc, uint32_t ob, int row,
+                                              const float (&f)[16], int mb) {
+  uint32_t o[32];
+  tmem_ld32(ob + 32 * mb, o);
+  tmem_wait_ld();
+  const int dim = 128 * mb + row;
+  if (pc.direct) {
+    __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(p.out) + static_cast<int64_t>(pc.token) * kHeads * kDv + dim;
+#pragma unroll
+    for (int h = 0; h < 16; ++h)
+      dst[h * kDv] = __float2bfloat16_rn((__uint_as_float(o[h]) + __uint_as_float(o[16 + h]) * (1.0f / kLoScale)) * f[h]);
+  } else {
+    float* dst = p.part_o + pc.slot * kHeads * kDv + dim;
+#pragma unroll
+    for (int h = 0; h < 16; ++h)
+      dst[h * kDv] = (__uint_as_float(o[h]) + __uint_as_float(o[16 + h]) * (1.0f / kLoScale)) * f[h];
+  }
+}
+
 // Epilogue for one piece: O (hi + lo/16 columns) times f[head] to the bf16
 // output (a whole-run piece) or the fp32 partial slot.
 __device__ __forceinline__ void store_o(const Stage1Params& p, const Piece& pc, uint32_t ob, int row, const float (&f)[16]) {
