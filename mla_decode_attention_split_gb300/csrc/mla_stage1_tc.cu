@@ -552,10 +552,12 @@ __device__ __forceinline__ float ring_scale(const Cx& cx, uint32_t k) {
   return ring_c[k & 3u];
 }
 
-// The epilogue of a piece, deferred: its O buffer is written out one 128-dim
-// block at a time in the idle time of the next piece's tiles (each softmax
-// pass ends waiting for the next scores), so the tensor core does not stop at
-// piece boundaries while the softmax warps store a whole partial.
+// The epilogue of a piece, deferred (contiguous cache): its O buffer is
+// written out one 128-dim block at a time in the idle time of the next
+// piece's tiles (each softmax pass ends waiting for the next scores), so the
+// tensor core does not stop at piece boundaries while the softmax warps store
+// a whole partial. The paged kernel stores a piece's output at its end (its
+// loop has no registers to spare, and the larger code slowed it down).
 struct PendingOut {
   Piece pc;
   uint32_t k;      // the piece's index (its O buffer k % 2, factors k % 2)
@@ -737,19 +739,18 @@ __device__ void softmax_role(const Stage1Params& p, const Cx& cx, PieceCursor cu
       if (lane == 0) mbar_arrive(cx.bar(L::kPFull));
       ++n;
       // a block of the previous piece's output while the next scores are computed
-      if (po.blocks > 0 && !pending_block(p, cx, sx, po)) return;
+      // (contiguous cache; the paged loop has no registers to spare for it)
+      if constexpr (!kPaged) {
+        if (po.blocks > 0 && !pending_block(p, cx, sx, po)) return;
+      }
     }
 
     // (the next piece's Q operand comes from warps 6-7, qprep_role)
-    while (po.blocks > 0)  // the previous piece's output, if this piece was too short to take it all
-      if (!pending_block(p, cx, sx, po)) return;
-    // l over the 128 rows, per head; the output factors go to the factor
-    // buffer of this piece (the last reader of that buffer, two pieces back,
-    // is done: its blocks were stored above)
-    const float wl = warp_reduce16<false>(l, lane);
-    if ((lane & 1) == 0) red_l[sx.wi * 16 + (lane >> 1)] = wl;
-    if (!group_sync(cx, sx)) return;
-    {
+    if constexpr (kPaged) {
+      // l over the 128 rows, per head; the output at once
+      const float wl = warp_reduce16<false>(l, lane);
+      if ((lane & 1) == 0) red_l[sx.wi * 16 + (lane >> 1)] = wl;
+      if (!group_sync(cx, sx)) return;
       float f[16];
 #pragma unroll
       for (int h = 0; h < 16; ++h) {
@@ -757,16 +758,41 @@ __device__ void softmax_role(const Stage1Params& p, const Cx& cx, PieceCursor cu
         f[h] = kvsc / (kPScale * L);
         if (!pc.direct && sx.row == h) p.part_lse[pc.slot * kHeads + h] = m[h] + fast_log2(L);
       }
-      if (sx.wi == 0) store16(reinterpret_cast<float*>(cx.g + L::kOffFac) + (k & 1u) * 16, f, lane);
-    }
-    // every warp sees the factors before any stores a block
-    if (!group_sync(cx, sx)) return;
-    po.pc = pc;
-    po.k = k;
-    po.blocks = 4;
-    if (!have_next)  // the CTA's last piece: nothing left to overlap with
-      while (po.blocks > 0)
+      if (!cx.wait(L::kOFull + (k & 1u), (k >> 1) & 1u)) return;
+      tc_fence_after();
+      store_o(p, pc, cx.tmem + sx.lane_base + kTmemO + (k & 1u) * 128, sx.row, f);
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(cx.bar(L::kOEmpty + (k & 1u)));
+      if (!pc.direct && !finish_partial(p, cx, sx, pc)) return;
+    } else {
+      while (po.blocks > 0)  // the previous piece's output, if this piece was too short to take it all
         if (!pending_block(p, cx, sx, po)) return;
+      // l over the 128 rows, per head; the output factors go to the factor
+      // buffer of this piece (the last reader of that buffer, two pieces back,
+      // is done: its blocks were stored above)
+      const float wl = warp_reduce16<false>(l, lane);
+      if ((lane & 1) == 0) red_l[sx.wi * 16 + (lane >> 1)] = wl;
+      if (!group_sync(cx, sx)) return;
+      {
+        float f[16];
+#pragma unroll
+        for (int h = 0; h < 16; ++h) {
+          const float L = red_l[h] + red_l[16 + h] + red_l[32 + h] + red_l[48 + h];
+          f[h] = kvsc / (kPScale * L);
+          if (!pc.direct && sx.row == h) p.part_lse[pc.slot * kHeads + h] = m[h] + fast_log2(L);
+        }
+        if (sx.wi == 0) store16(reinterpret_cast<float*>(cx.g + L::kOffFac) + (k & 1u) * 16, f, lane);
+      }
+      // every warp sees the factors before any stores a block
+      if (!group_sync(cx, sx)) return;
+      po.pc = pc;
+      po.k = k;
+      po.blocks = 4;
+      if (!have_next)  // the CTA's last piece: nothing left to overlap with
+        while (po.blocks > 0)
+          if (!pending_block(p, cx, sx, po)) return;
+    }
     pc = nxt;
     have = have_next;
     ++k;
