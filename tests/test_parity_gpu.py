@@ -294,6 +294,23 @@ def test_many_token_runs_per_cta_ragged():
             check(run_decode(inp, num_splits=ns).float().cpu().numpy(), ref)
 
 
+@pytest.mark.parametrize("q_dtype", [synth.BF16, synth.FP8_E4M3])
+def test_piece_outputs_stored_during_the_next_piece(q_dtype):
+    # Runs of 8, 6, 1, 16, 3 and 12 tiles: a run's output is stored one block
+    # per tile of the next run (all of it when that run has four tiles or more,
+    # the rest at its end when it is shorter), the CTA's last run at once. With
+    # 2, 3 and 7 CTAs runs split at CTA boundaries, so partials are counted in
+    # the middle of the next run; repeated calls give the same bits.
+    lens = [1000, 700, 100, 2000, 300, 1500]
+    w = synth.Workload("deferred", len(lens), 1, 0, q_dtype, synth.FP8_E4M3, seed=49)
+    inp = synth.make_inputs(w, "cuda", kv_lens=lens)
+    ref = oracle_ref(inp)
+    for ns in (1, 2, 3, 7):
+        a = run_decode(inp, num_splits=ns)
+        assert torch.equal(a, run_decode(inp, num_splits=ns))
+        check(a.float().cpu().numpy(), ref)
+
+
 @pytest.mark.parametrize("amax_bits", [0x3F80, 0x3FFF, 0x42C9, 0x3B01])
 def test_in_call_q_quantisation_codes_over_every_mantissa(amax_bits):
     # Every bf16 value within 13 binades below the tensor maximum (both signs) is
