@@ -65,7 +65,7 @@ struct L {
   static constexpr int kOffQpAmax = kOffCRing + 32;               // [2] u32: the q-prep warps' maxima
   static constexpr int kOffBars = kOffQpAmax + 16;
   enum {
-    kKvFull = 0, kKvEmpty = 3, kSFull = 6, kSEmpty = 8, kRopeFull = 10, kPFull = 11, kPEmpty = 12, kQFull = 13,
+    kKvFull = 0, kKvEmpty = 3, kSFull = 6, kSEmpty = 8, kRopeFull = 10, kPFull = 11, /* 12 unused */ kQFull = 13,
     kQEmpty = 14, kOFull = 15, kOEmpty = 17, kGrp = 19, kDrain = 21, kMerge = 22, kQ0 = 23, kNumBars = 24
   };
   static constexpr int kMergeBytes = kStages * kStageBytes;  // the stages hold partials for the end-of-CTA merge
@@ -88,7 +88,6 @@ struct L {
     }
     mbar_init(cx.bar(kRopeFull), 4);
     mbar_init(cx.bar(kPFull), 4);
-    mbar_init(cx.bar(kPEmpty), 1);
     mbar_init(cx.bar(kQFull), 4);  // piece 0: the 4 softmax warps; later pieces: the 2 q-prep warps, 2 each
     mbar_init(cx.bar(kQEmpty), 1);
     mbar_init(cx.bar(kDrain), 1);
@@ -310,8 +309,8 @@ __device__ bool issue_pv(const Cx& cx, const PendingPV& t) {
     for (int ks = 0; ks < 4; ++ks) {
       umma_e4m3(obuf + 32 * mb, pv_desc_a(stage, mb, ks), pv_desc_b(pbuf, ks), id_pv, (ks > 0 || !t.first) ? 1u : 0u);
     }
+  // one commit frees the stage and, for the softmax warps, the P buffer
   umma_commit(cx.bar(L::kKvEmpty + (t.n % kStages)));
-  umma_commit(cx.bar(L::kPEmpty));
   if (t.last) umma_commit(cx.bar(L::kOFull + (t.k & 1u)));
   return true;
 }
@@ -717,8 +716,8 @@ __device__ void softmax_role(const Stage1Params& p, const Cx& cx, PieceCursor cu
         l[h] = l[h] * alpha[h] + pv[h];
         pv[h] *= kPScale;
       }
-      // single P buffer: P.V(n-1) must be done
-      if (n >= 1 && !cx.wait(L::kPEmpty, (n - 1) & 1u)) return;
+      // single P buffer: P.V(n-1) must be done (the commit that releases its stage)
+      if (n >= 1 && !cx.wait(L::kKvEmpty + (n - 1) % kStages, ((n - 1) / kStages) & 1u)) return;
       put_p_row(cx.g + L::kOffP, sx.row, pv);
       if (!valid) {
         // rows past the piece: zero their V bytes so P = 0 meets finite values
