@@ -58,7 +58,7 @@ struct L {
   static constexpr int kOffScan = kOffMList + 128;                   // 16 x i64
   static constexpr int kOffBars = kOffScan + 16 * 8;
   enum {
-    kKvFull = 0, kKvEmpty = 3, kSFull = 6, kSEmpty = 8, kRopeFull = 10, kPFull = 11, kPEmpty = 12, kQFull = 13,
+    kKvFull = 0, kKvEmpty = 3, kSFull = 6, kSEmpty = 8, kRopeFull = 10, kPFull = 11, /* 12 unused */ kQFull = 13,
     kQEmpty = 14, kOFull = 15, kOEmpty = 16, kGrp = 17 /* [half][2] */, kDrain = 21, kMerge = 22, kNumBars = 23
   };
   static constexpr int kMergeBytes = kStages * kStageBytes;  // the stages hold partials for the end-of-CTA merge
@@ -79,7 +79,6 @@ struct L {
     for (int i = 0; i < 4; ++i) mbar_init(cx.bar(kGrp + i), 4);
     mbar_init(cx.bar(kRopeFull), 4);  // token A's warps write the rope operand
     mbar_init(cx.bar(kPFull), 8);
-    mbar_init(cx.bar(kPEmpty), 1);
     mbar_init(cx.bar(kQFull), 8);
     mbar_init(cx.bar(kQEmpty), 1);
     mbar_init(cx.bar(kOFull), 1);
@@ -156,7 +155,6 @@ __device__ bool issue_pv(const Cx& cx, const PendingPV& t) {
       umma_e4m3(cx.tmem + kTmO + 64 * mb, pv_desc_a(stage, mb, ks), pv_desc_b_duo(pbuf, ks), id_pv,
                 (ks > 0 || !t.first) ? 1u : 0u);
   umma_commit(cx.bar(L::kKvEmpty + (t.n % kStages)));
-  umma_commit(cx.bar(L::kPEmpty));
   if (t.last) umma_commit(cx.bar(L::kOFull));
   return true;
 }
@@ -449,8 +447,8 @@ __device__ void softmax_role(const Stage1Params& p, const Cx& cx, PieceCursor cu
       if (!half_sync(cx, sx, hf)) return;
       float alpha[16], pv[16];
       const bool grew = softmax_tok(rm, x, m, l, alpha, pv);
-      // single P buffer: P.V(n-1) must be done
-      if (n >= 1 && !cx.wait(L::kPEmpty, (n - 1) & 1u)) return;
+      // single P buffer: P.V(n-1) must be done (the commit that releases its stage)
+      if (n >= 1 && !cx.wait(L::kKvEmpty + (n - 1) % kStages, ((n - 1) / kStages) & 1u)) return;
       put_p_tok(cx.g + L::kOffP, sx.row, hf, pv);
       if (!valid && hf == 0) {
         // rows outside the piece: zero their V bytes so P = 0 meets finite values

@@ -57,7 +57,7 @@ struct L {
   static constexpr int kOffScan = kOffMList + 128;                    // 16 x i64
   static constexpr int kOffBars = kOffScan + 16 * 8;
   enum {
-    kKvFull = 0, kKvEmpty = 3, kSFull = 6, kSEmpty = 8, kRopeFull = 10, kPFull = 11, kPEmpty = 12, kQFull = 13,
+    kKvFull = 0, kKvEmpty = 3, kSFull = 6, kSEmpty = 8, kRopeFull = 10, kPFull = 11, /* 12 unused */ kQFull = 13,
     kQEmpty = 14, kOFull = 15, kOEmpty = 16, kGrp = 17, kDrain = 19, kMerge = 20, kNumBars = 21
   };
   static constexpr int kMergeBytes = kStages * kStageBytes;  // the stages hold partials for the end-of-CTA merge
@@ -78,7 +78,6 @@ struct L {
     }
     mbar_init(cx.bar(kRopeFull), 4);
     mbar_init(cx.bar(kPFull), 4);
-    mbar_init(cx.bar(kPEmpty), 1);
     mbar_init(cx.bar(kQFull), 4);
     mbar_init(cx.bar(kQEmpty), 1);
     mbar_init(cx.bar(kOFull), 1);
@@ -158,7 +157,6 @@ __device__ bool issue_pv(const Cx& cx, const PendingPV& t) {
       umma_e4m3(cx.tmem + L::kTmemO + 64 * mb, pv_desc_a(stage, mb, ks), pv_desc_b2(pbuf, ks), id_pv,
                 (ks > 0 || !t.first) ? 1u : 0u);
   umma_commit(cx.bar(L::kKvEmpty + (t.n % kStages)));
-  umma_commit(cx.bar(L::kPEmpty));
   if (t.last) umma_commit(cx.bar(L::kOFull));
   return true;
 }
@@ -453,8 +451,8 @@ __device__ void softmax_role(const Stage1Params& p, const Cx& cx, PieceCursor cu
       float alpha_a[16], pa[16], alpha_b[16], pb[16];
       const bool grew_a = softmax_tok(rm, xa, ma, la, alpha_a, pa);
       const bool grew_b = softmax_tok(rm + 64, xb, mb, lb, alpha_b, pb);
-      // single P buffer: P.V(n-1) must be done
-      if (n >= 1 && !cx.wait(L::kPEmpty, (n - 1) & 1u)) return;
+      // single P buffer: P.V(n-1) must be done (the commit that releases its stage)
+      if (n >= 1 && !cx.wait(L::kKvEmpty + (n - 1) % L::kStages, ((n - 1) / L::kStages) & 1u)) return;
       put_p_row2(cx.g + L::kOffP, sx.row, pa, pb);
       if (!valid) {
         // rows outside the piece: zero their V bytes so P = 0 meets finite values
