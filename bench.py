@@ -24,6 +24,7 @@ import datetime
 import hashlib
 import json
 import os
+import re
 import statistics
 import subprocess
 import sys
@@ -38,11 +39,20 @@ STAGE1_SOURCES = ["mla_stage1_tc.cu", "mla_tc_common.cuh", "mla_tcgen05.cuh", "m
                   "mla_internal.h"]
 
 
+def _code_only(src: str) -> str:
+    """The source with its comments and blank space removed (the sources hold no string
+    literal with a comment marker in it), so that editing a comment does not invalidate a
+    capture taken on the same code."""
+    src = re.sub(r"/\*.*?\*/", " ", src, flags=re.S)
+    src = re.sub(r"//[^\n]*", " ", src)
+    return " ".join(src.split())
+
+
 def _stage1_source_sha() -> str:
     h = hashlib.sha256()
     for f in STAGE1_SOURCES:
-        with open(os.path.join(ROOT, "mla_decode_attention_split_gb300", "csrc", f), "rb") as fh:
-            h.update(fh.read())
+        with open(os.path.join(ROOT, "mla_decode_attention_split_gb300", "csrc", f), encoding="utf-8") as fh:
+            h.update(_code_only(fh.read()).encode())
     return h.hexdigest()[:16]
 
 

@@ -18,8 +18,8 @@
 //    values hi = e4m3(x), lo = e4m3(16 (x - hi)) stacked along N (N = 32:
 //    16 hi columns + 16 lo columns): a UMMA with N = 32 costs the same as one
 //    with N = 16, and hi + lo/16 carries x to 8 significant bits wherever hi is
-//    a normal number. The per-tensor kv scale, 2^-shift of q and 1/256 of P are
-//    applied to the fp32 results.
+//    a normal number. The per-tensor kv scale, 2^-shift of q and 1/kPScale of P
+//    are applied to the fp32 results.
 //  * Shared memory holds three 64 KB stages of the 512 V dims of 128-row tiles
 //    (four 128B-swizzled 128x128 TMA boxes each), so two tiles stream in while
 //    one is consumed. The 64 rope dims of each row (used by Q.K^T only) are
@@ -27,11 +27,13 @@
 //    into a single 8 KB slot as soon as the previous tile's Q.K^T is done.
 //  * Warp 0 issues the TMA loads (a paged cache: runs of consecutive pool
 //    rows by TMA, other rows by cp.async), warp 1 owns tensor memory and
-//    issues QK(n)
-//    then PV(n-1) so the tensor core overlaps the softmax of tile n, warps 2-5
+//    issues QK(n) then PV(n-1) so the tensor core overlaps the softmax of tile
+//    n; one commit after PV(n-1) frees its stage and the P buffer. Warps 2-5
 //    (one thread per tile row / tensor-memory lane) read S, reduce the per-head
 //    max across the 128 rows, write P into shared memory, rescale O in tensor
-//    memory only when some head's running max grew, and run the epilogue.
+//    memory only when some head's reference max moved (lazily, see kMaxSlack),
+//    and store each token run's output (a contiguous cache: one 128-dim block
+//    per tile of the next run). Warps 6-7 prepare the Q operand of later runs.
 //  * Every mbarrier wait is bounded; on a timeout the CTA stops issuing work,
 //    lets in-flight copies and MMAs finish, frees tensor memory and returns.
 #include <cuda.h>
